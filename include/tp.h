@@ -1,0 +1,235 @@
+/*
+ * tp.h — C ABI of the GB300 tensor-parallel Transformer-block library.
+ *
+ * A Megatron tensor-parallel (TP) group of degree n is simulated as n logical
+ * shards on ONE GPU.  The g all-reduce (after the row-parallel projection, in
+ * forward) and the f all-reduce (on the input gradient, in backward) become an
+ * on-device sum over the n shard partials, either accumulated in the GEMM's
+ * tensor-memory accumulator in shard order ("fused") or written out as n
+ * partial tensors and summed by a reduce kernel ("materialised").
+ *
+ * Pages cited (short name -> page title):
+ *   [Grasp-TP]   Grasp lesson 11, "张量并行线性层分片与前反向通信量计算"
+ *   [Troverld]   cnblogs post "ラブパラ" (survey of parallelisms)
+ *   [hjcheng-TP] hjcheng0602 blog post "TP"
+ *   [adu-TP]     "Tensor Parallelism张量并行（一）" (Megatron-LM paper notes)
+ *
+ * Conventions for every call:
+ *  - All tensors are dense, row-major, on the device unless stated.  Token
+ *    t = batch·s + position; activations are [T, h] with T = b·s.
+ *  - Weights are stored [out_features, in_features] (the Linear.weight
+ *    storage noted in [Grasp-TP] §1) and are passed UNSHARDED: shard i of a
+ *    column-parallel weight is its row block i, shard i of a row-parallel
+ *    weight is its column block i.  The library never copies weights.
+ *  - Element type is the descriptor's dtype for every tensor argument except
+ *    the fp32 statistics named as `float*`.  TP_BF16 computes with fp32
+ *    accumulation; TP_F32 computes in fp32 throughout.
+ *  - Inner dimensions (h, h_ffn/n, n_q·d, n_kv·d) must be multiples of 8 and
+ *    all device pointers 16-byte aligned; otherwise TP_ERR_SHAPE / TP_ERR_ARG.
+ *  - Ownership: the caller allocates every buffer.  The library allocates no
+ *    device or host memory on any compute path.  `ws` (saved activations,
+ *    written by a forward call and read by the matching backward call) must
+ *    stay alive and unmodified between the two.  Gradients are overwritten,
+ *    never accumulated into.
+ *  - Asynchrony: compute calls only enqueue work on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and never synchronise.
+ *  - Errors: argument, shape and workspace errors are returned before any
+ *    launch, with nothing enqueued.  A failed launch returns TP_ERR_CUDA.
+ *    Device-side waits are bounded; one that runs out records a device status
+ *    word that tp_device_status() returns as TP_ERR_DEVICE_TIMEOUT.  No C++
+ *    exception crosses this boundary.
+ */
+#ifndef TP_H_
+#define TP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_NULL = 1,            /* a required pointer is NULL */
+  TP_ERR_SHAPE = 2,           /* n∤h_ffn, n∤n_q, n∤n_kv, n_kv∤n_q, bad sizes */
+  TP_ERR_DTYPE = 3,           /* unknown dtype / activation / mode */
+  TP_ERR_WORKSPACE = 4,       /* ws or scratch smaller than the *_bytes query */
+  TP_ERR_UNSUPPORTED = 5,     /* valid but not implemented (e.g. d != 128) */
+  TP_ERR_CUDA = 6,            /* a CUDA runtime/driver call failed */
+  TP_ERR_DEVICE_TIMEOUT = 7,  /* a bounded device wait ran out */
+  TP_ERR_ARG = 8              /* misaligned pointer or other bad argument */
+} tp_status;
+
+typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;            /* δ = 4 or 2 */
+typedef enum { TP_GELU = 0, TP_SWIGLU = 1 } tp_act;
+typedef enum { TP_REDUCE_FUSED = 0, TP_REDUCE_MATERIALISED = 1 } tp_reduce_mode;
+typedef enum { TP_SCOPE_MLP = 0, TP_SCOPE_ATTN = 1, TP_SCOPE_LAYER = 2 } tp_scope;
+
+typedef void* tp_stream; /* cudaStream_t */
+
+/* ------------------------------------------------------------------ MLP --
+ * The Megatron MLP ([Grasp-TP] §3; [hjcheng-TP] MLP, TP forward/backward;
+ * [adu-TP] 张量并行应用于 MLP 和 Attention):
+ *   GeLU:   H_i = X·W1_iᵀ (+ b1_i),  A_i = GeLU(H_i) = H_i·Φ(H_i)
+ *   SwiGLU: G_i = X·Wg_iᵀ, U_i = X·Wu_iᵀ, A_i = SiLU(G_i) ⊙ U_i
+ *   Z^i = A_i·W2_iᵀ,  Z = Σ_{i=0}^{n-1} Z^i  (g),
+ *   Out = R + mask ⊙ (Z + b2) / (1 − p)   (b2 once, after the sum: [Grasp-TP] §3)
+ * W1 is [h_ffn, h] (GeLU) or [2·h_ffn, h] with gate rows [0, h_ffn) and up
+ * rows [h_ffn, 2·h_ffn) (SwiGLU); W2 is [h, h_ffn].  Rank i holds W1 rows
+ * (and, for SwiGLU, gate and up rows) [i·h_ffn/n, (i+1)·h_ffn/n) and the same
+ * columns of W2.
+ * Dropout (p > 0) keeps element (t, j) of the [T, h] output when the top 24
+ * bits of draw e = t·h + j of the splitmix64 stream seeded with `seed` are
+ * ≥ round(p·2^24); the mask is regenerated, not stored, in backward.
+ */
+typedef struct {
+  int64_t T;          /* tokens b·s (≥ 1) */
+  int64_t h;          /* hidden size */
+  int64_t h_ffn;      /* MLP intermediate size f */
+  int32_t n;          /* TP degree: number of logical shards (n | h_ffn) */
+  int32_t dtype;      /* tp_dtype */
+  int32_t act;        /* tp_act */
+  int32_t mode;       /* tp_reduce_mode for the g and f reductions */
+  float dropout_p;    /* in [0, 1) */
+  uint64_t seed;      /* dropout stream seed */
+} tp_mlp_desc;
+
+/* Bytes of `ws` for tp_mlp_fwd/tp_mlp_bwd: saved activations (H and A for
+ * GeLU; G, U and A for SwiGLU; each [T, h_ffn] in dtype) followed by the
+ * forward scratch (n partial [T, h] tensors in materialised mode). */
+size_t tp_mlp_workspace_bytes(const tp_mlp_desc* d);
+/* Bytes of `scratch` for tp_mlp_bwd: dZ [T, h] (when p > 0), the
+ * activation-input gradient ([T, h_ffn] or [T, 2·h_ffn]), partial input
+ * gradients (materialised mode) and fp32 column-sum partials. */
+size_t tp_mlp_bwd_scratch_bytes(const tp_mlp_desc* d);
+
+/* Forward.  b1, b2, R may be NULL (absent).  Out: [T, h]. */
+tp_status tp_mlp_fwd(const tp_mlp_desc* d, const void* X, const void* W1,
+                     const void* b1, const void* W2, const void* b2,
+                     const void* R, void* Out, void* ws, size_t ws_bytes,
+                     tp_stream stream);
+
+/* Backward ([hjcheng-TP] 单卡backward / TP backward; f of [adu-TP]):
+ *   dZ = dOut ⊙ mask/(1−p);  db2 = Σ_t dZ;  dW2 = dZᵀ·A;  dA = dZ·W2;
+ *   dH = dA ⊙ GeLU'(H)  (SwiGLU: dG = dA ⊙ U ⊙ SiLU'(G), dU = dA ⊙ SiLU(G));
+ *   db1 = Σ_t dH;  dW1 = dHᵀ·X;  dX = Σ_i dH_i·W1_i (f)  + dres.
+ * `ws` is the buffer the forward call filled.  db1, db2 and dres may be NULL
+ * (not computed / not added); dres is the gradient of a residual whose
+ * source is X itself (e.g. R = X), added once after the f sum. */
+tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut, const void* X,
+                     const void* W1, const void* W2, const void* ws,
+                     const void* dres, void* dX, void* dW1, void* db1,
+                     void* dW2, void* db2, void* scratch,
+                     size_t scratch_bytes, tp_stream stream);
+
+/* ------------------------------------------------------------ attention --
+ * Head-sharded causal GQA attention ([Grasp-TP] §4; [Troverld] §I.III;
+ * [hjcheng-TP] Attention):
+ *   Q = X·Wqᵀ [T, n_q·d], K = X·Wkᵀ, V = X·Wvᵀ [T, n_kv·d]
+ *   O_j = softmax(mask(Q_j K_kvᵀ/√d)) V_kv per batch element and q head j,
+ *         kv = ⌊j·n_kv/n_q⌋, causal mask key ≤ query within one sequence
+ *   Z^i = O_i·Wo_iᵀ, Z = Σ_i Z^i (g), Out = R + Z + bo (bo once)
+ * Wq [n_q·d, h], Wk/Wv [n_kv·d, h], Wo [h, n_q·d].  Rank i holds q heads
+ * [i·n_q/n, (i+1)·n_q/n) and kv heads [i·n_kv/n, (i+1)·n_kv/n); n must divide
+ * n_q and n_kv ([Grasp-TP] §4 GQA note) else TP_ERR_SHAPE.  d must be 128
+ * (else TP_ERR_UNSUPPORTED). */
+typedef struct {
+  int64_t b, s, h;
+  int32_t n_q, n_kv, d, n;
+  int32_t dtype;      /* TP_BF16 only (TP_F32 -> TP_ERR_UNSUPPORTED) */
+  int32_t causal;     /* 1 = causal mask, 0 = full */
+  int32_t mode;       /* tp_reduce_mode */
+} tp_attn_desc;
+
+/* ws: Q, K, V, O (dtype) and LSE [b, n_q, s] fp32 saved for backward, then
+ * the forward scratch (n partial [T, h] tensors in materialised mode). */
+size_t tp_attn_workspace_bytes(const tp_attn_desc* d);
+/* scratch: dO, dQ, dK, dV, D = rowsum(dO∘O) [b, n_q, s] fp32, partials and
+ * column-sum partials. */
+size_t tp_attn_bwd_scratch_bytes(const tp_attn_desc* d);
+
+tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X, const void* Wq,
+                      const void* Wk, const void* Wv, const void* Wo,
+                      const void* bo, const void* R, void* Out, void* ws,
+                      size_t ws_bytes, tp_stream stream);
+
+/* dWo = dOutᵀ·O; dO = dOut·Wo; flash backward → dQ, dK, dV (GQA groups
+ * summed); dWq = dQᵀ·X, dWk, dWv likewise; dX = Σ_i (dQ_i Wq_i + dK_i Wk_i
+ * + dV_i Wv_i) (f) + dres; dbo = Σ_t dOut.  dbo and dres may be NULL. */
+tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut, const void* X,
+                      const void* Wq, const void* Wk, const void* Wv,
+                      const void* Wo, const void* ws, const void* dres,
+                      void* dX, void* dWq, void* dWk, void* dWv, void* dWo,
+                      void* dbo, void* scratch, size_t scratch_bytes,
+                      tp_stream stream);
+
+/* -------------------------------------------------------------- RMSNorm --
+ * Token-wise RMSNorm on the replicated activation ([Troverld] §II.III fused
+ * norm; pre-norm reading of §III.III):  rstd_t = 1/sqrt(mean_j x_tj² + ε),
+ * y = x·rstd·γ.  rstd [T] fp32 is written for the backward call. */
+tp_status tp_rmsnorm_fwd(int64_t T, int64_t h, float eps, int32_t dtype,
+                         const void* x, const void* gamma, void* y,
+                         float* rstd, tp_stream stream);
+size_t tp_rmsnorm_bwd_scratch_bytes(int64_t T, int64_t h);
+/* dx = rstd·(dy⊙γ) − x·rstd³·Σ_j(dy⊙γ⊙x)_j/h + dres;  dγ = Σ_t dy⊙x·rstd.
+ * dres may be NULL.  dgamma is reduced deterministically through scratch. */
+tp_status tp_rmsnorm_bwd(int64_t T, int64_t h, float eps, int32_t dtype,
+                         const void* dy, const void* x, const void* gamma,
+                         const float* rstd, const void* dres, void* dx,
+                         void* dgamma, void* scratch, size_t scratch_bytes,
+                         tp_stream stream);
+
+/* ----------------------------------------------------------- accounting --
+ * Host-only, exact integer figures; no GPU needed.
+ * Communication ([Grasp-TP] §5; [Troverld] §II.II; [adu-TP] 通信开销): each
+ * reduction carries payload P = T·h·δ bytes; a ring all-reduce moves
+ * 2(n−1)·P/n per rank (kept as the reduced fraction num/den); [Troverld]'s
+ * figure drops (n−1)/n: 2·P.  MLP and attention: 1 reduction forward + 1
+ * backward; a layer: 2 + 2. */
+typedef struct {
+  uint64_t reductions_fwd, reductions_bwd;
+  uint64_t payload_bytes;               /* T·h·δ */
+  uint64_t ring_bytes_num, ring_bytes_den; /* 2(n−1)·P / n, reduced */
+  uint64_t page2_bytes;                 /* 2·P */
+  uint64_t total_payload;               /* (fwd+bwd)·P */
+  uint64_t total_ring_num;              /* (fwd+bwd)·ring, over ring_bytes_den */
+  uint64_t total_page2;                 /* (fwd+bwd)·2·P */
+} tp_comm_report;
+
+tp_status tp_comm_bytes(int32_t scope, int64_t T, int64_t h, int32_t n,
+                        int32_t dtype, tp_comm_report* out);
+
+/* Algorithmic FLOPs ([hjcheng-TP] 单卡forward/backward tables): GeLU MLP
+ * 4·T·h·f forward, SwiGLU 6·T·h·f; attention projections
+ * 2·T·h·(n_q+2·n_kv)·d + 2·T·n_q·d·h plus 4·b·n_q·d·C with C = s(s+1)/2
+ * (causal) or s² (full); backward = 2 × forward. */
+tp_status tp_mlp_flops(const tp_mlp_desc* d, uint64_t* fwd, uint64_t* bwd);
+tp_status tp_attn_flops(const tp_attn_desc* d, uint64_t* fwd, uint64_t* bwd);
+
+/* ------------------------------------------------------- GEMM building block
+ * C[M, N] = Σ_k A[m, k]·B[n, k] on the tensor cores (bf16 in, fp32
+ * accumulate, bf16 out) or on CUDA cores (fp32).  a_mn_major = 0: A is
+ * [M, K] row-major (lda ≥ K); 1: A is stored [K, M] (lda ≥ M).  Likewise B
+ * ([N, K] or [K, N]).  C is [M, N] with ldc.  The building block of every
+ * projection above, exported for tests. */
+tp_status tp_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K,
+                  const void* A, int64_t lda, int32_t a_mn_major,
+                  const void* B, int64_t ldb, int32_t b_mn_major, void* C,
+                  int64_t ldc, tp_stream stream);
+
+/* ----------------------------------------------------------------- status */
+/* Synchronises `stream`, returns and clears the device status word
+ * (TP_OK or TP_ERR_DEVICE_TIMEOUT), or TP_ERR_CUDA if the stream failed. */
+tp_status tp_device_status(tp_stream stream);
+const char* tp_status_string(tp_status s);
+/* Number of kernels this library has launched since load (host counter). */
+uint64_t tp_launch_count(void);
+/* SM count of the current device (0 if none); cached per device. */
+int32_t tp_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_H_ */
