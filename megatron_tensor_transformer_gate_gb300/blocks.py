@@ -1,0 +1,154 @@
+"""Convenience wrappers that own the workspaces of the TP block calls.
+
+PyTorch only provides device memory here; every step runs in ``libtp.so``.
+``TPMLP`` / ``TPAttention`` hold the forward workspace (saved activations)
+and the backward scratch for one shape; ``TPLayer`` composes the pre-norm
+layer  x1 = x + Attn(RMSNorm₁(x)),  out = x1 + MLP(RMSNorm₂(x1))  out of the
+library's RMSNorm, attention and MLP entry points, which gives the layer's
+four TP reductions (attention g and MLP g in forward, MLP f and attention f
+in backward).
+"""
+
+import torch
+
+from . import binding as B
+
+_TD = {B.F32: torch.float32, B.BF16: torch.bfloat16}
+
+
+def _buf(nbytes, device):
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+class TPMLP:
+    def __init__(self, T, h, h_ffn, n, *, dtype=B.BF16, act=B.GELU,
+                 mode=B.FUSED, dropout_p=0.0, seed=0, device="cuda"):
+        self.desc = B.mlp_desc(T, h, h_ffn, n, dtype, act, mode, dropout_p,
+                               seed)
+        self.T, self.h, self.f, self.act = T, h, h_ffn, act
+        self.dtype = _TD[dtype]
+        self.device = device
+        self.ws = _buf(B.mlp_workspace_bytes(self.desc), device)
+        self.scratch = _buf(B.mlp_bwd_scratch_bytes(self.desc), device)
+
+    def forward(self, X, W1, W2, b1=None, b2=None, R=None, out=None,
+                stream=None):
+        if out is None:
+            out = torch.empty((self.T, self.h), dtype=self.dtype,
+                              device=self.device)
+        B.mlp_fwd(self.desc, X, W1, W2, out, self.ws, b1=b1, b2=b2, R=R,
+                  stream=stream)
+        return out
+
+    def backward(self, dOut, X, W1, W2, dres=None, want_db1=False,
+                 want_db2=False, grads=None, stream=None):
+        g = grads if grads is not None else self.alloc_grads(W1, W2,
+                                                             want_db1,
+                                                             want_db2)
+        B.mlp_bwd(self.desc, dOut, X, W1, W2, self.ws, g["dX"], g["dW1"],
+                  g["dW2"], self.scratch, db1=g.get("db1"), db2=g.get("db2"),
+                  dres=dres, stream=stream)
+        return g
+
+    def alloc_grads(self, W1, W2, want_db1=False, want_db2=False):
+        kw = dict(dtype=self.dtype, device=self.device)
+        g = {"dX": torch.empty((self.T, self.h), **kw),
+             "dW1": torch.empty_like(W1), "dW2": torch.empty_like(W2)}
+        if want_db1:
+            g["db1"] = torch.empty((W1.shape[0],), **kw)
+        if want_db2:
+            g["db2"] = torch.empty((self.h,), **kw)
+        return g
+
+
+class TPAttention:
+    def __init__(self, b, s, h, n_q, n_kv, d, n, *, causal=True, mode=B.FUSED,
+                 device="cuda"):
+        self.desc = B.attn_desc(b, s, h, n_q, n_kv, d, n, B.BF16, causal,
+                                mode)
+        self.T, self.h = b * s, h
+        self.device = device
+        self.ws = _buf(B.attn_workspace_bytes(self.desc), device)
+        self.scratch = _buf(B.attn_bwd_scratch_bytes(self.desc), device)
+
+    def forward(self, X, Wq, Wk, Wv, Wo, bo=None, R=None, out=None,
+                stream=None):
+        if out is None:
+            out = torch.empty((self.T, self.h), dtype=torch.bfloat16,
+                              device=self.device)
+        B.attn_fwd(self.desc, X, Wq, Wk, Wv, Wo, out, self.ws, bo=bo, R=R,
+                   stream=stream)
+        return out
+
+    def backward(self, dOut, X, Wq, Wk, Wv, Wo, dres=None, want_dbo=False,
+                 grads=None, stream=None):
+        g = grads if grads is not None else self.alloc_grads(Wq, Wk, Wv, Wo,
+                                                             want_dbo)
+        B.attn_bwd(self.desc, dOut, X, Wq, Wk, Wv, Wo, self.ws, g["dX"],
+                   g["dWq"], g["dWk"], g["dWv"], g["dWo"], self.scratch,
+                   dbo=g.get("dbo"), dres=dres, stream=stream)
+        return g
+
+    def alloc_grads(self, Wq, Wk, Wv, Wo, want_dbo=False):
+        g = {"dX": torch.empty((self.T, self.h), dtype=torch.bfloat16,
+                               device=self.device),
+             "dWq": torch.empty_like(Wq), "dWk": torch.empty_like(Wk),
+             "dWv": torch.empty_like(Wv), "dWo": torch.empty_like(Wo)}
+        if want_dbo:
+            g["dbo"] = torch.empty((self.h,), dtype=torch.bfloat16,
+                                   device=self.device)
+        return g
+
+
+class TPLayer:
+    """Pre-norm layer: RMSNorm → attention (+x) → RMSNorm → SwiGLU MLP (+x1)."""
+
+    def __init__(self, b, s, h, h_ffn, n_q, n_kv, d, n, *, eps=1e-5,
+                 act=B.SWIGLU, mode=B.FUSED, device="cuda"):
+        T = b * s
+        self.T, self.h, self.eps = T, h, eps
+        self.device = device
+        self.attn = TPAttention(b, s, h, n_q, n_kv, d, n, mode=mode,
+                                device=device)
+        self.mlp = TPMLP(T, h, h_ffn, n, dtype=B.BF16, act=act, mode=mode,
+                         device=device)
+        kw = dict(dtype=torch.bfloat16, device=device)
+        self.xn1 = torch.empty((T, h), **kw)
+        self.x1 = torch.empty((T, h), **kw)
+        self.xn2 = torch.empty((T, h), **kw)
+        self.rstd1 = torch.empty((T,), dtype=torch.float32, device=device)
+        self.rstd2 = torch.empty((T,), dtype=torch.float32, device=device)
+        self.norm_scratch = _buf(B.rmsnorm_bwd_scratch_bytes(T, h), device)
+        self.dxn = torch.empty((T, h), **kw)
+        self.dx1 = torch.empty((T, h), **kw)
+
+    def forward(self, x, P, out=None, stream=None):
+        B.rmsnorm_fwd(x, P["g1"], self.xn1, self.rstd1, self.eps, stream)
+        self.attn.forward(self.xn1, P["Wq"], P["Wk"], P["Wv"], P["Wo"], R=x,
+                          out=self.x1, stream=stream)
+        B.rmsnorm_fwd(self.x1, P["g2"], self.xn2, self.rstd2, self.eps, stream)
+        return self.mlp.forward(self.xn2, P["W1"], P["W2"], R=self.x1,
+                                out=out, stream=stream)
+
+    def alloc_grads(self, P):
+        g = {k: torch.empty_like(P[k]) for k in ("g1", "Wq", "Wk", "Wv", "Wo",
+                                                 "g2", "W1", "W2")}
+        g = {"d" + k: v for k, v in g.items()}
+        g["dX"] = torch.empty((self.T, self.h), dtype=torch.bfloat16,
+                              device=self.device)
+        return g
+
+    def backward(self, dout, x, P, grads=None, stream=None):
+        g = grads if grads is not None else self.alloc_grads(P)
+        mg = {"dX": self.dxn, "dW1": g["dW1"], "dW2": g["dW2"]}
+        self.mlp.backward(dout, self.xn2, P["W1"], P["W2"], grads=mg,
+                          stream=stream)
+        B.rmsnorm_bwd(self.dxn, self.x1, P["g2"], self.rstd2, self.dx1,
+                      g["dg2"], self.norm_scratch, dres=dout, stream=stream)
+        ag = {"dX": self.dxn, "dWq": g["dWq"], "dWk": g["dWk"],
+              "dWv": g["dWv"], "dWo": g["dWo"]}
+        self.attn.backward(self.dx1, self.xn1, P["Wq"], P["Wk"], P["Wv"],
+                           P["Wo"], grads=ag, stream=stream)
+        B.rmsnorm_bwd(self.dxn, x, P["g1"], self.rstd1, g["dX"], g["dg1"],
+                      self.norm_scratch, dres=self.dx1, stream=stream)
+        return g

@@ -1,0 +1,790 @@
+// api.cu — the C ABI of include/tp.h: argument validation, workspace carving
+// and the launch sequence of each block.  Every compute call only enqueues
+// kernels on the caller's stream; nothing here allocates memory.
+#include <algorithm>
+#include <atomic>
+#include <cfenv>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tp.h"
+#include "attention.h"
+#include "common.cuh"
+#include "elementwise.h"
+#include "gemm.h"
+
+namespace tp {
+
+// Device status word (see common.cuh); kernels receive its address.
+__device__ unsigned g_status[4];
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+unsigned* g_status_ptr[kMaxDevices];
+std::mutex g_dev_mu;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return -1;
+  return dev;
+}
+
+}  // namespace
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n); }
+
+int device_sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_sms[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess ||
+        v <= 0)
+      v = 1;
+    g_sms[dev] = v;
+  }
+  return g_sms[dev];
+}
+
+unsigned* device_status_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+}  // namespace tp
+
+using namespace tp;
+
+namespace {
+
+// Sequential carving of a caller buffer into 256-byte aligned regions; with a
+// null base it only measures.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  void* take(size_t bytes) {
+    const size_t o = (off + 255) & ~size_t(255);
+    off = o + bytes;
+    return base ? base + o : nullptr;
+  }
+};
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+bool opt_aligned(const void* p) { return p == nullptr || aligned16(p); }
+
+size_t elem_size(int32_t dtype) { return dtype == TP_F32 ? 4 : 2; }
+
+tp_status cuda_status(int err) {
+  return err == 0 ? TP_OK : TP_ERR_CUDA;
+}
+
+DropoutSpec make_dropout(float p, uint64_t seed) {
+  DropoutSpec d;
+  if (p > 0.0f) {
+    d.enabled = 1;
+    // thr = round(p·2^24), ties to even (the current rounding mode)
+    d.thr = (uint32_t)std::nearbyint((double)p * 16777216.0);
+    d.scale = 1.0f / (1.0f - p);
+    d.seed = seed;
+  }
+  return d;
+}
+
+int run_gemm(const GemmProblem& g, tp_stream s) {
+  if (g.dtype == TP_BF16) return launch_gemm_tc(g, s, device_status_ptr());
+  return launch_gemm_simt(g, s);
+}
+
+template <typename F>
+tp_status guarded(F&& f) {
+  try {
+    return f();
+  } catch (...) {
+    return TP_ERR_CUDA;
+  }
+}
+
+// ------------------------------------------------------------------- MLP --
+tp_status check_mlp(const tp_mlp_desc* d) {
+  if (d == nullptr) return TP_ERR_NULL;
+  if (d->dtype != TP_F32 && d->dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (d->act != TP_GELU && d->act != TP_SWIGLU) return TP_ERR_DTYPE;
+  if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED)
+    return TP_ERR_DTYPE;
+  if (d->T < 1 || d->h < 8 || d->h_ffn < 8 || d->n < 1) return TP_ERR_SHAPE;
+  if (d->T > (1 << 30) || d->h > (1 << 20) || d->h_ffn > (1 << 24))
+    return TP_ERR_SHAPE;
+  if (d->h % 8 || d->h_ffn % d->n || (d->h_ffn / d->n) % 8) return TP_ERR_SHAPE;
+  if (!(d->dropout_p >= 0.0f && d->dropout_p < 1.0f)) return TP_ERR_ARG;
+  return TP_OK;
+}
+
+struct MlpFwdLayout {
+  void *h_or_g = nullptr, *u = nullptr, *a = nullptr, *partials = nullptr;
+  size_t bytes = 0;
+};
+
+MlpFwdLayout mlp_fwd_layout(const tp_mlp_desc* d, void* ws) {
+  MlpFwdLayout L;
+  Carver c(ws);
+  const size_t es = elem_size(d->dtype);
+  const size_t tf = (size_t)d->T * (size_t)d->h_ffn * es;
+  L.h_or_g = c.take(tf);
+  if (d->act == TP_SWIGLU) L.u = c.take(tf);
+  L.a = c.take(tf);
+  if (d->mode == TP_REDUCE_MATERIALISED)
+    L.partials = c.take((size_t)d->n * (size_t)d->T * (size_t)d->h * es);
+  L.bytes = c.off;
+  return L;
+}
+
+struct MlpBwdLayout {
+  void *dz = nullptr, *dh1 = nullptr, *partials = nullptr;
+  float* colsum = nullptr;
+  size_t bytes = 0;
+};
+
+MlpBwdLayout mlp_bwd_layout(const tp_mlp_desc* d, void* scratch) {
+  MlpBwdLayout L;
+  Carver c(scratch);
+  const size_t es = elem_size(d->dtype);
+  const int64_t fp = d->act == TP_SWIGLU ? 2 * d->h_ffn : d->h_ffn;
+  if (d->dropout_p > 0.0f) L.dz = c.take((size_t)d->T * (size_t)d->h * es);
+  L.dh1 = c.take((size_t)d->T * (size_t)fp * es);
+  if (d->mode == TP_REDUCE_MATERIALISED)
+    L.partials = c.take((size_t)d->n * (size_t)d->T * (size_t)d->h * es);
+  L.colsum = static_cast<float*>(c.take(std::max(
+      colsum_scratch_bytes(d->T, fp), colsum_scratch_bytes(d->T, d->h))));
+  L.bytes = c.off;
+  return L;
+}
+
+template <typename T>
+int reduce_t(int32_t dtype, const void* P, int n, int64_t rows, int64_t h,
+             const void* bias, const void* resid, void* out,
+             const DropoutSpec& dr, tp_stream s) {
+  (void)sizeof(T);
+  return dtype == TP_F32
+             ? reduce_partials<float>(P, n, rows, h, bias, resid, out, dr, s)
+             : reduce_partials<__nv_bfloat16>(P, n, rows, h, bias, resid, out,
+                                              dr, s);
+}
+
+int colsum_d(int32_t dtype, const void* X, int64_t rows, int64_t cols,
+             void* out, float* scratch, tp_stream s) {
+  return dtype == TP_F32
+             ? colsum<float>(X, rows, cols, cols, out, scratch, s)
+             : colsum<__nv_bfloat16>(X, rows, cols, cols, out, scratch, s);
+}
+
+GemmOperand op(const void* p, int64_t ld, int mn, int64_t rows) {
+  GemmOperand o;
+  o.ptr = p;
+  o.ld = ld;
+  o.mn_major = mn;
+  o.rows = rows;
+  return o;
+}
+
+}  // namespace
+
+extern "C" size_t tp_mlp_workspace_bytes(const tp_mlp_desc* d) {
+  if (check_mlp(d) != TP_OK) return 0;
+  return mlp_fwd_layout(d, nullptr).bytes;
+}
+
+extern "C" size_t tp_mlp_bwd_scratch_bytes(const tp_mlp_desc* d) {
+  if (check_mlp(d) != TP_OK) return 0;
+  return mlp_bwd_layout(d, nullptr).bytes;
+}
+
+extern "C" tp_status tp_mlp_fwd(const tp_mlp_desc* d, const void* X,
+                                const void* W1, const void* b1, const void* W2,
+                                const void* b2, const void* R, void* Out,
+                                void* ws, size_t ws_bytes, tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    tp_status st = check_mlp(d);
+    if (st != TP_OK) return st;
+    if (!X || !W1 || !W2 || !Out || !ws) return TP_ERR_NULL;
+    if (!aligned16(X) || !aligned16(W1) || !aligned16(W2) || !aligned16(Out) ||
+        !aligned16(ws) || !opt_aligned(b1) || !opt_aligned(b2) ||
+        !opt_aligned(R))
+      return TP_ERR_ARG;
+    if (d->act == TP_SWIGLU && b1 != nullptr) return TP_ERR_UNSUPPORTED;
+    const MlpFwdLayout L = mlp_fwd_layout(d, ws);
+    if (ws_bytes < L.bytes) return TP_ERR_WORKSPACE;
+    const int64_t T = d->T, h = d->h, f = d->h_ffn;
+    const int n = d->n;
+    const size_t es = elem_size(d->dtype);
+    const DropoutSpec dr = make_dropout(d->dropout_p, d->seed);
+
+    // column-parallel first projection + activation (shard-local)
+    GemmProblem g1;
+    g1.dtype = d->dtype;
+    g1.M = T;
+    g1.N = f;
+    g1.parts[0].a = op(X, h, 0, T);
+    g1.parts[0].b = op(W1, h, 0, f);
+    g1.parts[0].kseg = h;
+    if (d->act == TP_GELU) {
+      g1.epi.kind = EPI_GELU;
+      g1.epi.out = L.h_or_g;
+      g1.epi.out2 = L.a;
+      g1.epi.bias = b1;
+    } else {
+      g1.parts[0].b2 = op(static_cast<const char*>(W1) + (size_t)f * h * es, h,
+                          0, f);
+      g1.epi.kind = EPI_SWIGLU;
+      g1.epi.out = L.h_or_g;
+      g1.epi.out2 = L.u;
+      g1.epi.out3 = L.a;
+    }
+    g1.epi.ldo = f;
+    g1.epi.ldo2 = f;
+    int err = run_gemm(g1, stream);
+    if (err) return cuda_status(err);
+
+    // row-parallel second projection + g reduction + bias/dropout/residual
+    GemmProblem g2;
+    g2.dtype = d->dtype;
+    g2.M = T;
+    g2.N = h;
+    g2.parts[0].a = op(L.a, f, 0, T);
+    g2.parts[0].b = op(W2, f, 0, h);
+    if (d->mode == TP_REDUCE_FUSED) {
+      g2.parts[0].kseg = f;
+      g2.epi.kind = EPI_STORE;
+      g2.epi.out = Out;
+      g2.epi.ldo = h;
+      g2.epi.bias = b2;
+      g2.epi.resid = R;
+      g2.epi.ldr = h;
+      g2.epi.dropout = dr.enabled;
+      g2.epi.drop_thr = dr.thr;
+      g2.epi.drop_scale = dr.scale;
+      g2.epi.seed = dr.seed;
+      return cuda_status(run_gemm(g2, stream));
+    }
+    g2.parts[0].kseg = f / n;
+    g2.parts[0].nseg = n;
+    g2.parts[0].seg_z_stride = 1;
+    g2.nz = n;
+    g2.epi.kind = EPI_STORE;
+    g2.epi.out = L.partials;
+    g2.epi.ldo = h;
+    g2.epi.out_z_stride = T * h;
+    err = run_gemm(g2, stream);
+    if (err) return cuda_status(err);
+    return cuda_status(reduce_t<int>(d->dtype, L.partials, n, T, h, b2, R, Out,
+                                     dr, stream));
+  });
+}
+
+extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
+                                const void* X, const void* W1, const void* W2,
+                                const void* ws, const void* dres, void* dX,
+                                void* dW1, void* db1, void* dW2, void* db2,
+                                void* scratch, size_t scratch_bytes,
+                                tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    tp_status st = check_mlp(d);
+    if (st != TP_OK) return st;
+    if (!dOut || !X || !W1 || !W2 || !ws || !dX || !dW1 || !dW2 || !scratch)
+      return TP_ERR_NULL;
+    if (!aligned16(dOut) || !aligned16(X) || !aligned16(W1) ||
+        !aligned16(W2) || !aligned16(ws) || !aligned16(dX) ||
+        !aligned16(dW1) || !aligned16(dW2) || !aligned16(scratch) ||
+        !opt_aligned(dres) || !opt_aligned(db1) || !opt_aligned(db2))
+      return TP_ERR_ARG;
+    const MlpFwdLayout F = mlp_fwd_layout(d, const_cast<void*>(ws));
+    const MlpBwdLayout L = mlp_bwd_layout(d, scratch);
+    if (scratch_bytes < L.bytes) return TP_ERR_WORKSPACE;
+    const int64_t T = d->T, h = d->h, f = d->h_ffn;
+    const int n = d->n;
+    const bool swiglu = d->act == TP_SWIGLU;
+    const int64_t fp = swiglu ? 2 * f : f;
+    const size_t es = elem_size(d->dtype);
+    const DropoutSpec dr = make_dropout(d->dropout_p, d->seed);
+    int err = 0;
+
+    // dZ = dOut ⊙ mask/(1−p)
+    const void* dZ = dOut;
+    if (dr.enabled) {
+      err = d->dtype == TP_F32
+                ? dropout_bwd<float>(dOut, T * h, L.dz, dr, stream)
+                : dropout_bwd<__nv_bfloat16>(dOut, T * h, L.dz, dr, stream);
+      if (err) return cuda_status(err);
+      dZ = L.dz;
+    }
+    if (db2) {
+      err = colsum_d(d->dtype, dZ, T, h, db2, L.colsum, stream);
+      if (err) return cuda_status(err);
+    }
+    // dA = dZ·W2 (shard-local columns), through the activation
+    GemmProblem ga;
+    ga.dtype = d->dtype;
+    ga.M = T;
+    ga.N = f;
+    ga.parts[0].a = op(dZ, h, 0, T);
+    ga.parts[0].b = op(W2, f, 1, f);
+    ga.parts[0].kseg = h;
+    if (!swiglu) {
+      ga.epi.kind = EPI_DGELU;
+      ga.epi.out = L.dh1;
+      ga.epi.ldo = f;
+      ga.epi.aux1 = F.h_or_g;
+      ga.epi.ld_aux = f;
+    } else {
+      ga.epi.kind = EPI_DSWIGLU;
+      ga.epi.out = L.dh1;
+      ga.epi.out2 = static_cast<char*>(L.dh1) + (size_t)f * es;
+      ga.epi.ldo = 2 * f;
+      ga.epi.aux1 = F.h_or_g;
+      ga.epi.aux2 = F.u;
+      ga.epi.ld_aux = f;
+    }
+    err = run_gemm(ga, stream);
+    if (err) return cuda_status(err);
+    if (db1) {
+      err = colsum_d(d->dtype, L.dh1, T, fp, db1, L.colsum, stream);
+      if (err) return cuda_status(err);
+    }
+    // dW2 = dZᵀ·A  [h, f]
+    GemmProblem gw2;
+    gw2.dtype = d->dtype;
+    gw2.M = h;
+    gw2.N = f;
+    gw2.parts[0].a = op(dZ, h, 1, h);
+    gw2.parts[0].b = op(F.a, f, 1, f);
+    gw2.parts[0].kseg = T;
+    gw2.epi.kind = EPI_STORE;
+    gw2.epi.out = dW2;
+    gw2.epi.ldo = f;
+    err = run_gemm(gw2, stream);
+    if (err) return cuda_status(err);
+    // dW1 = dH1ᵀ·X  [fp, h]
+    GemmProblem gw1;
+    gw1.dtype = d->dtype;
+    gw1.M = fp;
+    gw1.N = h;
+    gw1.parts[0].a = op(L.dh1, fp, 1, fp);
+    gw1.parts[0].b = op(X, h, 1, h);
+    gw1.parts[0].kseg = T;
+    gw1.epi.kind = EPI_STORE;
+    gw1.epi.out = dW1;
+    gw1.epi.ldo = h;
+    err = run_gemm(gw1, stream);
+    if (err) return cuda_status(err);
+    // f: dX = Σ_i dH1_i·W1_i (+ dres)
+    GemmProblem gx;
+    gx.dtype = d->dtype;
+    gx.M = T;
+    gx.N = h;
+    gx.parts[0].a = op(L.dh1, fp, 0, T);
+    gx.parts[0].b = op(W1, h, 1, h);
+    gx.epi.kind = EPI_STORE;
+    gx.epi.ldo = h;
+    if (d->mode == TP_REDUCE_FUSED) {
+      gx.parts[0].kseg = fp;
+      gx.epi.out = dX;
+      gx.epi.resid = dres;
+      gx.epi.ldr = h;
+      return cuda_status(run_gemm(gx, stream));
+    }
+    const int64_t w = f / n;
+    gx.parts[0].kseg = w;
+    gx.parts[0].nseg = (int)(fp / w);
+    gx.parts[0].seg_z_stride = 1;
+    gx.parts[0].nsub = swiglu ? 2 : 1;
+    gx.parts[0].seg_sub_stride = n;
+    gx.nz = n;
+    gx.epi.out = L.partials;
+    gx.epi.out_z_stride = T * h;
+    err = run_gemm(gx, stream);
+    if (err) return cuda_status(err);
+    return cuda_status(reduce_t<int>(d->dtype, L.partials, n, T, h, nullptr,
+                                     dres, dX, DropoutSpec(), stream));
+  });
+}
+
+// ------------------------------------------------------------- attention --
+namespace {
+
+tp_status check_attn(const tp_attn_desc* d) {
+  if (d == nullptr) return TP_ERR_NULL;
+  if (d->dtype != TP_F32 && d->dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED)
+    return TP_ERR_DTYPE;
+  if (d->b < 1 || d->s < 1 || d->h < 8 || d->n_q < 1 || d->n_kv < 1 ||
+      d->d < 1 || d->n < 1)
+    return TP_ERR_SHAPE;
+  if (d->b * d->s > (1 << 30) || d->h > (1 << 20) || d->h % 8)
+    return TP_ERR_SHAPE;
+  // GQA groups and heads must split evenly over the n ranks
+  if (d->n_q % d->n_kv || d->n_q % d->n || d->n_kv % d->n) return TP_ERR_SHAPE;
+  if (d->dtype != TP_BF16 || d->d != 128) return TP_ERR_UNSUPPORTED;
+  return TP_OK;
+}
+
+struct AttnFwdLayout {
+  void *q = nullptr, *k = nullptr, *v = nullptr, *o = nullptr;
+  float* lse = nullptr;
+  void* partials = nullptr;
+  size_t bytes = 0;
+};
+
+AttnFwdLayout attn_fwd_layout(const tp_attn_desc* d, void* ws) {
+  AttnFwdLayout L;
+  Carver c(ws);
+  const size_t T = (size_t)d->b * (size_t)d->s;
+  const size_t qd = (size_t)d->n_q * d->d, kd = (size_t)d->n_kv * d->d;
+  L.q = c.take(T * qd * 2);
+  L.k = c.take(T * kd * 2);
+  L.v = c.take(T * kd * 2);
+  L.o = c.take(T * qd * 2);
+  L.lse = static_cast<float*>(c.take((size_t)d->b * d->n_q * d->s * 4));
+  if (d->mode == TP_REDUCE_MATERIALISED)
+    L.partials = c.take((size_t)d->n * T * (size_t)d->h * 2);
+  L.bytes = c.off;
+  return L;
+}
+
+struct AttnBwdLayout {
+  void *dO = nullptr, *dQ = nullptr, *dK = nullptr, *dV = nullptr;
+  float* D = nullptr;
+  void* partials = nullptr;
+  float* colsum = nullptr;
+  size_t bytes = 0;
+};
+
+AttnBwdLayout attn_bwd_layout(const tp_attn_desc* d, void* scratch) {
+  AttnBwdLayout L;
+  Carver c(scratch);
+  const size_t T = (size_t)d->b * (size_t)d->s;
+  const size_t qd = (size_t)d->n_q * d->d, kd = (size_t)d->n_kv * d->d;
+  L.dO = c.take(T * qd * 2);
+  L.dQ = c.take(T * qd * 2);
+  L.dK = c.take(T * kd * 2);
+  L.dV = c.take(T * kd * 2);
+  L.D = static_cast<float*>(c.take((size_t)d->b * d->n_q * d->s * 4));
+  if (d->mode == TP_REDUCE_MATERIALISED)
+    L.partials = c.take((size_t)d->n * T * (size_t)d->h * 2);
+  L.colsum = static_cast<float*>(c.take(colsum_scratch_bytes(T, d->h)));
+  L.bytes = c.off;
+  return L;
+}
+
+AttnShape attn_shape(const tp_attn_desc* d) {
+  AttnShape sh;
+  sh.b = d->b;
+  sh.s = d->s;
+  sh.nq = d->n_q;
+  sh.nkv = d->n_kv;
+  sh.d = d->d;
+  sh.causal = d->causal ? 1 : 0;
+  sh.scale = 1.0f / std::sqrt((float)d->d);
+  return sh;
+}
+
+GemmProblem proj(int64_t M, int64_t N, const GemmOperand& a,
+                 const GemmOperand& b, int64_t K, void* out, int64_t ldo) {
+  GemmProblem g;
+  g.dtype = TP_BF16;
+  g.M = M;
+  g.N = N;
+  g.parts[0].a = a;
+  g.parts[0].b = b;
+  g.parts[0].kseg = K;
+  g.epi.kind = EPI_STORE;
+  g.epi.out = out;
+  g.epi.ldo = ldo;
+  return g;
+}
+
+}  // namespace
+
+extern "C" size_t tp_attn_workspace_bytes(const tp_attn_desc* d) {
+  if (check_attn(d) != TP_OK) return 0;
+  return attn_fwd_layout(d, nullptr).bytes;
+}
+
+extern "C" size_t tp_attn_bwd_scratch_bytes(const tp_attn_desc* d) {
+  if (check_attn(d) != TP_OK) return 0;
+  return attn_bwd_layout(d, nullptr).bytes;
+}
+
+extern "C" tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X,
+                                 const void* Wq, const void* Wk,
+                                 const void* Wv, const void* Wo,
+                                 const void* bo, const void* R, void* Out,
+                                 void* ws, size_t ws_bytes, tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    tp_status st = check_attn(d);
+    if (st != TP_OK) return st;
+    if (!X || !Wq || !Wk || !Wv || !Wo || !Out || !ws) return TP_ERR_NULL;
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) ||
+        !aligned16(Wo) || !aligned16(Out) || !aligned16(ws) ||
+        !opt_aligned(bo) || !opt_aligned(R))
+      return TP_ERR_ARG;
+    const AttnFwdLayout L = attn_fwd_layout(d, ws);
+    if (ws_bytes < L.bytes) return TP_ERR_WORKSPACE;
+    const int64_t T = d->b * d->s, h = d->h;
+    const int64_t qd = (int64_t)d->n_q * d->d, kd = (int64_t)d->n_kv * d->d;
+    const int n = d->n;
+    // column-parallel Q, K, V projections (each rank's heads are a column
+    // block of the same output)
+    int err = run_gemm(proj(T, qd, op(X, h, 0, T), op(Wq, h, 0, qd), h, L.q, qd),
+                       stream);
+    if (!err)
+      err = run_gemm(proj(T, kd, op(X, h, 0, T), op(Wk, h, 0, kd), h, L.k, kd),
+                     stream);
+    if (!err)
+      err = run_gemm(proj(T, kd, op(X, h, 0, T), op(Wv, h, 0, kd), h, L.v, kd),
+                     stream);
+    if (err) return cuda_status(err);
+    err = flash_fwd(attn_shape(d), L.q, L.k, L.v, L.o, L.lse, stream);
+    if (err) return cuda_status(err);
+    // row-parallel output projection + g reduction + bias + residual
+    GemmProblem g = proj(T, h, op(L.o, qd, 0, T), op(Wo, qd, 0, h), qd, Out, h);
+    if (d->mode == TP_REDUCE_FUSED) {
+      g.epi.bias = bo;
+      g.epi.resid = R;
+      g.epi.ldr = h;
+      return cuda_status(run_gemm(g, stream));
+    }
+    g.parts[0].kseg = qd / n;
+    g.parts[0].nseg = n;
+    g.parts[0].seg_z_stride = 1;
+    g.nz = n;
+    g.epi.out = L.partials;
+    g.epi.out_z_stride = T * h;
+    err = run_gemm(g, stream);
+    if (err) return cuda_status(err);
+    return cuda_status(reduce_partials<__nv_bfloat16>(
+        L.partials, n, T, h, bo, R, Out, DropoutSpec(), stream));
+  });
+}
+
+extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
+                                 const void* X, const void* Wq, const void* Wk,
+                                 const void* Wv, const void* Wo,
+                                 const void* ws, const void* dres, void* dX,
+                                 void* dWq, void* dWk, void* dWv, void* dWo,
+                                 void* dbo, void* scratch,
+                                 size_t scratch_bytes, tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    tp_status st = check_attn(d);
+    if (st != TP_OK) return st;
+    if (!dOut || !X || !Wq || !Wk || !Wv || !Wo || !ws || !dX || !dWq ||
+        !dWk || !dWv || !dWo || !scratch)
+      return TP_ERR_NULL;
+    if (!aligned16(dOut) || !aligned16(X) || !aligned16(Wq) ||
+        !aligned16(Wk) || !aligned16(Wv) || !aligned16(Wo) || !aligned16(ws) ||
+        !aligned16(dX) || !aligned16(dWq) || !aligned16(dWk) ||
+        !aligned16(dWv) || !aligned16(dWo) || !aligned16(scratch) ||
+        !opt_aligned(dres) || !opt_aligned(dbo))
+      return TP_ERR_ARG;
+    const AttnFwdLayout F = attn_fwd_layout(d, const_cast<void*>(ws));
+    const AttnBwdLayout L = attn_bwd_layout(d, scratch);
+    if (scratch_bytes < L.bytes) return TP_ERR_WORKSPACE;
+    const int64_t T = d->b * d->s, h = d->h;
+    const int64_t qd = (int64_t)d->n_q * d->d, kd = (int64_t)d->n_kv * d->d;
+    const int n = d->n;
+    int err = 0;
+    if (dbo) {
+      err = colsum<__nv_bfloat16>(dOut, T, h, h, dbo, L.colsum, stream);
+      if (err) return cuda_status(err);
+    }
+    // dO = dOut·Wo (local), dWo = dOutᵀ·O
+    err = run_gemm(proj(T, qd, op(dOut, h, 0, T), op(Wo, qd, 1, qd), h, L.dO,
+                        qd),
+                   stream);
+    if (!err)
+      err = run_gemm(proj(h, qd, op(dOut, h, 1, h), op(F.o, qd, 1, qd), T, dWo,
+                          qd),
+                     stream);
+    if (err) return cuda_status(err);
+    err = flash_bwd(attn_shape(d), F.q, F.k, F.v, F.o, L.dO, F.lse, L.D,
+                    nullptr, L.dQ, L.dK, L.dV, stream);
+    if (err) return cuda_status(err);
+    err = run_gemm(proj(qd, h, op(L.dQ, qd, 1, qd), op(X, h, 1, h), T, dWq, h),
+                   stream);
+    if (!err)
+      err = run_gemm(proj(kd, h, op(L.dK, kd, 1, kd), op(X, h, 1, h), T, dWk,
+                          h),
+                     stream);
+    if (!err)
+      err = run_gemm(proj(kd, h, op(L.dV, kd, 1, kd), op(X, h, 1, h), T, dWv,
+                          h),
+                     stream);
+    if (err) return cuda_status(err);
+    // f: dX = Σ_i (dQ_i Wq_i + dK_i Wk_i + dV_i Wv_i) (+ dres)
+    GemmProblem g = proj(T, h, op(L.dQ, qd, 0, T), op(Wq, h, 1, h), qd, dX, h);
+    g.nparts = 3;
+    g.parts[1].a = op(L.dK, kd, 0, T);
+    g.parts[1].b = op(Wk, h, 1, h);
+    g.parts[1].kseg = kd;
+    g.parts[2].a = op(L.dV, kd, 0, T);
+    g.parts[2].b = op(Wv, h, 1, h);
+    g.parts[2].kseg = kd;
+    if (d->mode == TP_REDUCE_FUSED) {
+      g.epi.resid = dres;
+      g.epi.ldr = h;
+      return cuda_status(run_gemm(g, stream));
+    }
+    g.parts[0].kseg = qd / n;
+    g.parts[1].kseg = kd / n;
+    g.parts[2].kseg = kd / n;
+    for (int i = 0; i < 3; ++i) {
+      g.parts[i].nseg = n;
+      g.parts[i].seg_z_stride = 1;
+    }
+    g.nz = n;
+    g.epi.out = L.partials;
+    g.epi.out_z_stride = T * h;
+    err = run_gemm(g, stream);
+    if (err) return cuda_status(err);
+    return cuda_status(reduce_partials<__nv_bfloat16>(
+        L.partials, n, T, h, nullptr, dres, dX, DropoutSpec(), stream));
+  });
+}
+
+// -------------------------------------------------------------- RMSNorm --
+extern "C" tp_status tp_rmsnorm_fwd(int64_t T, int64_t h, float eps,
+                                    int32_t dtype, const void* x,
+                                    const void* gamma, void* y, float* rstd,
+                                    tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    if (dtype != TP_F32 && dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (T < 1 || h < 8 || h % 8 || h > 16384) return TP_ERR_SHAPE;
+    if (!x || !gamma || !y || !rstd) return TP_ERR_NULL;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(y) || !aligned16(rstd))
+      return TP_ERR_ARG;
+    const int err =
+        dtype == TP_F32
+            ? rmsnorm_fwd<float>(x, gamma, y, rstd, T, h, eps, stream)
+            : rmsnorm_fwd<__nv_bfloat16>(x, gamma, y, rstd, T, h, eps, stream);
+    return cuda_status(err);
+  });
+}
+
+extern "C" size_t tp_rmsnorm_bwd_scratch_bytes(int64_t T, int64_t h) {
+  if (T < 1 || h < 1) return 0;
+  return rmsnorm_bwd_scratch(T, h);
+}
+
+extern "C" tp_status tp_rmsnorm_bwd(int64_t T, int64_t h, float eps,
+                                    int32_t dtype, const void* dy,
+                                    const void* x, const void* gamma,
+                                    const float* rstd, const void* dres,
+                                    void* dx, void* dgamma, void* scratch,
+                                    size_t scratch_bytes, tp_stream stream) {
+  (void)eps;  // rstd carries ε from the forward call
+  return guarded([&]() -> tp_status {
+    if (dtype != TP_F32 && dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (T < 1 || h < 8 || h % 8 || h > 16384) return TP_ERR_SHAPE;
+    if (!dy || !x || !gamma || !rstd || !dx || !dgamma || !scratch)
+      return TP_ERR_NULL;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) ||
+        !aligned16(rstd) || !aligned16(dx) || !opt_aligned(dres) ||
+        !aligned16(scratch))
+      return TP_ERR_ARG;
+    if (scratch_bytes < rmsnorm_bwd_scratch(T, h)) return TP_ERR_WORKSPACE;
+    float* sc = static_cast<float*>(scratch);
+    const int err =
+        dtype == TP_F32
+            ? rmsnorm_bwd<float>(dy, x, gamma, rstd, dres, dx, dgamma, sc, T,
+                                 h, stream)
+            : rmsnorm_bwd<__nv_bfloat16>(dy, x, gamma, rstd, dres, dx, dgamma,
+                                         sc, T, h, stream);
+    return cuda_status(err);
+  });
+}
+
+// ----------------------------------------------------------------- GEMM --
+extern "C" tp_status tp_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K,
+                             const void* A, int64_t lda, int32_t a_mn_major,
+                             const void* B, int64_t ldb, int32_t b_mn_major,
+                             void* C, int64_t ldc, tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    if (dtype != TP_F32 && dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (M < 1 || N < 1 || K < 1 || M > (1 << 30) || N > (1 << 30))
+      return TP_ERR_SHAPE;
+    if (!A || !B || !C) return TP_ERR_NULL;
+    const int64_t q = dtype == TP_BF16 ? 8 : 4;
+    if (lda % q || ldb % q || ldc % q || K % q) return TP_ERR_SHAPE;
+    if (lda < (a_mn_major ? M : K) || ldb < (b_mn_major ? N : K) || ldc < N)
+      return TP_ERR_SHAPE;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return TP_ERR_ARG;
+    GemmProblem g;
+    g.dtype = dtype;
+    g.M = M;
+    g.N = N;
+    g.parts[0].a = op(A, lda, a_mn_major ? 1 : 0, M);
+    g.parts[0].b = op(B, ldb, b_mn_major ? 1 : 0, N);
+    g.parts[0].kseg = K;
+    g.epi.kind = EPI_STORE;
+    g.epi.out = C;
+    g.epi.ldo = ldc;
+    return cuda_status(run_gemm(g, stream));
+  });
+}
+
+// --------------------------------------------------------------- status --
+extern "C" tp_status tp_device_status(tp_stream stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TP_ERR_CUDA;
+  unsigned* p = device_status_ptr();
+  if (p == nullptr) return TP_ERR_CUDA;
+  unsigned h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, p, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return TP_ERR_CUDA;
+  if (h[0] != 0) {
+    const unsigned zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(p, zero, sizeof(zero), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return TP_ERR_CUDA;
+    return TP_ERR_DEVICE_TIMEOUT;
+  }
+  return TP_OK;
+}
+
+extern "C" const char* tp_status_string(tp_status s) {
+  switch (s) {
+    case TP_OK: return "ok";
+    case TP_ERR_NULL: return "required pointer is NULL";
+    case TP_ERR_SHAPE: return "invalid or non-divisible shape";
+    case TP_ERR_DTYPE: return "unknown dtype, activation, mode or scope";
+    case TP_ERR_WORKSPACE: return "workspace or scratch too small";
+    case TP_ERR_UNSUPPORTED: return "combination not supported";
+    case TP_ERR_CUDA: return "CUDA call failed";
+    case TP_ERR_DEVICE_TIMEOUT: return "a bounded device wait timed out";
+    case TP_ERR_ARG: return "misaligned pointer or bad argument";
+  }
+  return "unknown status";
+}
+
+extern "C" uint64_t tp_launch_count(void) { return g_launches.load(); }
+
+extern "C" int32_t tp_num_sms(void) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) return 0;
+  return device_sm_count();
+}

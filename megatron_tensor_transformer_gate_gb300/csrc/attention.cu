@@ -1,0 +1,734 @@
+// attention.cu — per-head causal GQA flash attention, forward and backward.
+//
+// The attention core of one rank's local heads ([Grasp-TP] §4: softmax is
+// per head over the sequence, so a head on one rank needs no communication;
+// [Troverld] §I.O FlashAttention: row-blocked forward with an online softmax
+// that keeps O(S) statistics, backward that recomputes QKᵀ).
+//
+// Head dim d = 128.  Tiles live in shared memory with 16-byte chunks XOR-
+// swizzled by (row mod 8) so that ldmatrix reads are bank-conflict free;
+// products use mma.sync m16n8k16 (bf16 in, fp32 accumulate).
+//   forward   block = 128 query rows of one (batch, q head), 8 warps × 16
+//             rows, K/V blocks of 64 keys double-buffered with cp.async.
+//   backward  (1) D = rowsum(dO ∘ O);  (2) dK/dV: block = 64 keys of one kv
+//             head, looping over the group's q heads and the query blocks at
+//             or after the keys (GQA sums stay inside the block);
+//             (3) dQ: block = 64 query rows, looping over key blocks.  Both
+//             recompute P from the saved log-sum-exp; no atomics, so reruns
+//             are bit-identical.
+#include <algorithm>
+
+#include "attention.h"
+#include "common.cuh"
+#include "gemm.h"
+
+namespace tp {
+namespace {
+
+constexpr int HD = 128;             // head dim
+constexpr int ROW_BYTES = HD * 2;   // 256 bytes per tile row
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  // byte offset of element (row, col) in a [rows][128] bf16 tile
+  return row * ROW_BYTES + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src,
+                                           bool valid) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Load rows [r0, r0+ROWS) of a head slice (row stride ld elements) into a
+// swizzled tile; rows ≥ limit are zero-filled.
+template <int ROWS, int NT>
+__device__ __forceinline__ void load_tile(uint32_t tile,
+                                          const __nv_bfloat16* base,
+                                          int64_t ld, int64_t r0,
+                                          int64_t limit) {
+  for (int idx = threadIdx.x; idx < ROWS * 16; idx += NT) {
+    const int r = idx >> 4, c = idx & 15;
+    const int64_t row = r0 + r;
+    const bool ok = row < limit;
+    const __nv_bfloat16* src = base + (ok ? row : 0) * ld + c * 8;
+    cp_async16(tile + swz(r, c * 8), src, ok);
+  }
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0,
+                                        uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0,
+                                          uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1,
+                                         uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// A fragments (16 rows × 16 k) of rows [row0, row0+16) of a tile, k-step kk.
+__device__ __forceinline__ void lda_frag(uint32_t tile, int row0, int kk,
+                                         uint32_t (&a)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int c = kk * 16 + (lane >> 4) * 8;
+  ldsm_x4(tile + swz(r, c), a[0], a[1], a[2], a[3]);
+}
+
+// B fragments for two n-tiles (rows n0..n0+15 of a tile stored [n][k]),
+// k-step kk: (b[0], b[1]) for n-tile n0, (b[2], b[3]) for n0+8.
+__device__ __forceinline__ void ldb_frag_nk(uint32_t tile, int n0, int kk,
+                                            uint32_t (&b)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int r = n0 + (lane & 7) + (lane >> 4) * 8;
+  const int c = kk * 16 + ((lane >> 3) & 1) * 8;
+  ldsm_x4(tile + swz(r, c), b[0], b[1], b[2], b[3]);
+}
+
+// B fragments for two n-tiles (columns d0..d0+15) of a tile stored [k][n]
+// (rows = k), k rows [k0, k0+16).
+__device__ __forceinline__ void ldb_frag_kn(uint32_t tile, int k0, int d0,
+                                            uint32_t (&b)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int r = k0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int c = d0 + (lane >> 4) * 8;
+  ldsm_x4_t(tile + swz(r, c), b[0], b[1], b[2], b[3]);
+}
+
+// ------------------------------------------------------------------ forward --
+constexpr int FQ = 128, FK = 64, FWARPS = 8, FTHREADS = FWARPS * 32;
+constexpr int FWD_SMEM = FQ * ROW_BYTES + 2 * 2 * FK * ROW_BYTES;  // 96 KB
+
+struct FwdArgs {
+  const __nv_bfloat16 *Q, *K, *V;
+  __nv_bfloat16* O;
+  float* LSE;
+  int64_t s;
+  int nq, nkv, causal;
+  float scale_log2;
+};
+
+__global__ void __launch_bounds__(FTHREADS, 1)
+    flash_fwd_kernel(const FwdArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const uint32_t sQ = smem_u32(sm);
+  const uint32_t sK0 = sQ + FQ * ROW_BYTES;
+  const uint32_t sV0 = sK0 + 2 * FK * ROW_BYTES;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int b = blockIdx.z, j = blockIdx.y;
+  const int nqb = gridDim.x;
+  const int64_t q0 = (int64_t)(nqb - 1 - blockIdx.x) * FQ;
+  const int kvh = j / (a.nq / a.nkv);
+  const int64_t ldq = (int64_t)a.nq * HD, ldk = (int64_t)a.nkv * HD;
+  const __nv_bfloat16* Qb = a.Q + (int64_t)b * a.s * ldq + j * HD;
+  const __nv_bfloat16* Kb = a.K + (int64_t)b * a.s * ldk + kvh * HD;
+  const __nv_bfloat16* Vb = a.V + (int64_t)b * a.s * ldk + kvh * HD;
+  const int64_t kv_end = a.causal ? min(a.s, q0 + (int64_t)FQ) : a.s;
+  const int nkb = (int)((kv_end + FK - 1) / FK);
+
+  load_tile<FQ, FTHREADS>(sQ, Qb, ldq, q0, a.s);
+  load_tile<FK, FTHREADS>(sK0, Kb, ldk, 0, a.s);
+  load_tile<FK, FTHREADS>(sV0, Vb, ldk, 0, a.s);
+  cp_commit();
+
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+  uint32_t qf[8][4];
+  const int64_t row_a = q0 + warp * 16 + g, row_b = row_a + 8;
+
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int st = kb & 1;
+    if (kb + 1 < nkb) {
+      const uint32_t nk = sK0 + (st ^ 1) * FK * ROW_BYTES;
+      const uint32_t nv = sV0 + (st ^ 1) * FK * ROW_BYTES;
+      load_tile<FK, FTHREADS>(nk, Kb, ldk, (int64_t)(kb + 1) * FK, a.s);
+      load_tile<FK, FTHREADS>(nv, Vb, ldk, (int64_t)(kb + 1) * FK, a.s);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    if (kb == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) lda_frag(sQ, warp * 16, kk, qf[kk]);
+    }
+    const uint32_t sK = sK0 + st * FK * ROW_BYTES;
+    const uint32_t sV = sV0 + st * FK * ROW_BYTES;
+    float sc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t bf[4];
+        ldb_frag_nk(sK, np * 16, kk, bf);
+        mma16816(sc[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], bf[0],
+                 bf[1]);
+        mma16816(sc[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
+                 bf[2], bf[3]);
+      }
+    }
+    // mask, scale, online softmax
+    const int64_t k0 = (int64_t)kb * FK;
+    const bool need_mask = (k0 + FK > a.s) || (a.causal && k0 + FK - 1 > q0);
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = sc[nt][e] * a.scale_log2;
+        if (need_mask) {
+          const int64_t key = k0 + nt * 8 + 2 * t + (e & 1);
+          const int64_t row = (e < 2) ? row_a : row_b;
+          if (key >= a.s || (a.causal && key > row)) v = -INFINITY;
+        }
+        sc[nt][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
+    }
+    float alpha[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float m_new = fmaxf(m_run[r], mx[r]);
+      alpha[r] = exp2f(m_run[r] - m_new);
+      m_run[r] = m_new;
+      l_run[r] *= alpha[r];
+    }
+    uint32_t pf[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const float p0 = exp2f(sc[nt][0] - m_run[0]);
+      const float p1 = exp2f(sc[nt][1] - m_run[0]);
+      const float p2 = exp2f(sc[nt][2] - m_run[1]);
+      const float p3 = exp2f(sc[nt][3] - m_run[1]);
+      l_run[0] += p0 + p1;
+      l_run[1] += p2 + p3;
+      pf[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
+      pf[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      o[i][0] *= alpha[0];
+      o[i][1] *= alpha[0];
+      o[i][2] *= alpha[1];
+      o[i][3] *= alpha[1];
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t bf[4];
+        ldb_frag_kn(sV, kk * 16, dp * 16, bf);
+        mma16816(o[2 * dp], pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3], bf[0],
+                 bf[1]);
+        mma16816(o[2 * dp + 1], pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3],
+                 bf[2], bf[3]);
+      }
+    }
+    __syncthreads();
+  }
+  // finalize: O /= l, LSE = ln(l) + m·ln2 (m in log2 units)
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+  }
+  const float inv0 = 1.0f / l_run[0], inv1 = 1.0f / l_run[1];
+  // stage this warp's 16 rows in the (now free) Q tile, then 16-byte stores
+  const int wr = warp * 16;
+#pragma unroll
+  for (int dt = 0; dt < 16; ++dt) {
+    const int col = dt * 8 + 2 * t;
+    *reinterpret_cast<uint32_t*>(sm + swz(wr + g, col)) =
+        pack_bf16x2(o[dt][0] * inv0, o[dt][1] * inv0);
+    *reinterpret_cast<uint32_t*>(sm + swz(wr + g + 8, col)) =
+        pack_bf16x2(o[dt][2] * inv1, o[dt][3] * inv1);
+  }
+  __syncwarp();
+  __nv_bfloat16* Ob = a.O + (int64_t)b * a.s * ldq + j * HD;
+  for (int idx = lane; idx < 16 * 16; idx += 32) {
+    const int r = idx >> 4, c = idx & 15;
+    const int64_t row = q0 + wr + r;
+    if (row < a.s)
+      *reinterpret_cast<uint4*>(Ob + row * ldq + c * 8) =
+          *reinterpret_cast<const uint4*>(sm + swz(wr + r, c * 8));
+  }
+  if (t == 0) {
+    float* L = a.LSE + ((int64_t)b * a.nq + j) * a.s;
+    if (row_a < a.s) L[row_a] = (m_run[0] + log2f(l_run[0])) * 0.69314718055994531f;
+    if (row_b < a.s) L[row_b] = (m_run[1] + log2f(l_run[1])) * 0.69314718055994531f;
+  }
+}
+
+// ------------------------------------------------------------ backward: D --
+__global__ void __launch_bounds__(256)
+    flash_bwd_dot_kernel(const __nv_bfloat16* __restrict__ O,
+                         const __nv_bfloat16* __restrict__ dO, float* D,
+                         int64_t rows, int nq, int64_t s) {
+  // one warp per (token, head); lane holds 4 consecutive elements
+  const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= rows * nq) return;
+  const int64_t tok = w / nq;
+  const int j = (int)(w - tok * nq);
+  const int64_t off = tok * nq * HD + j * HD + lane * 4;
+  const uint2 uo = *reinterpret_cast<const uint2*>(O + off);
+  const uint2 ud = *reinterpret_cast<const uint2*>(dO + off);
+  float2 o0 = unpack_bf16x2(uo.x), o1 = unpack_bf16x2(uo.y);
+  float2 d0 = unpack_bf16x2(ud.x), d1 = unpack_bf16x2(ud.y);
+  float acc = o0.x * d0.x + o0.y * d0.y + o1.x * d1.x + o1.y * d1.y;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    const int64_t b = tok / s, pos = tok - b * s;
+    D[(b * nq + j) * s + pos] = acc;
+  }
+}
+
+constexpr int BQ = 64, BKV = 64, BWARPS = 4, BTHREADS = BWARPS * 32;
+constexpr int BWD_SMEM = 6 * 64 * ROW_BYTES + 4 * 64 * 4;  // 96 KB + stats
+
+struct BwdArgs {
+  const __nv_bfloat16 *Q, *K, *V, *dO;
+  const float *LSE, *D;
+  __nv_bfloat16 *dQ, *dK, *dV;
+  int64_t s;
+  int nq, nkv, causal;
+  float scale, scale_log2;
+};
+
+// ------------------------------------------------------- backward: dK, dV --
+__global__ void __launch_bounds__(BTHREADS)
+    flash_bwd_dkdv_kernel(const BwdArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const uint32_t sK = smem_u32(sm);
+  const uint32_t sV = sK + BKV * ROW_BYTES;
+  const uint32_t sQ0 = sV + BKV * ROW_BYTES;            // 2 stages
+  const uint32_t sdO0 = sQ0 + 2 * BQ * ROW_BYTES;       // 2 stages
+  float* sStat = reinterpret_cast<float*>(sm + 6 * 64 * ROW_BYTES);  // [2][2][64]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int64_t k0 = (int64_t)blockIdx.x * BKV;
+  const int group = a.nq / a.nkv;
+  const int64_t ldq = (int64_t)a.nq * HD, ldk = (int64_t)a.nkv * HD;
+  const __nv_bfloat16* Kb = a.K + (int64_t)b * a.s * ldk + kvh * HD;
+  const __nv_bfloat16* Vb = a.V + (int64_t)b * a.s * ldk + kvh * HD;
+  const int nqb_total = (int)((a.s + BQ - 1) / BQ);
+  const int qb_first = a.causal ? (int)(k0 / BQ) : 0;
+  const int per_head = nqb_total - qb_first;
+  const int iters = per_head * group;
+
+  load_tile<BKV, BTHREADS>(sK, Kb, ldk, k0, a.s);
+  load_tile<BKV, BTHREADS>(sV, Vb, ldk, k0, a.s);
+
+  auto issue = [&](int it, int st) {
+    const int j = kvh * group + it / per_head;
+    const int64_t q0 = (int64_t)(qb_first + it % per_head) * BQ;
+    const __nv_bfloat16* Qb = a.Q + (int64_t)b * a.s * ldq + j * HD;
+    const __nv_bfloat16* dOb = a.dO + (int64_t)b * a.s * ldq + j * HD;
+    load_tile<BQ, BTHREADS>(sQ0 + st * BQ * ROW_BYTES, Qb, ldq, q0, a.s);
+    load_tile<BQ, BTHREADS>(sdO0 + st * BQ * ROW_BYTES, dOb, ldq, q0, a.s);
+  };
+  auto stats = [&](int it, int st) {
+    const int j = kvh * group + it / per_head;
+    const int64_t q0 = (int64_t)(qb_first + it % per_head) * BQ;
+    const int64_t base = ((int64_t)b * a.nq + j) * a.s;
+    for (int i = threadIdx.x; i < BQ; i += BTHREADS) {
+      const int64_t q = q0 + i;
+      sStat[(st * 2 + 0) * 64 + i] = q < a.s ? a.LSE[base + q] * LOG2E : 0.0f;
+      sStat[(st * 2 + 1) * 64 + i] = q < a.s ? a.D[base + q] : 0.0f;
+    }
+  };
+  if (iters > 0) issue(0, 0);
+  cp_commit();
+
+  float dk[16][4], dv[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dk[i][e] = dv[i][e] = 0.0f;
+  const int64_t key_a = k0 + warp * 16 + g, key_b = key_a + 8;
+
+  for (int it = 0; it < iters; ++it) {
+    const int st = it & 1;
+    stats(it, st);
+    if (it + 1 < iters) {
+      issue(it + 1, st ^ 1);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t sQ = sQ0 + st * BQ * ROW_BYTES;
+    const uint32_t sdO = sdO0 + st * BQ * ROW_BYTES;
+    const float* lse = sStat + (st * 2 + 0) * 64;
+    const float* dd = sStat + (st * 2 + 1) * 64;
+    const int64_t q0 = (int64_t)(qb_first + it % per_head) * BQ;
+
+    // Sᵀ = K Qᵀ  (16 keys × 64 queries per warp)
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t af[4];
+      lda_frag(sK, warp * 16, kk, af);
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t bf[4];
+        ldb_frag_nk(sQ, np * 16, kk, bf);
+        mma16816(s[2 * np], af[0], af[1], af[2], af[3], bf[0], bf[1]);
+        mma16816(s[2 * np + 1], af[0], af[1], af[2], af[3], bf[2], bf[3]);
+      }
+    }
+    // Pᵀ = exp(Sᵀ·scale − LSE[query]) with the mask
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int qi = nt * 8 + 2 * t + (e & 1);
+        const int64_t q = q0 + qi;
+        const int64_t key = (e < 2) ? key_a : key_b;
+        float p = exp2f(s[nt][e] * a.scale_log2 - lse[qi]);
+        if (q >= a.s || key >= a.s || (a.causal && key > q)) p = 0.0f;
+        s[nt][e] = p;
+      }
+    }
+    uint32_t pf[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      pf[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(s[nt][0], s[nt][1]);
+      pf[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(s[nt][2], s[nt][3]);
+    }
+    // dV += Pᵀ dO
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t bf[4];
+        ldb_frag_kn(sdO, kk * 16, dp * 16, bf);
+        mma16816(dv[2 * dp], pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3], bf[0],
+                 bf[1]);
+        mma16816(dv[2 * dp + 1], pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3],
+                 bf[2], bf[3]);
+      }
+    }
+    // dPᵀ = V dOᵀ
+    float dp_[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      dp_[i][0] = dp_[i][1] = dp_[i][2] = dp_[i][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t af[4];
+      lda_frag(sV, warp * 16, kk, af);
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t bf[4];
+        ldb_frag_nk(sdO, np * 16, kk, bf);
+        mma16816(dp_[2 * np], af[0], af[1], af[2], af[3], bf[0], bf[1]);
+        mma16816(dp_[2 * np + 1], af[0], af[1], af[2], af[3], bf[2], bf[3]);
+      }
+    }
+    // dSᵀ = Pᵀ ⊙ (dPᵀ − D[query])
+    uint32_t df[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int qi = nt * 8 + 2 * t + (e & 1);
+        v[e] = s[nt][e] * (dp_[nt][e] - dd[qi]);
+      }
+      df[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(v[0], v[1]);
+      df[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(v[2], v[3]);
+    }
+    // dK += dSᵀ Q
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+      for (int dq = 0; dq < 8; ++dq) {
+        uint32_t bf[4];
+        ldb_frag_kn(sQ, kk * 16, dq * 16, bf);
+        mma16816(dk[2 * dq], df[kk][0], df[kk][1], df[kk][2], df[kk][3], bf[0],
+                 bf[1]);
+        mma16816(dk[2 * dq + 1], df[kk][0], df[kk][1], df[kk][2], df[kk][3],
+                 bf[2], bf[3]);
+      }
+    }
+    __syncthreads();
+  }
+  // store dK·scale and dV through shared memory (reuse the Q stage 0 area)
+  uint8_t* stage = sm + 2 * 64 * ROW_BYTES + warp * 16 * ROW_BYTES;
+  uint8_t* stage2 = sm + 4 * 64 * ROW_BYTES + warp * 16 * ROW_BYTES;
+#pragma unroll
+  for (int dt = 0; dt < 16; ++dt) {
+    const int col = dt * 8 + 2 * t;
+    *reinterpret_cast<uint32_t*>(stage + swz(g, col)) =
+        pack_bf16x2(dk[dt][0] * a.scale, dk[dt][1] * a.scale);
+    *reinterpret_cast<uint32_t*>(stage + swz(g + 8, col)) =
+        pack_bf16x2(dk[dt][2] * a.scale, dk[dt][3] * a.scale);
+    *reinterpret_cast<uint32_t*>(stage2 + swz(g, col)) =
+        pack_bf16x2(dv[dt][0], dv[dt][1]);
+    *reinterpret_cast<uint32_t*>(stage2 + swz(g + 8, col)) =
+        pack_bf16x2(dv[dt][2], dv[dt][3]);
+  }
+  __syncwarp();
+  __nv_bfloat16* dKb = a.dK + (int64_t)b * a.s * ldk + kvh * HD;
+  __nv_bfloat16* dVb = a.dV + (int64_t)b * a.s * ldk + kvh * HD;
+  for (int idx = lane; idx < 16 * 16; idx += 32) {
+    const int r = idx >> 4, c = idx & 15;
+    const int64_t key = k0 + warp * 16 + r;
+    if (key < a.s) {
+      *reinterpret_cast<uint4*>(dKb + key * ldk + c * 8) =
+          *reinterpret_cast<const uint4*>(stage + swz(r, c * 8));
+      *reinterpret_cast<uint4*>(dVb + key * ldk + c * 8) =
+          *reinterpret_cast<const uint4*>(stage2 + swz(r, c * 8));
+    }
+  }
+}
+
+// --------------------------------------------------------------- backward: dQ --
+__global__ void __launch_bounds__(BTHREADS)
+    flash_bwd_dq_kernel(const BwdArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const uint32_t sQ = smem_u32(sm);
+  const uint32_t sdO = sQ + BQ * ROW_BYTES;
+  const uint32_t sK0 = sdO + BQ * ROW_BYTES;      // 2 stages
+  const uint32_t sV0 = sK0 + 2 * BKV * ROW_BYTES;  // 2 stages
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int b = blockIdx.z, j = blockIdx.y;
+  const int nqb = gridDim.x;
+  const int64_t q0 = (int64_t)(nqb - 1 - blockIdx.x) * BQ;
+  const int kvh = j / (a.nq / a.nkv);
+  const int64_t ldq = (int64_t)a.nq * HD, ldk = (int64_t)a.nkv * HD;
+  const __nv_bfloat16* Qb = a.Q + (int64_t)b * a.s * ldq + j * HD;
+  const __nv_bfloat16* dOb = a.dO + (int64_t)b * a.s * ldq + j * HD;
+  const __nv_bfloat16* Kb = a.K + (int64_t)b * a.s * ldk + kvh * HD;
+  const __nv_bfloat16* Vb = a.V + (int64_t)b * a.s * ldk + kvh * HD;
+  const int64_t kv_end = a.causal ? min(a.s, q0 + (int64_t)BQ) : a.s;
+  const int nkb = (int)((kv_end + BKV - 1) / BKV);
+
+  load_tile<BQ, BTHREADS>(sQ, Qb, ldq, q0, a.s);
+  load_tile<BQ, BTHREADS>(sdO, dOb, ldq, q0, a.s);
+  load_tile<BKV, BTHREADS>(sK0, Kb, ldk, 0, a.s);
+  load_tile<BKV, BTHREADS>(sV0, Vb, ldk, 0, a.s);
+  cp_commit();
+
+  const int64_t row_a = q0 + warp * 16 + g, row_b = row_a + 8;
+  const int64_t sbase = ((int64_t)b * a.nq + j) * a.s;
+  const float lse_a = row_a < a.s ? a.LSE[sbase + row_a] * LOG2E : 0.0f;
+  const float lse_b = row_b < a.s ? a.LSE[sbase + row_b] * LOG2E : 0.0f;
+  const float d_a = row_a < a.s ? a.D[sbase + row_a] : 0.0f;
+  const float d_b = row_b < a.s ? a.D[sbase + row_b] : 0.0f;
+
+  float dq[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.0f;
+  uint32_t qf[8][4], of[8][4];
+
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int st = kb & 1;
+    if (kb + 1 < nkb) {
+      load_tile<BKV, BTHREADS>(sK0 + (st ^ 1) * BKV * ROW_BYTES, Kb, ldk,
+                               (int64_t)(kb + 1) * BKV, a.s);
+      load_tile<BKV, BTHREADS>(sV0 + (st ^ 1) * BKV * ROW_BYTES, Vb, ldk,
+                               (int64_t)(kb + 1) * BKV, a.s);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    if (kb == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        lda_frag(sQ, warp * 16, kk, qf[kk]);
+        lda_frag(sdO, warp * 16, kk, of[kk]);
+      }
+    }
+    const uint32_t sK = sK0 + st * BKV * ROW_BYTES;
+    const uint32_t sV = sV0 + st * BKV * ROW_BYTES;
+    float s[8][4], dp_[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.0f;
+      dp_[i][0] = dp_[i][1] = dp_[i][2] = dp_[i][3] = 0.0f;
+    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t bf[4];
+        ldb_frag_nk(sK, np * 16, kk, bf);
+        mma16816(s[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], bf[0],
+                 bf[1]);
+        mma16816(s[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
+                 bf[2], bf[3]);
+        uint32_t vf[4];
+        ldb_frag_nk(sV, np * 16, kk, vf);
+        mma16816(dp_[2 * np], of[kk][0], of[kk][1], of[kk][2], of[kk][3],
+                 vf[0], vf[1]);
+        mma16816(dp_[2 * np + 1], of[kk][0], of[kk][1], of[kk][2], of[kk][3],
+                 vf[2], vf[3]);
+      }
+    }
+    const int64_t k0 = (int64_t)kb * BKV;
+    uint32_t df[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t key = k0 + nt * 8 + 2 * t + (e & 1);
+        const int64_t row = (e < 2) ? row_a : row_b;
+        float p = exp2f(s[nt][e] * a.scale_log2 - ((e < 2) ? lse_a : lse_b));
+        if (key >= a.s || row >= a.s || (a.causal && key > row)) p = 0.0f;
+        v[e] = p * (dp_[nt][e] - ((e < 2) ? d_a : d_b));
+      }
+      df[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(v[0], v[1]);
+      df[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(v[2], v[3]);
+    }
+    // dQ += dS K
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+      for (int dt = 0; dt < 8; ++dt) {
+        uint32_t bf[4];
+        ldb_frag_kn(sK, kk * 16, dt * 16, bf);
+        mma16816(dq[2 * dt], df[kk][0], df[kk][1], df[kk][2], df[kk][3], bf[0],
+                 bf[1]);
+        mma16816(dq[2 * dt + 1], df[kk][0], df[kk][1], df[kk][2], df[kk][3],
+                 bf[2], bf[3]);
+      }
+    }
+    __syncthreads();
+  }
+  // store dQ·scale via the Q tile
+  const int wr = warp * 16;
+#pragma unroll
+  for (int dt = 0; dt < 16; ++dt) {
+    const int col = dt * 8 + 2 * t;
+    *reinterpret_cast<uint32_t*>(sm + swz(wr + g, col)) =
+        pack_bf16x2(dq[dt][0] * a.scale, dq[dt][1] * a.scale);
+    *reinterpret_cast<uint32_t*>(sm + swz(wr + g + 8, col)) =
+        pack_bf16x2(dq[dt][2] * a.scale, dq[dt][3] * a.scale);
+  }
+  __syncwarp();
+  __nv_bfloat16* dQb = a.dQ + (int64_t)b * a.s * ldq + j * HD;
+  for (int idx = lane; idx < 16 * 16; idx += 32) {
+    const int r = idx >> 4, c = idx & 15;
+    const int64_t row = q0 + wr + r;
+    if (row < a.s)
+      *reinterpret_cast<uint4*>(dQb + row * ldq + c * 8) =
+          *reinterpret_cast<const uint4*>(sm + swz(wr + r, c * 8));
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              bytes);
+}
+
+}  // namespace
+
+int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
+              void* O, float* LSE, void* stream) {
+  if (sh.d != HD) return cudaErrorInvalidValue;
+  static cudaError_t e = set_smem(flash_fwd_kernel, FWD_SMEM);
+  if (e != cudaSuccess) return e;
+  FwdArgs a;
+  a.Q = static_cast<const __nv_bfloat16*>(Q);
+  a.K = static_cast<const __nv_bfloat16*>(K);
+  a.V = static_cast<const __nv_bfloat16*>(V);
+  a.O = static_cast<__nv_bfloat16*>(O);
+  a.LSE = LSE;
+  a.s = sh.s;
+  a.nq = sh.nq;
+  a.nkv = sh.nkv;
+  a.causal = sh.causal;
+  a.scale_log2 = sh.scale * LOG2E;
+  dim3 grid((unsigned)((sh.s + FQ - 1) / FQ), (unsigned)sh.nq, (unsigned)sh.b);
+  flash_fwd_kernel<<<grid, FTHREADS, FWD_SMEM,
+                     static_cast<cudaStream_t>(stream)>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
+              const void* O, const void* dO, const float* LSE, float* D,
+              float* /*dq_acc*/, void* dQ, void* dK, void* dV, void* stream) {
+  if (sh.d != HD) return cudaErrorInvalidValue;
+  static cudaError_t e1 = set_smem(flash_bwd_dkdv_kernel, BWD_SMEM);
+  static cudaError_t e2 = set_smem(flash_bwd_dq_kernel, BWD_SMEM);
+  if (e1 != cudaSuccess) return e1;
+  if (e2 != cudaSuccess) return e2;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t rows = sh.b * sh.s;
+  const int64_t warps = rows * sh.nq;
+  flash_bwd_dot_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(O),
+      static_cast<const __nv_bfloat16*>(dO), D, rows, sh.nq, sh.s);
+  BwdArgs a;
+  a.Q = static_cast<const __nv_bfloat16*>(Q);
+  a.K = static_cast<const __nv_bfloat16*>(K);
+  a.V = static_cast<const __nv_bfloat16*>(V);
+  a.dO = static_cast<const __nv_bfloat16*>(dO);
+  a.LSE = LSE;
+  a.D = D;
+  a.dQ = static_cast<__nv_bfloat16*>(dQ);
+  a.dK = static_cast<__nv_bfloat16*>(dK);
+  a.dV = static_cast<__nv_bfloat16*>(dV);
+  a.s = sh.s;
+  a.nq = sh.nq;
+  a.nkv = sh.nkv;
+  a.causal = sh.causal;
+  a.scale = sh.scale;
+  a.scale_log2 = sh.scale * LOG2E;
+  dim3 gkv((unsigned)((sh.s + BKV - 1) / BKV), (unsigned)sh.nkv,
+           (unsigned)sh.b);
+  flash_bwd_dkdv_kernel<<<gkv, BTHREADS, BWD_SMEM, s>>>(a);
+  dim3 gq((unsigned)((sh.s + BQ - 1) / BQ), (unsigned)sh.nq, (unsigned)sh.b);
+  flash_bwd_dq_kernel<<<gq, BTHREADS, BWD_SMEM, s>>>(a);
+  count_launch(3);
+  return cudaGetLastError();
+}
+
+}  // namespace tp

@@ -1,0 +1,26 @@
+// attention.h — launchers of the flash-attention kernels (attention.cu).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tp {
+
+// Causal (or full) GQA attention on per-head views of row-major Q [T, nq·d],
+// K/V [T, nkv·d], O [T, nq·d]; token t = batch·s + position; LSE [b, nq, s].
+struct AttnShape {
+  int64_t b, s;
+  int nq, nkv, d;
+  int causal;
+  float scale;  // 1/√d
+};
+
+int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
+              void* O, float* LSE, void* stream);
+// dQ, dK, dV (bf16, GQA groups summed); D [b, nq, s] fp32 scratch;
+// dq_acc [T, nq·d] fp32 scratch.
+int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
+              const void* O, const void* dO, const float* LSE, float* D,
+              float* dq_acc, void* dQ, void* dK, void* dV, void* stream);
+
+}  // namespace tp

@@ -1,0 +1,433 @@
+// elementwise.cu — HBM-bound kernels of the TP block.
+//
+//  * reduce_partials: the materialised g / f reduction
+//      out = resid + Dropout(Σ_{i=0}^{n−1} P_i + bias)
+//    summed in fp32 in shard order and rounded once ([Grasp-TP] §3: the full
+//    bias is added once, after the sum; [Troverld] §II.III: fused bias +
+//    dropout + residual add and fused all-reduce + residual add).
+//  * dropout_bwd: dZ = dOut ⊙ mask / (1 − p)  ([hjcheng-TP] 单卡backward).
+//  * column sums (bias gradients) in two deterministic stages.
+//  * RMSNorm forward / backward ([Troverld] §II.III fused norm).
+// All loads and stores are 16-byte vectors; grids are a multiple of the SM
+// count and grid-stride.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "elementwise.h"
+#include "gemm.h"
+
+namespace tp {
+namespace {
+
+template <typename T>
+struct Vec;  // 16-byte vector of T
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const float* p, float* v) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  }
+  __device__ static void store(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(const __nv_bfloat16* p, float* v) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y),
+           c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
+  }
+  __device__ static void store(__nv_bfloat16* p, const float* v) {
+    uint4 u;
+    u.x = pack_bf16x2(v[0], v[1]);
+    u.y = pack_bf16x2(v[2], v[3]);
+    u.z = pack_bf16x2(v[4], v[5]);
+    u.w = pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// ------------------------------------------------------- reduce_partials --
+template <typename T>
+__global__ void __launch_bounds__(256)
+    reduce_partials_kernel(const T* __restrict__ P, int n, int64_t count,
+                           int64_t h, const T* __restrict__ bias,
+                           const T* __restrict__ resid, T* __restrict__ out,
+                           int dropout, uint32_t thr, float scale,
+                           uint64_t seed) {
+  constexpr int V = Vec<T>::N;
+  const int64_t nvec = count / V;
+  for (int64_t iv = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; iv < nvec;
+       iv += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = iv * V;
+    float acc[V], v[V];
+    Vec<T>::load(P + i, acc);
+    for (int s = 1; s < n; ++s) {
+      Vec<T>::load(P + (int64_t)s * count + i, v);
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] += v[q];
+    }
+    if (bias != nullptr) {
+      Vec<T>::load(bias + (i % h), v);
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] += v[q];
+    }
+    if (dropout) {
+#pragma unroll
+      for (int q = 0; q < V; ++q)
+        acc[q] = dropout_keep(seed, (uint64_t)(i + q), thr) ? acc[q] * scale
+                                                            : 0.0f;
+    }
+    if (resid != nullptr) {
+      Vec<T>::load(resid + i, v);
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] += v[q];
+    }
+    Vec<T>::store(out + i, acc);
+  }
+}
+
+// ----------------------------------------------------------- dropout_bwd --
+template <typename T>
+__global__ void __launch_bounds__(256)
+    dropout_bwd_kernel(const T* __restrict__ dout, int64_t count,
+                       T* __restrict__ dz, uint32_t thr, float scale,
+                       uint64_t seed) {
+  constexpr int V = Vec<T>::N;
+  const int64_t nvec = count / V;
+  for (int64_t iv = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; iv < nvec;
+       iv += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = iv * V;
+    float v[V];
+    Vec<T>::load(dout + i, v);
+#pragma unroll
+    for (int q = 0; q < V; ++q)
+      v[q] = dropout_keep(seed, (uint64_t)(i + q), thr) ? v[q] * scale : 0.0f;
+    Vec<T>::store(dz + i, v);
+  }
+}
+
+// --------------------------------------------------------------- colsum --
+// Stage 1: block (cx, chunk) sums rows [chunk·rpc, (chunk+1)·rpc) of columns
+// [cx·32·V, (cx+1)·32·V): 32 column groups of V × 8 row lanes; the 8 lane
+// partials are combined in a fixed order.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    colsum_stage1(const T* __restrict__ X, int64_t rows, int64_t cols,
+                  int64_t ld, int64_t rpc, float* __restrict__ partial) {
+  constexpr int V = Vec<T>::N;
+  __shared__ float red[8][32 * V + 1];
+  const int cg = threadIdx.x & 31, rl = threadIdx.x >> 5;
+  const int64_t c0 = (int64_t)blockIdx.x * 32 * V + cg * V;
+  const int64_t r_begin = (int64_t)blockIdx.y * rpc;
+  const int64_t r_end = min(rows, r_begin + rpc);
+  float acc[V];
+#pragma unroll
+  for (int q = 0; q < V; ++q) acc[q] = 0.0f;
+  if (c0 < cols) {
+    for (int64_t r = r_begin + rl; r < r_end; r += 8) {
+      float v[V];
+      Vec<T>::load(X + r * ld + c0, v);
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] += v[q];
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < V; ++q) red[rl][cg * V + q] = acc[q];
+  __syncthreads();
+  for (int c = threadIdx.x; c < 32 * V; c += blockDim.x) {
+    float s = 0.0f;
+#pragma unroll
+    for (int l = 0; l < 8; ++l) s += red[l][c];
+    const int64_t col = (int64_t)blockIdx.x * 32 * V + c;
+    if (col < cols) partial[(int64_t)blockIdx.y * cols + col] = s;
+  }
+}
+
+// Stage 2: out[c] = Σ_chunk partial[chunk][c] in chunk order.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    colsum_stage2(const float* __restrict__ partial, int chunks, int64_t cols,
+                  T* __restrict__ out) {
+  for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols;
+       c += (int64_t)gridDim.x * blockDim.x) {
+    float s = 0.0f;
+    for (int k = 0; k < chunks; ++k) s += partial[(int64_t)k * cols + c];
+    out[c] = from_f<T>(s);
+  }
+}
+
+// -------------------------------------------------------------- RMSNorm --
+// One block per row (grid-stride over rows); each thread owns columns
+// {V·(tid + 256·j)}.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    rmsnorm_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
+                       T* __restrict__ y, float* __restrict__ rstd_out,
+                       int64_t rows, int64_t h, float eps) {
+  constexpr int V = Vec<T>::N;
+  __shared__ float red[8];
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const T* xr = x + r * h;
+    float ss = 0.0f;
+    for (int64_t c = (int64_t)threadIdx.x * V; c < h; c += 256 * V) {
+      float v[V];
+      Vec<T>::load(xr + c, v);
+#pragma unroll
+      for (int q = 0; q < V; ++q) ss += v[q] * v[q];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    const float rs = rsqrtf(tot / (float)h + eps);
+    if (threadIdx.x == 0) rstd_out[r] = rs;
+    for (int64_t c = (int64_t)threadIdx.x * V; c < h; c += 256 * V) {
+      float v[V], g[V];
+      Vec<T>::load(xr + c, v);
+      Vec<T>::load(gamma + c, g);
+#pragma unroll
+      for (int q = 0; q < V; ++q) v[q] = v[q] * rs * g[q];
+      Vec<T>::store(y + r * h + c, v);
+    }
+    __syncthreads();
+  }
+}
+
+// Block = rows [chunk·rpc, …); per row: g = dy⊙γ, dot = Σ g·x,
+// dx = rstd·g − x·rstd³·dot/h (+ dres); dγ partial Σ_rows dy·x·rstd kept in
+// registers (each thread owns at most MAXC columns) and written per chunk.
+template <typename T, int MAXC>
+__global__ void __launch_bounds__(256)
+    rmsnorm_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+                       const T* __restrict__ gamma,
+                       const float* __restrict__ rstd,
+                       const T* __restrict__ dres, T* __restrict__ dx,
+                       float* __restrict__ dg_partial, int64_t rows, int64_t h,
+                       int64_t rpc) {
+  constexpr int V = Vec<T>::N;
+  __shared__ float red[8];
+  float dgacc[MAXC];
+#pragma unroll
+  for (int j = 0; j < MAXC; ++j) dgacc[j] = 0.0f;
+  const int64_t r_begin = (int64_t)blockIdx.x * rpc;
+  const int64_t r_end = min(rows, r_begin + rpc);
+  for (int64_t r = r_begin; r < r_end; ++r) {
+    const float rs = rstd[r];
+    float dot = 0.0f;
+#pragma unroll
+    for (int j = 0; j < MAXC / V; ++j) {
+      const int64_t c = ((int64_t)threadIdx.x + 256 * j) * V;
+      if (c < h) {
+        float d[V], xv[V], g[V];
+        Vec<T>::load(dy + r * h + c, d);
+        Vec<T>::load(x + r * h + c, xv);
+        Vec<T>::load(gamma + c, g);
+#pragma unroll
+        for (int q = 0; q < V; ++q) {
+          dot += d[q] * g[q] * xv[q];
+          dgacc[j * V + q] += d[q] * xv[q] * rs;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = dot;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    __syncthreads();
+    const float coef = rs * rs * rs * tot / (float)h;
+#pragma unroll
+    for (int j = 0; j < MAXC / V; ++j) {
+      const int64_t c = ((int64_t)threadIdx.x + 256 * j) * V;
+      if (c < h) {
+        float d[V], xv[V], g[V], o[V];
+        Vec<T>::load(dy + r * h + c, d);
+        Vec<T>::load(x + r * h + c, xv);
+        Vec<T>::load(gamma + c, g);
+        if (dres != nullptr) {
+          Vec<T>::load(dres + r * h + c, o);
+        } else {
+#pragma unroll
+          for (int q = 0; q < V; ++q) o[q] = 0.0f;
+        }
+#pragma unroll
+        for (int q = 0; q < V; ++q) o[q] += rs * d[q] * g[q] - xv[q] * coef;
+        Vec<T>::store(dx + r * h + c, o);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < MAXC / V; ++j) {
+    const int64_t c = ((int64_t)threadIdx.x + 256 * j) * V;
+    if (c < h) {
+#pragma unroll
+      for (int q = 0; q < V; ++q)
+        dg_partial[(int64_t)blockIdx.x * h + c + q] = dgacc[j * V + q];
+    }
+  }
+}
+
+int grid_for(int64_t work_items, int per_block) {
+  const int64_t blocks = (work_items + per_block - 1) / per_block;
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  return (int)std::max<int64_t>(1, std::min(blocks, cap));
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------- host --
+template <typename T>
+int reduce_partials(const void* P, int n, int64_t rows, int64_t h,
+                    const void* bias, const void* resid, void* out,
+                    const DropoutSpec& d, void* stream) {
+  const int64_t count = rows * h;
+  if (count == 0) return cudaSuccess;
+  const int grid = grid_for(count / Vec<T>::N, 256);
+  reduce_partials_kernel<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const T*>(P), n, count, h, static_cast<const T*>(bias),
+      static_cast<const T*>(resid), static_cast<T*>(out), d.enabled, d.thr,
+      d.scale, d.seed);
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <typename T>
+int dropout_bwd(const void* dout, int64_t count, void* dz, const DropoutSpec& d,
+                void* stream) {
+  if (count == 0) return cudaSuccess;
+  const int grid = grid_for(count / Vec<T>::N, 256);
+  dropout_bwd_kernel<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const T*>(dout), count, static_cast<T*>(dz), d.thr, d.scale,
+      d.seed);
+  count_launch();
+  return cudaGetLastError();
+}
+
+int colsum_chunks(int64_t rows) {
+  return (int)std::max<int64_t>(1, std::min<int64_t>(64, (rows + 63) / 64));
+}
+
+size_t colsum_scratch_bytes(int64_t rows, int64_t cols) {
+  return (size_t)colsum_chunks(rows) * (size_t)cols * sizeof(float);
+}
+
+template <typename T>
+int colsum(const void* X, int64_t rows, int64_t cols, int64_t ld, void* out,
+           float* scratch, void* stream) {
+  if (cols == 0) return cudaSuccess;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int chunks = colsum_chunks(rows);
+  const int64_t rpc = (rows + chunks - 1) / chunks;
+  constexpr int V = Vec<T>::N;
+  dim3 g1((unsigned)((cols + 32 * V - 1) / (32 * V)), (unsigned)chunks);
+  colsum_stage1<T><<<g1, 256, 0, s>>>(static_cast<const T*>(X), rows, cols, ld,
+                                      rpc, scratch);
+  colsum_stage2<T><<<grid_for(cols, 256), 256, 0, s>>>(scratch, chunks, cols,
+                                                       static_cast<T*>(out));
+  count_launch(2);
+  return cudaGetLastError();
+}
+
+template <typename T>
+int rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
+                int64_t rows, int64_t h, float eps, void* stream) {
+  if (rows == 0) return cudaSuccess;
+  const int grid = (int)std::min<int64_t>(rows, (int64_t)device_sm_count() * 8);
+  rmsnorm_fwd_kernel<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const T*>(x), static_cast<const T*>(gamma),
+      static_cast<T*>(y), rstd, rows, h, eps);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// A fixed chunk count keeps the scratch size independent of the device.
+int rmsnorm_bwd_chunks(int64_t rows) {
+  return (int)std::max<int64_t>(1, std::min<int64_t>(rows, 256));
+}
+
+size_t rmsnorm_bwd_scratch(int64_t rows, int64_t h) {
+  return (size_t)rmsnorm_bwd_chunks(rows) * (size_t)h * sizeof(float);
+}
+
+template <typename T>
+int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
+                const float* rstd, const void* dres, void* dx, void* dgamma,
+                float* scratch, int64_t rows, int64_t h, void* stream) {
+  if (rows == 0) return cudaSuccess;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int chunks = rmsnorm_bwd_chunks(rows);
+  const int64_t rpc = (rows + chunks - 1) / chunks;
+  constexpr int V = Vec<T>::N;
+  // columns per thread: 256 threads × V per sweep
+  const int64_t sweeps = (h + 256 * V - 1) / (256 * V);
+  if (sweeps > 8) return cudaErrorInvalidValue;
+  const T* dyp = static_cast<const T*>(dy);
+  const T* xp = static_cast<const T*>(x);
+  const T* gp = static_cast<const T*>(gamma);
+  const T* rp = static_cast<const T*>(dres);
+  T* dxp = static_cast<T*>(dx);
+  if (sweeps <= 2)
+    rmsnorm_bwd_kernel<T, 2 * V><<<chunks, 256, 0, s>>>(dyp, xp, gp, rstd, rp,
+                                                        dxp, scratch, rows, h,
+                                                        rpc);
+  else if (sweeps <= 4)
+    rmsnorm_bwd_kernel<T, 4 * V><<<chunks, 256, 0, s>>>(dyp, xp, gp, rstd, rp,
+                                                        dxp, scratch, rows, h,
+                                                        rpc);
+  else
+    rmsnorm_bwd_kernel<T, 8 * V><<<chunks, 256, 0, s>>>(dyp, xp, gp, rstd, rp,
+                                                        dxp, scratch, rows, h,
+                                                        rpc);
+  colsum_stage2<T><<<grid_for(h, 256), 256, 0, s>>>(scratch, chunks, h,
+                                                    static_cast<T*>(dgamma));
+  count_launch(2);
+  return cudaGetLastError();
+}
+
+#define TP_INST(T)                                                            \
+  template int reduce_partials<T>(const void*, int, int64_t, int64_t,         \
+                                  const void*, const void*, void*,            \
+                                  const DropoutSpec&, void*);                 \
+  template int dropout_bwd<T>(const void*, int64_t, void*, const DropoutSpec&, \
+                              void*);                                         \
+  template int colsum<T>(const void*, int64_t, int64_t, int64_t, void*,       \
+                         float*, void*);                                      \
+  template int rmsnorm_fwd<T>(const void*, const void*, void*, float*,        \
+                              int64_t, int64_t, float, void*);                \
+  template int rmsnorm_bwd<T>(const void*, const void*, const void*,          \
+                              const float*, const void*, void*, void*,        \
+                              float*, int64_t, int64_t, void*);
+TP_INST(float)
+TP_INST(__nv_bfloat16)
+#undef TP_INST
+
+}  // namespace tp

@@ -1,0 +1,40 @@
+// elementwise.h — host launchers of the HBM-bound kernels (elementwise.cu).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tp {
+
+struct DropoutSpec {
+  int enabled = 0;
+  uint32_t thr = 0;       // keep iff the top 24 bits of the draw ≥ thr
+  float scale = 1.0f;     // 1 / (1 − p)
+  uint64_t seed = 0;
+};
+
+// out = resid + Dropout(Σ_{i<n} P[i] + bias); P is n × [rows, h] contiguous.
+template <typename T>
+int reduce_partials(const void* P, int n, int64_t rows, int64_t h,
+                    const void* bias, const void* resid, void* out,
+                    const DropoutSpec& d, void* stream);
+// dz = dout ⊙ mask · scale over `count` elements of a [*, h] tensor.
+template <typename T>
+int dropout_bwd(const void* dout, int64_t count, void* dz,
+                const DropoutSpec& d, void* stream);
+// out[c] = Σ_r X[r, c] (deterministic two-stage; scratch from
+// colsum_scratch_bytes).
+size_t colsum_scratch_bytes(int64_t rows, int64_t cols);
+template <typename T>
+int colsum(const void* X, int64_t rows, int64_t cols, int64_t ld, void* out,
+           float* scratch, void* stream);
+template <typename T>
+int rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
+                int64_t rows, int64_t h, float eps, void* stream);
+size_t rmsnorm_bwd_scratch(int64_t rows, int64_t h);
+template <typename T>
+int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
+                const float* rstd, const void* dres, void* dx, void* dgamma,
+                float* scratch, int64_t rows, int64_t h, void* stream);
+
+}  // namespace tp

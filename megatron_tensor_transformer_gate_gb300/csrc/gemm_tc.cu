@@ -1,0 +1,537 @@
+// gemm_tc.cu — tcgen05 (5th-generation tensor core) GEMM of the TP block.
+//
+// One persistent kernel per GEMM launch: 192 threads per CTA, one CTA per SM.
+//   warp 0   TMA producer: one thread streams A and B tiles of 64 K-elements
+//            into a 4-stage shared-memory ring (128-byte swizzle).
+//   warp 1   allocates 512 TMEM columns (two 128×256 fp32 accumulators) and
+//            one thread issues tcgen05.mma (M=128, N=256, K=16) into them.
+//   warps 2–5 epilogue: tcgen05.ld of the finished accumulator (one TMEM lane
+//            = one output row per thread), the fused elementwise work of the
+//            launch, and 16-byte stores.  Double-buffered accumulators let
+//            the epilogue of tile i overlap the main loop of tile i+1.
+// The segment / part structure of the K loop is described in gemm.h; it is
+// how the shard sum of a row-parallel projection (g) or of an input gradient
+// (f) is taken in the accumulator ([Grasp-TP] §2–§3, [adu-TP] 算子 f 和 g).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm.h"
+
+namespace tp {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;           // 16 KB
+constexpr int B_BYTES = BN * BK * 2;           // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+struct TcPart {
+  int kblocks;
+  int nsub;
+  int seg_z_stride;
+  int seg_sub_stride;
+};
+
+struct TcParams {
+  CUtensorMap ma[3];
+  CUtensorMap mb[3];
+  CUtensorMap mb2;
+  TcPart part[3];
+  int nparts;
+  int M, N;            // N is the logical output width
+  int m_tiles, n_tiles, nz, total_tiles, group_m;
+  GemmEpilogue epi;
+  unsigned* status;
+};
+
+__device__ __forceinline__ void decode_tile(const TcParams& p, int t, int& z,
+                                            int& mt, int& nt) {
+  const int per_z = p.m_tiles * p.n_tiles;
+  z = t / per_z;
+  const int r = t - z * per_z;
+  const int gsz = p.group_m * p.n_tiles;
+  const int g = r / gsz;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.group_m, p.m_tiles - first_m);
+  const int rr = r - g * gsz;
+  mt = first_m + rr % gm;
+  nt = rr / gm;
+}
+
+// ---------------------------------------------------------------- epilogue --
+__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src,
+                                            float* v, int valid) {
+  if (valid >= 32) {
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = __ldg(s + q);
+      float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y),
+             c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+      v[8 * q + 0] = a.x; v[8 * q + 1] = a.y; v[8 * q + 2] = b.x;
+      v[8 * q + 3] = b.y; v[8 * q + 4] = c.x; v[8 * q + 5] = c.y;
+      v[8 * q + 6] = d.x; v[8 * q + 7] = d.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      v[i] = (i < valid) ? __bfloat162float(src[i]) : 0.0f;
+  }
+}
+
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst,
+                                             const float* v, int valid) {
+  if (valid >= 32) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 u;
+      u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      d[q] = u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < valid) dst[i] = __float2bfloat16_rn(v[i]);
+  }
+}
+
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(const TcParams& p,
+                                              uint32_t taddr, int z, int m,
+                                              int n0) {
+  const GemmEpilogue& e = p.epi;
+  const bool row_ok = m < p.M;
+  if constexpr (EPI == EPI_SWIGLU) {
+    // accumulator columns [0,128): gate, [128,256): up, same hidden units
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t rg[32], ru[32];
+      tmem_ld32(taddr + c * 32, rg);
+      tmem_ld_wait(rg);
+      tmem_ld32(taddr + 128 + c * 32, ru);
+      tmem_ld_wait(ru);
+      const int n = n0 + c * 32;
+      if (row_ok && n < p.N) {
+        const int valid = min(32, p.N - n);
+        float g[32], u[32], a[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          g[i] = __uint_as_float(rg[i]);
+          u[i] = __uint_as_float(ru[i]);
+          a[i] = g[i] * sigmoid_f(g[i]) * u[i];
+        }
+        const int64_t off = (int64_t)m * e.ldo + n;
+        store32_bf16(static_cast<__nv_bfloat16*>(e.out) + off, g, valid);
+        store32_bf16(static_cast<__nv_bfloat16*>(e.out2) + off, u, valid);
+        store32_bf16(static_cast<__nv_bfloat16*>(e.out3) +
+                         (int64_t)m * e.ldo2 + n,
+                     a, valid);
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      tmem_ld_wait(r);
+      const int n = n0 + c * 32;
+      if (!row_ok || n >= p.N) continue;
+      const int valid = min(32, p.N - n);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      if constexpr (EPI == EPI_STORE) {
+        if (e.bias != nullptr) {
+          float b[32];
+          load32_bf16(static_cast<const __nv_bfloat16*>(e.bias) + n, b, valid);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] += b[i];
+        }
+        if (e.dropout) {
+          const uint64_t base = (uint64_t)m * (uint64_t)p.N + (uint64_t)n;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[i] = dropout_keep(e.seed, base + i, e.drop_thr)
+                       ? v[i] * e.drop_scale
+                       : 0.0f;
+        }
+        if (e.resid != nullptr) {
+          float rr[32];
+          load32_bf16(static_cast<const __nv_bfloat16*>(e.resid) +
+                          (int64_t)m * e.ldr + n,
+                      rr, valid);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] += rr[i];
+        }
+        store32_bf16(static_cast<__nv_bfloat16*>(e.out) +
+                         (int64_t)z * e.out_z_stride + (int64_t)m * e.ldo + n,
+                     v, valid);
+      } else if constexpr (EPI == EPI_GELU) {
+        if (e.bias != nullptr) {
+          float b[32];
+          load32_bf16(static_cast<const __nv_bfloat16*>(e.bias) + n, b, valid);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] += b[i];
+        }
+        const int64_t off = (int64_t)m * e.ldo + n;
+        store32_bf16(static_cast<__nv_bfloat16*>(e.out) + off, v, valid);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+        store32_bf16(static_cast<__nv_bfloat16*>(e.out2) +
+                         (int64_t)m * e.ldo2 + n,
+                     v, valid);
+      } else if constexpr (EPI == EPI_DGELU) {
+        float hv[32];
+        load32_bf16(static_cast<const __nv_bfloat16*>(e.aux1) +
+                        (int64_t)m * e.ld_aux + n,
+                    hv, valid);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(hv[i]);
+        store32_bf16(static_cast<__nv_bfloat16*>(e.out) + (int64_t)m * e.ldo + n,
+                     v, valid);
+      } else if constexpr (EPI == EPI_DSWIGLU) {
+        float g[32], u[32], dg[32];
+        const int64_t aoff = (int64_t)m * e.ld_aux + n;
+        load32_bf16(static_cast<const __nv_bfloat16*>(e.aux1) + aoff, g, valid);
+        load32_bf16(static_cast<const __nv_bfloat16*>(e.aux2) + aoff, u, valid);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float s = sigmoid_f(g[i]);
+          dg[i] = v[i] * u[i] * s * (1.0f + g[i] * (1.0f - s));
+          v[i] = v[i] * g[i] * s;   // dU = dA · SiLU(G)
+        }
+        const int64_t off = (int64_t)m * e.ldo + n;
+        store32_bf16(static_cast<__nv_bfloat16*>(e.out) + off, dg, valid);
+        store32_bf16(static_cast<__nv_bfloat16*>(e.out2) + off, v, valid);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel --
+template <int A_MN, int B_MN, int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smB + STAGES * B_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr int BN_LOG = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.nparts; ++i) {
+      tma_prefetch_desc(&p.ma[i]);
+      tma_prefetch_desc(&p.mb[i]);
+    }
+    if (EPI == EPI_SWIGLU) tma_prefetch_desc(&p.mb2);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------- TMA producer --
+      uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+        int z, mt, nt;
+        decode_tile(p, t, z, mt, nt);
+        const int m0 = mt * BM, n0 = nt * BN_LOG;
+        for (int pi = 0; ok && pi < p.nparts; ++pi) {
+          const TcPart& pt = p.part[pi];
+          for (int j = 0; ok && j < pt.nsub; ++j) {
+            const int seg = z * pt.seg_z_stride + j * pt.seg_sub_stride;
+            for (int kb = 0; kb < pt.kblocks; ++kb) {
+              if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status,
+                             1)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+              armed |= 1u << stage;
+              armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+              uint8_t* sa = smA + stage * A_BYTES;
+              uint8_t* sb = smB + stage * B_BYTES;
+              const int k0 = kb * BK;
+              if (A_MN) {
+                tma_load_3d(sa, &p.ma[pi], &full[stage], m0, k0, seg);
+                tma_load_3d(sa + 8192, &p.ma[pi], &full[stage], m0 + 64, k0,
+                            seg);
+              } else {
+                tma_load_3d(sa, &p.ma[pi], &full[stage], k0, seg, m0);
+              }
+              if (EPI == EPI_SWIGLU) {
+                tma_load_3d(sb, &p.mb[pi], &full[stage], k0, seg, n0);
+                tma_load_3d(sb + 16384, &p.mb2, &full[stage], k0, seg, n0);
+              } else if (B_MN) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  tma_load_3d(sb + q * 8192, &p.mb[pi], &full[stage],
+                              n0 + 64 * q, k0, seg);
+              } else {
+                tma_load_3d(sb, &p.mb[pi], &full[stage], k0, seg, n0);
+              }
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let every copy this thread started land before the CTA exits
+        volatile int no_abort = 0;
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s))
+            mbar_wait(&full[s], (armed_par >> s) & 1u, &no_abort, nullptr, 0);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------- MMA issue --
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = blockIdx.x; ok && t < p.total_tiles;
+           t += gridDim.x, ++it) {
+        int z, mt, nt;
+        decode_tile(p, t, z, mt, nt);
+        const int buf = it & 1;
+        const uint32_t aphase = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[buf], aphase ^ 1, abort_flag, p.status, 2)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        uint32_t acc = 0;
+        for (int pi = 0; ok && pi < p.nparts; ++pi) {
+          const TcPart& pt = p.part[pi];
+          for (int j = 0; ok && j < pt.nsub; ++j) {
+            for (int kb = 0; kb < pt.kblocks; ++kb) {
+              if (!mbar_wait(&full[stage], phase, abort_flag, p.status, 3)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a0 = smem_u32(smA + stage * A_BYTES);
+              const uint32_t b0 = smem_u32(smB + stage * B_BYTES);
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                const uint64_t ad =
+                    A_MN ? smem_desc_sw128(a0 + kk * 2048, 8192, 1024)
+                         : smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                const uint64_t bd =
+                    B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
+                         : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                tc_mma_f16(d_tmem, ad, bd, IDESC, acc);
+                acc = 1;
+              }
+              tc_commit(&empty[stage]);
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1;
+              }
+            }
+          }
+        }
+        if (ok) tc_commit(&tfull[buf]);
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        tc_commit(drain);
+        mbar_wait(drain, 0, &no_abort, nullptr, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    const int quarter = warp & 3;   // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+      int z, mt, nt;
+      decode_tile(p, t, z, mt, nt);
+      const int buf = it & 1;
+      const uint32_t aphase = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[buf], aphase, abort_flag, p.status, 4)) break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN;
+      epilogue_tile<EPI>(p, taddr, z, mt * BM + row, nt * BN_LOG);
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------- host --
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
+               uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0,
+               uint32_t b1, uint32_t b2) {
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K-major operand (rows × K, row stride ld): dims {kseg, nseg, rows}.
+// MN-major operand (K × rows, row stride ld): dims {rows, kseg, nseg}.
+bool encode_operand(CUtensorMap* m, const GemmOperand& o, int64_t kseg,
+                    int nseg, uint32_t box_rows) {
+  if (o.mn_major)
+    return encode_3d(m, o.ptr, o.rows, kseg, nseg, o.ld * 2,
+                     (uint64_t)kseg * o.ld * 2, 64, BK, 1);
+  return encode_3d(m, o.ptr, kseg, nseg, o.rows, kseg * 2, o.ld * 2, BK, 1,
+                   box_rows);
+}
+
+template <int A_MN, int B_MN, int EPI>
+int launch_inst(const TcParams& prm, int grid, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<A_MN, B_MN, EPI>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  gemm_tc_kernel<A_MN, B_MN, EPI><<<grid, THREADS, SMEM_BYTES, s>>>(prm);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
+  if (!get_encode()) return cudaErrorNotSupported;
+  const GemmEpilogue& e = pr.epi;
+  const int a_mn = pr.parts[0].a.mn_major, b_mn = pr.parts[0].b.mn_major;
+  for (int i = 1; i < pr.nparts; ++i)
+    if (pr.parts[i].a.mn_major != a_mn || pr.parts[i].b.mn_major != b_mn)
+      return cudaErrorInvalidValue;
+  if (e.kind == EPI_SWIGLU && (b_mn || a_mn || pr.nparts != 1))
+    return cudaErrorInvalidValue;
+
+  TcParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.nparts = pr.nparts;
+  for (int i = 0; i < pr.nparts; ++i) {
+    const GemmPart& pt = pr.parts[i];
+    if (!encode_operand(&prm.ma[i], pt.a, pt.kseg, pt.nseg, BM))
+      return cudaErrorInvalidValue;
+    const uint32_t brows = (e.kind == EPI_SWIGLU) ? BN / 2 : BN;
+    if (!encode_operand(&prm.mb[i], pt.b, pt.kseg, pt.nseg, brows))
+      return cudaErrorInvalidValue;
+    if (e.kind == EPI_SWIGLU &&
+        !encode_operand(&prm.mb2, pt.b2, pt.kseg, pt.nseg, brows))
+      return cudaErrorInvalidValue;
+    prm.part[i].kblocks = (int)((pt.kseg + BK - 1) / BK);
+    prm.part[i].nsub = pt.nsub;
+    prm.part[i].seg_z_stride = pt.seg_z_stride;
+    prm.part[i].seg_sub_stride = pt.seg_sub_stride;
+  }
+  const int bn_log = (e.kind == EPI_SWIGLU) ? BN / 2 : BN;
+  prm.M = (int)pr.M;
+  prm.N = (int)pr.N;
+  prm.m_tiles = (int)((pr.M + BM - 1) / BM);
+  prm.n_tiles = (int)((pr.N + bn_log - 1) / bn_log);
+  prm.nz = pr.nz;
+  prm.total_tiles = prm.m_tiles * prm.n_tiles * pr.nz;
+  prm.group_m = 16;
+  prm.epi = e;
+  prm.status = status;
+  if (prm.total_tiles == 0) return cudaSuccess;
+  const int grid = std::min(prm.total_tiles, device_sm_count());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  switch (e.kind) {
+    case EPI_STORE:
+      if (!a_mn && !b_mn) return launch_inst<0, 0, EPI_STORE>(prm, grid, s);
+      if (!a_mn && b_mn) return launch_inst<0, 1, EPI_STORE>(prm, grid, s);
+      if (a_mn && b_mn) return launch_inst<1, 1, EPI_STORE>(prm, grid, s);
+      return launch_inst<1, 0, EPI_STORE>(prm, grid, s);
+    case EPI_GELU:
+      if (a_mn || b_mn) return cudaErrorInvalidValue;
+      return launch_inst<0, 0, EPI_GELU>(prm, grid, s);
+    case EPI_SWIGLU:
+      return launch_inst<0, 0, EPI_SWIGLU>(prm, grid, s);
+    case EPI_DGELU:
+      if (a_mn || !b_mn) return cudaErrorInvalidValue;
+      return launch_inst<0, 1, EPI_DGELU>(prm, grid, s);
+    case EPI_DSWIGLU:
+      if (a_mn || !b_mn) return cudaErrorInvalidValue;
+      return launch_inst<0, 1, EPI_DSWIGLU>(prm, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tp

@@ -1,0 +1,137 @@
+"""Host-side checks of the C ABI: it builds, loads, exports every declared
+symbol, its accountant is bit-exact against the oracle, and invalid calls are
+rejected before any launch (no GPU needed)."""
+
+import ctypes
+import os
+import re
+from fractions import Fraction
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tp.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tp_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(tp):
+    names = declared_functions()
+    assert len(names) >= 18
+    L = tp.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(tp.SIGNATURES), "binding and header disagree"
+
+
+WORKLOADS = [  # scope, T, h, n, dtype
+    ("mlp", 64, 128, 2, "f32"), ("mlp", 4096, 1024, 4, "bf16"),
+    ("mlp", 8192, 4096, 8, "bf16"), ("attn", 4096, 4096, 4, "bf16"),
+    ("layer", 8192, 8192, 8, "bf16"), ("layer", 3, 40, 5, "f32"),
+    ("mlp", 1, 8, 1, "bf16"),
+]
+
+
+@pytest.mark.parametrize("scope,T,h,n,dt", WORKLOADS)
+def test_comm_bytes_bit_exact(tp, scope, T, h, n, dt):
+    r = tp.comm_bytes({"mlp": 0, "attn": 1, "layer": 2}[scope], T, h, n,
+                      {"f32": tp.F32, "bf16": tp.BF16}[dt])
+    o = oracle.comm_report(scope, T, h, n, dt)
+    assert r["reductions_fwd"] == o["reductions_fwd"]
+    assert r["reductions_bwd"] == o["reductions_bwd"]
+    assert r["payload_bytes"] == o["payload_bytes"]
+    assert Fraction(r["ring_bytes_num"], r["ring_bytes_den"]) == o["ring_bytes"]
+    assert r["page2_bytes"] == o["page2_bytes"]
+    assert r["total_payload"] == o["total_payload"]
+    assert Fraction(r["total_ring_num"], r["ring_bytes_den"]) == o["total_ring"]
+    assert r["total_page2"] == o["total_page2"]
+
+
+def test_comm_bytes_named_workloads(tp):
+    # 2 reductions per MLP, 4 per layer, each T·h·δ
+    r = tp.comm_bytes(tp.SCOPE_MLP, 8192, 4096, 8, tp.BF16)
+    assert r["total_payload"] == 2 * 67_108_864
+    r = tp.comm_bytes(tp.SCOPE_LAYER, 8192, 8192, 8, tp.BF16)
+    assert r["total_payload"] == 4 * 134_217_728
+    assert r["total_page2"] == 1_073_741_824
+    assert r["total_ring_num"] // r["ring_bytes_den"] == 939_524_096
+
+
+@pytest.mark.parametrize("T,h,f,act", [(64, 128, 512, "gelu"),
+                                       (4096, 1024, 4096, "gelu"),
+                                       (8192, 4096, 11008, "swiglu"),
+                                       (8192, 8192, 28672, "swiglu"),
+                                       (7, 24, 40, "gelu")])
+def test_mlp_flops_bit_exact(tp, T, h, f, act):
+    d = tp.mlp_desc(T, h, f, 1, act=tp.GELU if act == "gelu" else tp.SWIGLU)
+    assert tp.mlp_flops(d) == oracle.mlp_flops(T, h, f, act)
+
+
+@pytest.mark.parametrize("b,s,h,nq,nkv,d,causal", [
+    (2, 2048, 4096, 32, 8, 128, True), (1, 8192, 8192, 64, 8, 128, True),
+    (2, 2048, 4096, 32, 8, 128, False), (3, 5, 24, 3, 1, 8, True)])
+def test_attn_flops_bit_exact(tp, b, s, h, nq, nkv, d, causal):
+    desc = tp.attn_desc(b, s, h, nq, nkv, d, 1, causal=causal)
+    assert tp.attn_flops(desc) == oracle.attn_flops(b, s, h, nq, nkv, d,
+                                                    causal)
+
+
+def test_named_flop_totals(tp):
+    a = tp.attn_flops(tp.attn_desc(1, 8192, 8192, 64, 8, 128, 8))
+    m = tp.mlp_flops(tp.mlp_desc(8192, 8192, 28672, 8, act=tp.SWIGLU))
+    assert sum(a) + sum(m) == 45_355_257_298_944
+    assert sum(tp.mlp_flops(tp.mlp_desc(8192, 4096, 11008, 8,
+                                        act=tp.SWIGLU))) == 6_648_609_374_208
+
+
+FAKE = ctypes.c_void_p(0x100000)   # an aligned address never dereferenced
+
+
+def _fwd(tp, desc, ws_bytes=1 << 40):
+    L = tp.lib()
+    return L.tp_mlp_fwd(ctypes.byref(desc), FAKE, FAKE, None, FAKE, None, None,
+                        FAKE, FAKE, ws_bytes, None)
+
+
+def test_mlp_rejects_before_launch(tp):
+    L = tp.lib()
+    assert L.tp_mlp_fwd(None, FAKE, FAKE, None, FAKE, None, None, FAKE, FAKE,
+                        1, None) == 1                       # NULL desc
+    assert _fwd(tp, tp.mlp_desc(64, 128, 500, 4)) == 2      # n ∤ h_ffn
+    assert _fwd(tp, tp.mlp_desc(64, 124, 512, 2)) == 2      # h % 8
+    assert _fwd(tp, tp.mlp_desc(64, 128, 512, 2, dtype=7)) == 3
+    assert _fwd(tp, tp.mlp_desc(64, 128, 512, 2, dropout_p=1.0)) == 8
+    d = tp.mlp_desc(64, 128, 512, 2)
+    assert _fwd(tp, d, ws_bytes=16) == 4                    # ws too small
+    assert tp.mlp_workspace_bytes(d) >= 2 * 64 * 512 * 2
+    mis = ctypes.c_void_p(0x100004)
+    assert L.tp_mlp_fwd(ctypes.byref(d), mis, FAKE, None, FAKE, None, None,
+                        FAKE, FAKE, 1 << 40, None) == 8     # misaligned
+    assert L.tp_mlp_fwd(ctypes.byref(d), None, FAKE, None, FAKE, None, None,
+                        FAKE, FAKE, 1 << 40, None) == 1
+
+
+def test_attn_rejects_before_launch(tp):
+    L = tp.lib()
+
+    def call(desc, ws_bytes=1 << 40):
+        return L.tp_attn_fwd(ctypes.byref(desc), FAKE, FAKE, FAKE, FAKE, FAKE,
+                             None, None, FAKE, FAKE, ws_bytes, None)
+
+    assert call(tp.attn_desc(1, 64, 512, 6, 4, 128, 2)) == 2   # n_kv ∤ n_q
+    assert call(tp.attn_desc(1, 64, 512, 8, 2, 128, 4)) == 2   # n ∤ n_kv
+    assert call(tp.attn_desc(1, 64, 512, 8, 2, 64, 2)) == 5    # d != 128
+    assert call(tp.attn_desc(1, 64, 512, 8, 2, 128, 2, dtype=tp.F32)) == 5
+    assert call(tp.attn_desc(1, 64, 512, 8, 2, 128, 2), ws_bytes=1) == 4
+    assert tp.attn_workspace_bytes(tp.attn_desc(1, 64, 512, 8, 2, 128, 2)) > 0
+
+
+def test_status_strings(tp):
+    L = tp.lib()
+    for code in range(9):
+        assert L.tp_status_string(code)

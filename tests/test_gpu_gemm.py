@@ -1,0 +1,60 @@
+"""Tensor-core (bf16) and CUDA-core (fp32) GEMM building block vs the plain
+definition C[m, n] = Σ_k A[m, k]·B[n, k] in fp64, all operand layouts, tile
+tails, multi-tile K."""
+
+import numpy as np
+import pytest
+import torch
+
+from _parity import f64
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(128, 256, 64), (200, 264, 136), (384, 520, 1000), (1, 8, 8),
+          (1000, 24, 72)]
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_bf16_layouts(tp, a_mn, b_mn, M, N, K):
+    g = torch.Generator().manual_seed(M * 7 + N * 3 + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    Bm = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    ref = f64(A) @ f64(Bm).T
+    dA = (A.t().contiguous() if a_mn else A).cuda()
+    dB = (Bm.t().contiguous() if b_mn else Bm).cuda()
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tp.gemm(dA, dB, C, a_mn_major=bool(a_mn), b_mn_major=bool(b_mn))
+    tp.device_status()
+    got = f64(C)
+    assert np.isfinite(got).all()
+    # bf16 output rounding (2^-8 relative) dominates fp32 accumulation error
+    err = np.abs(got - ref).max()
+    assert err <= 8e-3 * np.abs(ref).max() + 1e-3, err
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
+def test_gemm_f32(tp, a_mn, b_mn):
+    M, N, K = 130, 70, 200
+    g = torch.Generator().manual_seed(5)
+    A = torch.randn(M, K, generator=g)
+    Bm = torch.randn(N, K, generator=g)
+    ref = f64(A) @ f64(Bm).T
+    dA = (A.t().contiguous() if a_mn else A).cuda()
+    dB = (Bm.t().contiguous() if b_mn else Bm).cuda()
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    tp.gemm(dA, dB, C, a_mn_major=bool(a_mn), b_mn_major=bool(b_mn))
+    tp.device_status()
+    assert np.abs(f64(C) - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+def test_gemm_large_k_many_tiles(tp):
+    M, N, K = 512, 1024, 4096
+    g = torch.Generator().manual_seed(11)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    Bm = (torch.randn(N, K, generator=g) / 64).to(torch.bfloat16)
+    ref = f64(A) @ f64(Bm).T
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    tp.gemm(A.cuda(), Bm.cuda(), C)
+    tp.device_status()
+    assert np.abs(f64(C) - ref).max() <= 8e-3 * np.abs(ref).max()
