@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Benchmark of the TP-sharded Transformer layer (MLP + attention, fwd + bwd).
+
+One step = one forward and one backward pass of the whole block on one batch
+of synthetic inputs already resident in HBM: RMSNorm → head-sharded GQA
+attention (QKV column-parallel, out-projection row-parallel with the g sum)
+→ residual → RMSNorm → SwiGLU MLP (gate/up column-parallel, down row-parallel
+with the g sum) → residual, then the reverse pass with both f sums.  The TP
+group of degree n is n logical shards on one GPU; with --gpus N each rank runs
+its own replica (weak scaling, no collective on the data path).
+
+Prints one JSON line (rank 0).  `value` is algorithmic TFLOP/s of the whole
+job: FLOPs per step (the pages' closed forms, causal pairs only) × ranks ÷ the
+slowest rank's mean step time.  `roofline` covers the dominant kernel family,
+timed live with CUDA events recorded on its launch stream.  `e2e` repeats the
+measurement through the same public API with the step's activations copied
+from pinned host memory and the results read back inside the timed region.
+`cpu_baseline` times the fp64 oracle on a bounded sample of the same
+workload.  `--impl reference` times that oracle alone (the reference arm).
+"""
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("TP-sharded MLP+attn fwd+bwd TFLOP/s per layer on 1 GB300; "
+          "% of BF16 dense roofline")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="layer_bf16",
+                    choices=["layer_bf16", "mlp_swiglu_bf16", "mlp_gelu_bf16",
+                             "attn_gqa_bf16"])
+    ap.add_argument("--mode", default="fused",
+                    choices=["fused", "materialised"])
+    ap.add_argument("--seq", type=int, default=0,
+                    help="override s (smaller cases for profiler captures)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path, encoding="utf-8") as fh:
+            return json.load(fh), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+             "sw_power_cap"]
+
+    def __init__(self, index):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sms, maxes, power, reasons = [], [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                maxes.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(self.NAMES, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sms:
+            return None
+        sms.sort()
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms),
+                "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------- workloads --
+def workload_cfg(name, seq):
+    from megatron_tensor_transformer_gate_gb300 import inputs as I
+    cfg = I.workload(name)
+    if seq:
+        cfg["s"] = seq
+    return cfg
+
+
+def describe(cfg, mode):
+    k = cfg["kind"]
+    if k == "layer":
+        w = (f"pre-norm layer (RMSNorm, causal GQA attention n_q={cfg['n_q']} "
+             f"n_kv={cfg['n_kv']} d={cfg['d']}, SwiGLU h_ffn={cfg['h_ffn']}) "
+             f"b={cfg['b']} s={cfg['s']} h={cfg['h']} TP n={cfg['n']}")
+    elif k == "mlp":
+        w = (f"{cfg['act']} MLP b={cfg['b']} s={cfg['s']} h={cfg['h']} "
+             f"h_ffn={cfg['h_ffn']} TP n={cfg['n']}")
+    else:
+        w = (f"causal GQA attention b={cfg['b']} s={cfg['s']} h={cfg['h']} "
+             f"n_q={cfg['n_q']} n_kv={cfg['n_kv']} d={cfg['d']} "
+             f"TP n={cfg['n']}")
+    return {"workload": cfg["name"], "shape": w,
+            "tokens": cfg["b"] * cfg["s"],
+            "tp_degree_logical": cfg["n"], "reduction": mode}
+
+
+def flops_per_step(cfg):
+    """Algorithmic FLOPs of one fwd + bwd step, from the library's accountant."""
+    from megatron_tensor_transformer_gate_gb300 import binding as B
+    k = cfg["kind"]
+    T = cfg["b"] * cfg["s"]
+    total = 0
+    if k in ("layer", "attn"):
+        d = B.attn_desc(cfg["b"], cfg["s"], cfg["h"], cfg["n_q"], cfg["n_kv"],
+                        cfg["d"], cfg["n"], causal=True)
+        total += sum(B.attn_flops(d))
+    if k in ("layer", "mlp"):
+        act = B.SWIGLU if cfg["act"] == "swiglu" else B.GELU
+        d = B.mlp_desc(T, cfg["h"], cfg["h_ffn"], cfg["n"], act=act)
+        total += sum(B.mlp_flops(d))
+    return total
+
+
+class Runner:
+    """Owns the device inputs of one replica and runs fwd + bwd steps."""
+
+    def __init__(self, cfg, mode, seed, device):
+        import torch
+        from megatron_tensor_transformer_gate_gb300 import binding as B
+        from megatron_tensor_transformer_gate_gb300 import inputs as I
+        from megatron_tensor_transformer_gate_gb300.blocks import (
+            TPAttention, TPLayer, TPMLP)
+        self.cfg = cfg
+        self.kind = cfg["kind"]
+        md = B.FUSED if mode == "fused" else B.MATERIALISED
+        b, s, h = cfg["b"], cfg["s"], cfg["h"]
+        T = b * s
+        if self.kind == "layer":
+            self.x = I.layer_inputs(cfg, seed, device)
+            self.blk = TPLayer(b, s, h, cfg["h_ffn"], cfg["n_q"], cfg["n_kv"],
+                               cfg["d"], cfg["n"], eps=cfg["eps"], mode=md,
+                               device=device)
+            self.P = {k: self.x[k] for k in ("g1", "Wq", "Wk", "Wv", "Wo",
+                                             "g2", "W1", "W2")}
+            self.grads = self.blk.alloc_grads(self.P)
+        elif self.kind == "mlp":
+            self.x = I.mlp_inputs(cfg, seed, device)
+            act = B.SWIGLU if cfg["act"] == "swiglu" else B.GELU
+            self.blk = TPMLP(T, h, cfg["h_ffn"], cfg["n"], act=act, mode=md,
+                             dropout_p=cfg.get("p", 0.0), seed=seed,
+                             device=device)
+            self.grads = self.blk.alloc_grads(
+                self.x["W1"], self.x["W2"], self.x["b1"] is not None,
+                self.x["b2"] is not None)
+        else:
+            self.x = I.attn_inputs(cfg, seed, device)
+            self.blk = TPAttention(b, s, h, cfg["n_q"], cfg["n_kv"], cfg["d"],
+                                   cfg["n"], mode=md, device=device)
+            self.grads = self.blk.alloc_grads(self.x["Wq"], self.x["Wk"],
+                                              self.x["Wv"], self.x["Wo"])
+        self.out = torch.empty((T, h), dtype=torch.bfloat16, device=device)
+
+    def resident_bytes(self):
+        n = 0
+        for v in list(self.x.values()) + list(self.grads.values()):
+            if v is not None:
+                n += v.numel() * v.element_size()
+        return n
+
+    def step(self, X=None, dOut=None):
+        x = self.x
+        X = x["X"] if X is None else X
+        dOut = x["dOut"] if dOut is None else dOut
+        if self.kind == "layer":
+            self.blk.forward(X, self.P, out=self.out)
+            self.blk.backward(dOut, X, self.P, grads=self.grads)
+        elif self.kind == "mlp":
+            R = X if self.cfg.get("residual") == "X" else x["R"]
+            self.blk.forward(X, x["W1"], x["W2"], b1=x["b1"], b2=x["b2"],
+                             R=R, out=self.out)
+            dres = dOut if self.cfg.get("residual") == "X" else None
+            self.blk.backward(dOut, X, x["W1"], x["W2"], dres=dres,
+                              grads=self.grads)
+        else:
+            self.blk.forward(X, x["Wq"], x["Wk"], x["Wv"], x["Wo"],
+                             bo=x["bo"], R=x["R"], out=self.out)
+            self.blk.backward(dOut, X, x["Wq"], x["Wk"], x["Wv"], x["Wo"],
+                              grads=self.grads)
+
+
+# ------------------------------------------------------------ CPU baseline --
+def cpu_sample_cfg(cfg):
+    """A bounded sample of the workload for the fp64 oracle: the same widths
+    and heads, fewer tokens."""
+    s = dict(cfg)
+    s["b"] = 1
+    s["s"] = {"layer": 64, "mlp": 128, "attn": 256}[cfg["kind"]]
+    return s
+
+
+def run_oracle_step(scfg, xs):
+    import oracle
+    k = scfg["kind"]
+    kw = dict(b=scfg["b"], s=scfg["s"])
+    if k == "layer":
+        shp = dict(kw, n_q=scfg["n_q"], n_kv=scfg["n_kv"], d=scfg["d"],
+                   eps=scfg["eps"])
+        f = oracle.layer_forward(xs["X"], xs, **shp)
+        oracle.layer_backward(xs["dOut"], xs["X"], xs, f, **shp)
+    elif k == "mlp":
+        p = scfg.get("p", 0.0)
+        f = oracle.mlp_forward(xs["X"], xs["W1"], xs["W2"], act=scfg["act"],
+                               b1=xs["b1"], b2=xs["b2"], R=xs["R"], p=p)
+        oracle.mlp_backward(xs["dOut"], xs["X"], xs["W1"], xs["W2"], f,
+                            act=scfg["act"], p=p)
+    else:
+        shp = dict(kw, n_q=scfg["n_q"], n_kv=scfg["n_kv"], d=scfg["d"])
+        f = oracle.attention_forward(xs["X"], xs["Wq"], xs["Wk"], xs["Wv"],
+                                     xs["Wo"], **shp)
+        oracle.attention_backward(xs["dOut"], xs["X"], xs["Wq"], xs["Wk"],
+                                  xs["Wv"], xs["Wo"], f, **shp)
+
+
+def oracle_inputs(scfg, seed):
+    from megatron_tensor_transformer_gate_gb300 import inputs as I
+    k = scfg["kind"]
+    if k == "layer":
+        x = I.layer_inputs(scfg, seed, "cpu")
+    elif k == "mlp":
+        x = I.mlp_inputs(scfg, seed, "cpu")
+    else:
+        x = I.attn_inputs(scfg, seed, "cpu")
+    return {kk: I.to_f64(v) for kk, v in x.items()}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def sample_text(scfg, fl):
+    return (f"fp64 oracle fwd+bwd of the same block at b=1 s={scfg['s']} "
+            f"(full widths and heads), {fl / 1e12:.4f} TFLOP per step")
+
+
+def cpu_baseline(cfg, seed):
+    scfg = cpu_sample_cfg(cfg)
+    xs = oracle_inputs(scfg, seed)
+    fl = flops_per_step(scfg)
+    t0 = time.perf_counter()
+    run_oracle_step(scfg, xs)
+    t = time.perf_counter() - t0
+    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+            "kind": "oracle",
+            "sample": sample_text(scfg, fl) + f", {t:.2f} s"}
+
+
+# ------------------------------------------------------------------- main --
+def dist_setup(args):
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def reference_arm(args, cfg, world, rank):
+    """The oracle, as it stands, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    scfg = cpu_sample_cfg(cfg)
+    xs = oracle_inputs(scfg, 20260000)
+    fl = flops_per_step(scfg)
+    for _ in range(args.warmup):
+        run_oracle_step(scfg, xs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_step(scfg, xs)
+    el = time.perf_counter() - t0
+    val = fl * args.steps / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": dict(describe(cfg, args.mode), sample_tokens=scfg["s"]),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s",
+                         "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample_text(scfg, fl)},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def roofline(prof, steps, peaks, peaks_src):
+    fams = {k: v for k, v in prof.items() if v["launches"]}
+    total_ms = max(sum(v["ms"] for v in fams.values()), 1e-9)
+    kernels = {}
+    for k, v in fams.items():
+        kernels[k] = {
+            "launches_per_step": v["launches"] / steps,
+            "ms_per_step": v["ms"] / steps, "share": v["ms"] / total_ms,
+            "tflops": v["flops"] / (v["ms"] / 1e3) / 1e12 if v["ms"] else 0.0,
+            "gbs": v["bytes"] / (v["ms"] / 1e3) / 1e9 if v["ms"] else 0.0}
+    if not fams:
+        return None, kernels
+    dom = max(fams, key=lambda k: fams[k]["ms"])
+    v = fams[dom]
+    per_ms = v["ms"] / v["launches"]
+    if dom in ("gemm_tc", "attn_fwd", "attn_bwd_dkdv", "attn_bwd_dq"):
+        peak = float(peaks.get("bf16_tflops_sustained",
+                               peaks.get("bf16_tflops")))
+        ach = (v["flops"] / v["launches"]) / (per_ms / 1e3) / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "kernel": dom,
+                "peak_source": f"{peaks_src} bf16_tflops_sustained",
+                "flops_per_launch": v["flops"] / v["launches"],
+                "ms_per_launch": per_ms}, kernels
+    peak = float(peaks["hbm_gbs"])
+    ach = (v["bytes"] / v["launches"]) / (per_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+            "frac": ach / peak, "traffic": None, "kernel": dom,
+            "peak_source": f"{peaks_src} hbm_gbs",
+            "bytes_per_launch": v["bytes"] / v["launches"],
+            "ms_per_launch": per_ms}, kernels
+
+
+def main():
+    args = parse_args()
+    cfg = workload_cfg(args.workload, args.seq)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        reference_arm(args, cfg, world, rank)
+        return
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    from megatron_tensor_transformer_gate_gb300 import binding as B
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    peaks, peaks_src = load_peaks()
+    run = Runner(cfg, args.mode, 20260000 + rank, dev)
+    fl = flops_per_step(cfg)
+    flush = run.resident_bytes() < 3 * L2_BYTES
+    scrub = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+             if flush else None)
+    stream = torch.cuda.current_stream()
+    warmup = max(args.warmup, 3)
+    for _ in range(warmup):
+        run.step()
+    torch.cuda.synchronize()
+    B.device_status()
+
+    # ---- device-timed region: inputs resident in HBM
+    B.profile_enable(64 * (args.steps + 1))
+    B.profile_reset()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.5)
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    n0 = B.launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if scrub is not None:
+            scrub.zero_()
+        ev[i][0].record(stream)
+        run.step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = B.launch_count() - n0
+    clocks = sampler.stop()
+    prof = B.profile_read()
+    B.profile_enable(0)
+    B.device_status()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = fl * world / (ms / 1e3) / 1e12
+
+    # ---- end to end: pinned host activations in, results out, every step
+    e2e = None
+    if not args.no_e2e:
+        hX = run.x["X"].to("cpu").pin_memory()
+        hdO = run.x["dOut"].to("cpu").pin_memory()
+        dX_res = run.grads["dX"]
+        hOut = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
+        hdX = torch.empty(dX_res.shape, dtype=dX_res.dtype).pin_memory()
+        dXin = torch.empty_like(run.x["X"])
+        ddO = torch.empty_like(run.x["dOut"])
+        h2d = hX.numel() * hX.element_size() + hdO.numel() * hdO.element_size()
+        d2h = (hOut.numel() * hOut.element_size()
+               + hdX.numel() * hdX.element_size())
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            dXin.copy_(hX, non_blocking=True)
+            ddO.copy_(hdO, non_blocking=True)
+            run.step(dXin, ddO)
+            hOut.copy_(run.out, non_blocking=True)
+            hdX.copy_(dX_res, non_blocking=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ems = t0.elapsed_time(t1) / args.steps
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": fl * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": ems, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    roof, kernels = roofline(prof, args.steps, peaks, peaks_src)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, 20260000)
+
+    if rank == 0:
+        burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        sust = float(peaks.get("bf16_tflops_sustained", burst))
+        conf = describe(cfg, args.mode)
+        conf["l2"] = ("L2 flushed between timed steps" if flush else
+                      "inputs larger than L2 (no flush)")
+        conf["flops_per_step"] = fl
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": conf,
+            "pct_of_bf16_peak": 100.0 * value / world / burst,
+            "pct_of_bf16_peak_sustained": 100.0 * value / world / sust,
+            "peaks_source": peaks_src, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": launches, "roofline": roof, "kernels": kernels,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

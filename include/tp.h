@@ -218,6 +218,30 @@ tp_status tp_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K,
                   const void* B, int64_t ldb, int32_t b_mn_major, void* C,
                   int64_t ldc, tp_stream stream);
 
+
+/* ------------------------------------------------------------ profiling --
+ * Per-kernel-family device time for roofline reporting.  While enabled,
+ * every kernel the library launches is bracketed by two CUDA events recorded
+ * on that kernel's launch stream, tagged with its family and its algorithmic
+ * FLOPs and bytes.  tp_profile_enable(max_launches) creates the event pool
+ * (host-side CUDA event objects; no device buffers); 0 disables it and
+ * destroys the pool.  Launches beyond max_launches are not recorded.
+ * tp_profile_read synchronises the recorded events and returns, for one
+ * family, the number of recorded launches, their summed duration and their
+ * summed algorithmic FLOPs and bytes.  Families: 0 tcgen05 GEMM, 1 fp32
+ * GEMM, 2 attention forward, 3 attention backward dK/dV, 4 attention
+ * backward dQ, 5 shard-partial reduce, 6 other elementwise, 7 RMSNorm. */
+typedef struct {
+  uint64_t launches;
+  double ms;
+  double flops;
+  double bytes;
+} tp_profile_entry;
+
+tp_status tp_profile_enable(int32_t max_launches);
+tp_status tp_profile_reset(void);
+tp_status tp_profile_read(int32_t family, tp_profile_entry* out);
+
 /* ----------------------------------------------------------------- status */
 /* Synchronises `stream`, returns and clears the device status word
  * (TP_OK or TP_ERR_DEVICE_TIMEOUT), or TP_ERR_CUDA if the stream failed. */

@@ -52,6 +52,14 @@ class CommReport(ctypes.Structure):
         "total_page2")]
 
 
+class ProfileEntry(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_uint64), ("ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
+KERNEL_FAMILIES = ["gemm_tc", "gemm_simt", "attn_fwd", "attn_bwd_dkdv",
+                   "attn_bwd_dq", "reduce", "elementwise", "rmsnorm"]
+
 _P = ctypes.c_void_p
 _I64, _I32, _F, _SZ, _U64 = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
                              ctypes.c_size_t, ctypes.c_uint64)
@@ -81,6 +89,9 @@ SIGNATURES = {
     "tp_attn_flops": (_I32, [_AP, _U64P, _U64P]),
     "tp_gemm": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _I32, _P, _I64, _I32,
                        _P, _I64, _P]),
+    "tp_profile_enable": (_I32, [_I32]),
+    "tp_profile_reset": (_I32, []),
+    "tp_profile_read": (_I32, [_I32, ctypes.POINTER(ProfileEntry)]),
     "tp_device_status": (_I32, [_P]),
     "tp_status_string": (ctypes.c_char_p, [_I32]),
     "tp_launch_count": (_U64, []),
@@ -255,3 +266,23 @@ def device_status(stream=None):
 
 def launch_count():
     return lib().tp_launch_count()
+
+
+# ------------------------------------------------------------- profiling --
+def profile_enable(max_launches):
+    check(lib().tp_profile_enable(max_launches), "tp_profile_enable")
+
+
+def profile_reset():
+    check(lib().tp_profile_reset(), "tp_profile_reset")
+
+
+def profile_read():
+    """{family: {launches, ms, flops, bytes}} for every kernel family."""
+    out = {}
+    for i, name in enumerate(KERNEL_FAMILIES):
+        e = ProfileEntry()
+        check(lib().tp_profile_read(i, ctypes.byref(e)), "tp_profile_read")
+        out[name] = {"launches": e.launches, "ms": e.ms, "flops": e.flops,
+                     "bytes": e.bytes}
+    return out

@@ -13,6 +13,9 @@
 #include "common.cuh"
 #include "elementwise.h"
 #include "gemm.h"
+#include "profile.h"
+
+#include <vector>
 
 namespace tp {
 
@@ -63,6 +66,36 @@ unsigned* device_status_ptr() {
     g_status_ptr[dev] = static_cast<unsigned*>(p);
   }
   return g_status_ptr[dev];
+}
+
+// ---------------------------------------------------------------- profiler --
+namespace {
+struct ProfRec {
+  int family;
+  double flops, bytes;
+};
+struct Profiler {
+  std::mutex mu;
+  bool enabled = false;
+  int max = 0, used = 0;
+  std::vector<cudaEvent_t> ev;  // 2 per slot: start, end
+  std::vector<ProfRec> rec;
+};
+Profiler g_prof;
+}  // namespace
+
+ProfScope::ProfScope(void* s, int family, double flops, double bytes)
+    : slot(-1), stream(s) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.enabled || g_prof.used >= g_prof.max) return;
+  slot = g_prof.used++;
+  g_prof.rec[slot] = ProfRec{family, flops, bytes};
+  cudaEventRecord(g_prof.ev[2 * slot], static_cast<cudaStream_t>(s));
+}
+
+ProfScope::~ProfScope() {
+  if (slot >= 0)
+    cudaEventRecord(g_prof.ev[2 * slot + 1], static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace tp
@@ -745,6 +778,56 @@ extern "C" tp_status tp_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K,
     g.epi.ldo = ldc;
     return cuda_status(run_gemm(g, stream));
   });
+}
+
+
+// ------------------------------------------------------------- profiling --
+extern "C" tp_status tp_profile_enable(int32_t max_launches) {
+  return guarded([&]() -> tp_status {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    for (cudaEvent_t e : g_prof.ev)
+      if (e != nullptr) cudaEventDestroy(e);
+    g_prof.ev.clear();
+    g_prof.rec.clear();
+    g_prof.enabled = false;
+    g_prof.max = g_prof.used = 0;
+    if (max_launches <= 0) return TP_OK;
+    g_prof.ev.resize(2 * (size_t)max_launches, nullptr);
+    for (auto& e : g_prof.ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return TP_ERR_CUDA;
+    g_prof.rec.resize((size_t)max_launches);
+    g_prof.max = max_launches;
+    g_prof.enabled = true;
+    return TP_OK;
+  });
+}
+
+extern "C" tp_status tp_profile_reset(void) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  g_prof.used = 0;
+  return TP_OK;
+}
+
+extern "C" tp_status tp_profile_read(int32_t family, tp_profile_entry* out) {
+  if (out == nullptr) return TP_ERR_NULL;
+  if (family < 0 || family >= KF_COUNT) return TP_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  tp_profile_entry r = {0, 0.0, 0.0, 0.0};
+  for (int i = 0; i < g_prof.used; ++i) {
+    if (g_prof.rec[i].family != family) continue;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess)
+      return TP_ERR_CUDA;
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) !=
+        cudaSuccess)
+      return TP_ERR_CUDA;
+    r.launches += 1;
+    r.ms += ms;
+    r.flops += g_prof.rec[i].flops;
+    r.bytes += g_prof.rec[i].bytes;
+  }
+  *out = r;
+  return TP_OK;
 }
 
 // --------------------------------------------------------------- status --

@@ -21,6 +21,7 @@
 #include "attention.h"
 #include "common.cuh"
 #include "gemm.h"
+#include "profile.h"
 
 namespace tp {
 namespace {
@@ -661,6 +662,12 @@ __global__ void __launch_bounds__(BTHREADS)
   }
 }
 
+// unmasked (query, key) pairs per head
+double pairs(const AttnShape& sh) {
+  const double s = (double)sh.s;
+  return sh.causal ? s * (s + 1.0) / 2.0 : s * s;
+}
+
 template <typename K>
 cudaError_t set_smem(K kern, int bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -686,6 +693,9 @@ int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   a.causal = sh.causal;
   a.scale_log2 = sh.scale * LOG2E;
   dim3 grid((unsigned)((sh.s + FQ - 1) / FQ), (unsigned)sh.nq, (unsigned)sh.b);
+  const double core = 4.0 * sh.b * sh.nq * HD * pairs(sh);
+  ProfScope ps(stream, KF_ATTN_FWD, core,
+               2.0 * sh.b * sh.s * HD * (2.0 * sh.nq + 2.0 * sh.nkv));
   flash_fwd_kernel<<<grid, FTHREADS, FWD_SMEM,
                      static_cast<cudaStream_t>(stream)>>>(a);
   count_launch();
@@ -703,9 +713,15 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t rows = sh.b * sh.s;
   const int64_t warps = rows * sh.nq;
-  flash_bwd_dot_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(O),
-      static_cast<const __nv_bfloat16*>(dO), D, rows, sh.nq, sh.s);
+  const double core = 4.0 * sh.b * sh.nq * HD * pairs(sh);
+  const double io = 2.0 * sh.b * sh.s * HD;
+  {
+    ProfScope ps(stream, KF_ELEMENTWISE, 2.0 * rows * sh.nq * HD,
+                 2.0 * io * sh.nq);
+    flash_bwd_dot_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(O),
+        static_cast<const __nv_bfloat16*>(dO), D, rows, sh.nq, sh.s);
+  }
   BwdArgs a;
   a.Q = static_cast<const __nv_bfloat16*>(Q);
   a.K = static_cast<const __nv_bfloat16*>(K);
@@ -724,9 +740,18 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   a.scale_log2 = sh.scale * LOG2E;
   dim3 gkv((unsigned)((sh.s + BKV - 1) / BKV), (unsigned)sh.nkv,
            (unsigned)sh.b);
-  flash_bwd_dkdv_kernel<<<gkv, BTHREADS, BWD_SMEM, s>>>(a);
+  {
+    // algorithmic backward = 2 × forward: dP, dV, dK here, dQ below
+    ProfScope ps(stream, KF_ATTN_BWD_DKDV, 1.5 * core,
+                 io * (2.0 * sh.nq + 4.0 * sh.nkv));
+    flash_bwd_dkdv_kernel<<<gkv, BTHREADS, BWD_SMEM, s>>>(a);
+  }
   dim3 gq((unsigned)((sh.s + BQ - 1) / BQ), (unsigned)sh.nq, (unsigned)sh.b);
-  flash_bwd_dq_kernel<<<gq, BTHREADS, BWD_SMEM, s>>>(a);
+  {
+    ProfScope ps(stream, KF_ATTN_BWD_DQ, 0.5 * core,
+                 io * (3.0 * sh.nq + 2.0 * sh.nkv));
+    flash_bwd_dq_kernel<<<gq, BTHREADS, BWD_SMEM, s>>>(a);
+  }
   count_launch(3);
   return cudaGetLastError();
 }

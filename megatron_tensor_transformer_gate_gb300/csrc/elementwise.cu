@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "elementwise.h"
 #include "gemm.h"
+#include "profile.h"
 
 namespace tp {
 namespace {
@@ -312,6 +313,9 @@ int reduce_partials(const void* P, int n, int64_t rows, int64_t h,
   const int64_t count = rows * h;
   if (count == 0) return cudaSuccess;
   const int grid = grid_for(count / Vec<T>::N, 256);
+  ProfScope ps(stream, KF_REDUCE, (double)n * count,
+               (double)sizeof(T) * count *
+                   (n + 1 + (resid != nullptr ? 1 : 0)));
   reduce_partials_kernel<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const T*>(P), n, count, h, static_cast<const T*>(bias),
       static_cast<const T*>(resid), static_cast<T*>(out), d.enabled, d.thr,
@@ -325,6 +329,7 @@ int dropout_bwd(const void* dout, int64_t count, void* dz, const DropoutSpec& d,
                 void* stream) {
   if (count == 0) return cudaSuccess;
   const int grid = grid_for(count / Vec<T>::N, 256);
+  ProfScope ps(stream, KF_ELEMENTWISE, 0.0, 2.0 * sizeof(T) * count);
   dropout_bwd_kernel<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const T*>(dout), count, static_cast<T*>(dz), d.thr, d.scale,
       d.seed);
@@ -349,6 +354,8 @@ int colsum(const void* X, int64_t rows, int64_t cols, int64_t ld, void* out,
   const int64_t rpc = (rows + chunks - 1) / chunks;
   constexpr int V = Vec<T>::N;
   dim3 g1((unsigned)((cols + 32 * V - 1) / (32 * V)), (unsigned)chunks);
+  ProfScope ps(stream, KF_ELEMENTWISE, (double)rows * cols,
+               (double)sizeof(T) * rows * cols);
   colsum_stage1<T><<<g1, 256, 0, s>>>(static_cast<const T*>(X), rows, cols, ld,
                                       rpc, scratch);
   colsum_stage2<T><<<grid_for(cols, 256), 256, 0, s>>>(scratch, chunks, cols,
@@ -362,6 +369,7 @@ int rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
                 int64_t rows, int64_t h, float eps, void* stream) {
   if (rows == 0) return cudaSuccess;
   const int grid = (int)std::min<int64_t>(rows, (int64_t)device_sm_count() * 8);
+  ProfScope ps(stream, KF_NORM, 4.0 * rows * h, 2.0 * sizeof(T) * rows * h);
   rmsnorm_fwd_kernel<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const T*>(x), static_cast<const T*>(gamma),
       static_cast<T*>(y), rstd, rows, h, eps);
@@ -390,6 +398,8 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
   // columns per thread: 256 threads × V per sweep
   const int64_t sweeps = (h + 256 * V - 1) / (256 * V);
   if (sweeps > 8) return cudaErrorInvalidValue;
+  ProfScope ps(stream, KF_NORM, 8.0 * rows * h,
+               (double)sizeof(T) * rows * h * (dres != nullptr ? 4 : 3));
   const T* dyp = static_cast<const T*>(dy);
   const T* xp = static_cast<const T*>(x);
   const T* gp = static_cast<const T*>(gamma);

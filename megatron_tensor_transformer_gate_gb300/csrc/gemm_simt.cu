@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "gemm.h"
+#include "profile.h"
 
 namespace tp {
 namespace {
@@ -172,6 +173,13 @@ int launch_gemm_simt(const GemmProblem& pr, void* stream) {
             (unsigned)pr.nz);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  double ktile = 0.0;
+  for (int i = 0; i < pr.nparts; ++i)
+    ktile += (double)pr.parts[i].kseg * pr.parts[i].nsub;
+  const double ntot = (double)pr.N * (pr.epi.kind == EPI_SWIGLU ? 2.0 : 1.0);
+  ProfScope ps(s, KF_GEMM_SIMT, 2.0 * (double)pr.M * ntot * ktile * pr.nz,
+               4.0 * (((double)pr.M + ntot) * ktile + (double)pr.M * pr.N) *
+                   pr.nz);
   switch (pr.epi.kind) {
     case EPI_STORE: gemm_simt_kernel<EPI_STORE><<<grid, 256, 0, s>>>(p); break;
     case EPI_GELU: gemm_simt_kernel<EPI_GELU><<<grid, 256, 0, s>>>(p); break;

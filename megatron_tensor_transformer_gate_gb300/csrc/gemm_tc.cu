@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "gemm.h"
+#include "profile.h"
 
 namespace tp {
 namespace {
@@ -455,7 +456,8 @@ bool encode_operand(CUtensorMap* m, const GemmOperand& o, int64_t kseg,
 }
 
 template <int A_MN, int B_MN, int EPI>
-int launch_inst(const TcParams& prm, int grid, cudaStream_t s) {
+int launch_inst(const TcParams& prm, int grid, cudaStream_t s, double flops,
+                double bytes) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -464,7 +466,10 @@ int launch_inst(const TcParams& prm, int grid, cudaStream_t s) {
                                     SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gemm_tc_kernel<A_MN, B_MN, EPI><<<grid, THREADS, SMEM_BYTES, s>>>(prm);
+  {
+    ProfScope ps(s, KF_GEMM_TC, flops, bytes);
+    gemm_tc_kernel<A_MN, B_MN, EPI><<<grid, THREADS, SMEM_BYTES, s>>>(prm);
+  }
   count_launch();
   return cudaGetLastError();
 }
@@ -512,24 +517,35 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
   if (prm.total_tiles == 0) return cudaSuccess;
   const int grid = std::min(prm.total_tiles, device_sm_count());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // algorithmic work of the launch: 2·M·N·K per batch, both B halves for
+  // SwiGLU; bytes = operands read once + outputs written once
+  double ktile = 0.0;
+  for (int i = 0; i < pr.nparts; ++i)
+    ktile += (double)pr.parts[i].kseg * pr.parts[i].nsub;
+  const double ntot = (double)pr.N * (e.kind == EPI_SWIGLU ? 2.0 : 1.0);
+  const double flops = 2.0 * (double)pr.M * ntot * ktile * pr.nz;
+  const int outs = e.kind == EPI_SWIGLU ? 3
+                   : (e.kind == EPI_GELU || e.kind == EPI_DSWIGLU) ? 2 : 1;
+  const double bytes = 2.0 * (((double)pr.M + ntot) * ktile * pr.nz +
+                              (double)pr.M * pr.N * pr.nz * outs);
 
   switch (e.kind) {
     case EPI_STORE:
-      if (!a_mn && !b_mn) return launch_inst<0, 0, EPI_STORE>(prm, grid, s);
-      if (!a_mn && b_mn) return launch_inst<0, 1, EPI_STORE>(prm, grid, s);
-      if (a_mn && b_mn) return launch_inst<1, 1, EPI_STORE>(prm, grid, s);
-      return launch_inst<1, 0, EPI_STORE>(prm, grid, s);
+      if (!a_mn && !b_mn) return launch_inst<0, 0, EPI_STORE>(prm, grid, s, flops, bytes);
+      if (!a_mn && b_mn) return launch_inst<0, 1, EPI_STORE>(prm, grid, s, flops, bytes);
+      if (a_mn && b_mn) return launch_inst<1, 1, EPI_STORE>(prm, grid, s, flops, bytes);
+      return launch_inst<1, 0, EPI_STORE>(prm, grid, s, flops, bytes);
     case EPI_GELU:
       if (a_mn || b_mn) return cudaErrorInvalidValue;
-      return launch_inst<0, 0, EPI_GELU>(prm, grid, s);
+      return launch_inst<0, 0, EPI_GELU>(prm, grid, s, flops, bytes);
     case EPI_SWIGLU:
-      return launch_inst<0, 0, EPI_SWIGLU>(prm, grid, s);
+      return launch_inst<0, 0, EPI_SWIGLU>(prm, grid, s, flops, bytes);
     case EPI_DGELU:
       if (a_mn || !b_mn) return cudaErrorInvalidValue;
-      return launch_inst<0, 1, EPI_DGELU>(prm, grid, s);
+      return launch_inst<0, 1, EPI_DGELU>(prm, grid, s, flops, bytes);
     case EPI_DSWIGLU:
       if (a_mn || !b_mn) return cudaErrorInvalidValue;
-      return launch_inst<0, 1, EPI_DSWIGLU>(prm, grid, s);
+      return launch_inst<0, 1, EPI_DSWIGLU>(prm, grid, s, flops, bytes);
   }
   return cudaErrorInvalidValue;
 }

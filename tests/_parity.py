@@ -1,7 +1,14 @@
 """Error metrics of the GPU-vs-oracle parity tests.
 
-bf16 workloads (fp32 accumulation): per tensor ‖g − o‖_F / ‖o‖_F ≤ 1e-2 and
-max|g − o| / rms(o) ≤ 3e-2.  fp32 workloads: max|g − o| / max|o| ≤ 1e-4.
+bf16 workloads (fp32 accumulation): per tensor ‖g − o‖_F / ‖o‖_F ≤ 1e-2, and
+the max-abs/rms ratio ≤ 3e-2 taken row by row — max_j |g − o|_rj ≤ 3e-2 ·
+rms_j(o_rj) for every row r (a token for activations and their gradients, an
+output feature for weight gradients; 1-D tensors are one row).  Row by row,
+because a tensor-wide rms is unattainable for bf16 storage when rows differ in
+scale: in causal attention the first tokens attend to few keys and are 15–18×
+the tensor rms, so even the exact result rounded to bf16 has a tensor-wide
+max/rms of ≈4e-2.
+fp32 workloads: max|g − o| / max|o| ≤ 1e-4 per tensor.
 """
 
 import numpy as np
@@ -19,12 +26,18 @@ def f64(t):
 
 
 def errors(g, o):
+    """(Frobenius rel. error, worst row max-abs/rms, tensor max rel. error)."""
     g, o = f64(g), f64(o)
     d = g - o
+    if d.size == 0:
+        return 0.0, 0.0, 0.0
     fro = np.linalg.norm(d) / max(np.linalg.norm(o), 1e-300)
-    rms = np.sqrt(np.mean(o * o)) if o.size else 0.0
-    maxrms = np.abs(d).max() / max(rms, 1e-300) if d.size else 0.0
-    maxrel = np.abs(d).max() / max(np.abs(o).max(), 1e-300) if d.size else 0.0
+    d2 = d.reshape(-1, d.shape[-1]) if d.ndim > 1 else d.reshape(1, -1)
+    o2 = o.reshape(d2.shape)
+    rms = np.sqrt(np.mean(o2 * o2, axis=1))
+    rowmax = np.abs(d2).max(axis=1)
+    maxrms = float((rowmax / np.maximum(rms, 1e-300)).max())
+    maxrel = np.abs(d).max() / max(np.abs(o).max(), 1e-300)
     return fro, maxrms, maxrel
 
 
@@ -34,5 +47,5 @@ def check(g, o, name, dtype="bf16"):
         assert maxrel <= F32_MAXREL, f"{name}: max rel {maxrel:.3e}"
     else:
         assert fro <= BF16_FRO and maxrms <= BF16_MAXRMS, \
-            f"{name}: fro {fro:.3e}, max/rms {maxrms:.3e}"
+            f"{name}: fro {fro:.3e}, row max/rms {maxrms:.3e}"
     return fro, maxrms, maxrel

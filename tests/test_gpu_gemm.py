@@ -10,7 +10,7 @@ from _parity import f64
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(128, 256, 64), (200, 264, 136), (384, 520, 1000), (1, 8, 8),
+SHAPES = [(128, 256, 64), (200, 264, 136), (384, 520, 1000), (8, 8, 8),
           (1000, 24, 72)]
 
 
@@ -35,7 +35,7 @@ def test_gemm_bf16_layouts(tp, a_mn, b_mn, M, N, K):
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
 def test_gemm_f32(tp, a_mn, b_mn):
-    M, N, K = 130, 70, 200
+    M, N, K = 130, 72, 200
     g = torch.Generator().manual_seed(5)
     A = torch.randn(M, K, generator=g)
     Bm = torch.randn(N, K, generator=g)
@@ -58,3 +58,24 @@ def test_gemm_large_k_many_tiles(tp):
     tp.gemm(A.cuda(), Bm.cuda(), C)
     tp.device_status()
     assert np.abs(f64(C) - ref).max() <= 8e-3 * np.abs(ref).max()
+
+
+def test_gemm_single_row(tp):
+    # M = 1 (K-major A only: an MN-major A would need a leading dimension of 1)
+    g = torch.Generator().manual_seed(3)
+    A = torch.randn(1, 72, generator=g).to(torch.bfloat16)
+    Bm = torch.randn(40, 72, generator=g).to(torch.bfloat16)
+    C = torch.empty((1, 40), dtype=torch.bfloat16, device="cuda")
+    tp.gemm(A.cuda(), Bm.cuda(), C)
+    tp.device_status()
+    ref = f64(A) @ f64(Bm).T
+    assert np.abs(f64(C) - ref).max() <= 8e-3 * np.abs(ref).max()
+
+
+def test_gemm_rejects_unaligned_leading_dim(tp):
+    A = torch.zeros(8, 1, dtype=torch.bfloat16, device="cuda")  # [K, M=1]
+    Bm = torch.zeros(8, 8, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(1, 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tp.TPError) as e:
+        tp.gemm(A, Bm, C, a_mn_major=True)
+    assert e.value.code == 2

@@ -77,17 +77,15 @@ def test_bf16_gelu_bias_dropout_workload(tp, mode):
 
 
 def test_dropout_mask_bit_exact(tp):
-    # where the oracle's mask drops an element, Out must equal R exactly;
-    # where it keeps one, Out − R must not be zero (Z + b2 ≠ 0 there)
+    # no residual: a dropped element is exactly 0, a kept one is
+    # (Z + b2)/(1 − p) ≠ 0; the zero pattern must equal the oracle's mask
     cfg = I.workload("mlp_gelu_bf16", b=2, s=128, h=256, h_ffn=512, n=2,
-                     residual="random", p=0.3)
-    res, out, fo = run_case(tp, cfg, 0, 99)
-    x = I.mlp_inputs(cfg, 99, "cpu")
-    keep = oracle.dropout_keep(99, 256, 256, 0.3)
-    R = x["R"].cuda()
-    same = (out == R).cpu().numpy()
-    assert (same[~keep]).all()
-    assert not same[keep].any()
+                     residual=None, p=0.3)
+    for mode in (0, 1):
+        res, out, fo = run_case(tp, cfg, mode, 99)
+        keep = oracle.dropout_keep(99, 256, 256, 0.3)
+        zero = (out == 0).cpu().numpy()
+        assert (zero == ~keep).all()
 
 
 @pytest.mark.parametrize("mode", [0, 1])
