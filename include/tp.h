@@ -36,8 +36,9 @@
  *  - Errors: argument, shape and workspace errors are returned before any
  *    launch, with nothing enqueued.  A failed launch returns TP_ERR_CUDA.
  *    Device-side waits are bounded; one that runs out records a device status
- *    word that tp_device_status() returns as TP_ERR_DEVICE_TIMEOUT.  No C++
- *    exception crosses this boundary.
+ *    word that tp_device_status() returns as TP_ERR_DEVICE_TIMEOUT (or
+ *    TP_ERR_RANGE for an fp16 overflow).  No C++ exception crosses this
+ *    boundary.
  */
 #ifndef TP_H_
 #define TP_H_
@@ -58,7 +59,8 @@ typedef enum {
   TP_ERR_UNSUPPORTED = 5,     /* valid but not implemented (e.g. d != 128) */
   TP_ERR_CUDA = 6,            /* a CUDA runtime/driver call failed */
   TP_ERR_DEVICE_TIMEOUT = 7,  /* a bounded device wait ran out */
-  TP_ERR_ARG = 8              /* misaligned pointer or other bad argument */
+  TP_ERR_ARG = 8,             /* misaligned pointer or other bad argument */
+  TP_ERR_RANGE = 9            /* an fp16 attention operand overflowed */
 } tp_status;
 
 typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;            /* δ = 4 or 2 */
@@ -142,8 +144,12 @@ typedef struct {
   int32_t mode;       /* tp_reduce_mode */
 } tp_attn_desc;
 
-/* ws: Q, K, V, O (dtype) and LSE [b, n_q, s] fp32 saved for backward, then
- * the forward scratch (n partial [T, h] tensors in materialised mode). */
+/* ws: Q, K, V (fp16), O (bf16) and LSE [b, n_q, s] fp32 saved for backward,
+ * then the forward scratch (n partial [T, h] tensors in materialised mode).
+ * The attention core multiplies fp16 operands with fp32 accumulation (Q, K,
+ * V, dO in fp16; the probabilities and their gradients rounded to fp16):
+ * |Q|, |K|, |V|, |dO| must stay below 65504, else tp_device_status reports
+ * TP_ERR_RANGE. */
 size_t tp_attn_workspace_bytes(const tp_attn_desc* d);
 /* scratch: dO, dQ, dK, dV, D = rowsum(dO∘O) [b, n_q, s] fp32, partials and
  * column-sum partials. */
@@ -244,7 +250,8 @@ tp_status tp_profile_read(int32_t family, tp_profile_entry* out);
 
 /* ----------------------------------------------------------------- status */
 /* Synchronises `stream`, returns and clears the device status word
- * (TP_OK or TP_ERR_DEVICE_TIMEOUT), or TP_ERR_CUDA if the stream failed. */
+ * (TP_OK, TP_ERR_DEVICE_TIMEOUT or TP_ERR_RANGE), or TP_ERR_CUDA if the
+ * stream failed. */
 tp_status tp_device_status(tp_stream stream);
 const char* tp_status_string(tp_status s);
 /* Number of kernels this library has launched since load (host counter). */

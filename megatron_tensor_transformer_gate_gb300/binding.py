@@ -20,7 +20,7 @@ SCOPE_MLP, SCOPE_ATTN, SCOPE_LAYER = 0, 1, 2
 
 STATUS = {0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_DTYPE",
           4: "TP_ERR_WORKSPACE", 5: "TP_ERR_UNSUPPORTED", 6: "TP_ERR_CUDA",
-          7: "TP_ERR_DEVICE_TIMEOUT", 8: "TP_ERR_ARG"}
+          7: "TP_ERR_DEVICE_TIMEOUT", 8: "TP_ERR_ARG", 9: "TP_ERR_RANGE"}
 
 
 class TPError(RuntimeError):

@@ -582,15 +582,14 @@ extern "C" tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X,
     const int64_t qd = (int64_t)d->n_q * d->d, kd = (int64_t)d->n_kv * d->d;
     const int n = d->n;
     // column-parallel Q, K, V projections (each rank's heads are a column
-    // block of the same output)
-    int err = run_gemm(proj(T, qd, op(X, h, 0, T), op(Wq, h, 0, qd), h, L.q, qd),
-                       stream);
-    if (!err)
-      err = run_gemm(proj(T, kd, op(X, h, 0, T), op(Wk, h, 0, kd), h, L.k, kd),
-                     stream);
-    if (!err)
-      err = run_gemm(proj(T, kd, op(X, h, 0, T), op(Wv, h, 0, kd), h, L.v, kd),
-                     stream);
+    // block, written in fp16 for the attention core)
+    GemmProblem gq = proj(T, qd, op(X, h, 0, T), op(Wq, h, 0, qd), h, L.q, qd);
+    GemmProblem gk = proj(T, kd, op(X, h, 0, T), op(Wk, h, 0, kd), h, L.k, kd);
+    GemmProblem gv = proj(T, kd, op(X, h, 0, T), op(Wv, h, 0, kd), h, L.v, kd);
+    gq.epi.out_f16 = gk.epi.out_f16 = gv.epi.out_f16 = 1;
+    int err = run_gemm(gq, stream);
+    if (!err) err = run_gemm(gk, stream);
+    if (!err) err = run_gemm(gv, stream);
     if (err) return cuda_status(err);
     err = flash_fwd(attn_shape(d), L.q, L.k, L.v, L.o, L.lse, stream);
     if (err) return cuda_status(err);
@@ -646,9 +645,10 @@ extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
       if (err) return cuda_status(err);
     }
     // dO = dOut·Wo (local), dWo = dOutᵀ·O
-    err = run_gemm(proj(T, qd, op(dOut, h, 0, T), op(Wo, qd, 1, qd), h, L.dO,
-                        qd),
-                   stream);
+    GemmProblem gdo = proj(T, qd, op(dOut, h, 0, T), op(Wo, qd, 1, qd), h,
+                           L.dO, qd);
+    gdo.epi.out_f16 = 1;   // attention-core operand
+    err = run_gemm(gdo, stream);
     if (!err)
       err = run_gemm(proj(h, qd, op(dOut, h, 1, h), op(F.o, qd, 1, qd), T, dWo,
                           qd),
@@ -844,7 +844,7 @@ extern "C" tp_status tp_device_status(tp_stream stream) {
     if (cudaMemcpy(p, zero, sizeof(zero), cudaMemcpyHostToDevice) !=
         cudaSuccess)
       return TP_ERR_CUDA;
-    return TP_ERR_DEVICE_TIMEOUT;
+    return h[0] == kDevRange ? TP_ERR_RANGE : TP_ERR_DEVICE_TIMEOUT;
   }
   return TP_OK;
 }
@@ -860,6 +860,7 @@ extern "C" const char* tp_status_string(tp_status s) {
     case TP_ERR_CUDA: return "CUDA call failed";
     case TP_ERR_DEVICE_TIMEOUT: return "a bounded device wait timed out";
     case TP_ERR_ARG: return "misaligned pointer or bad argument";
+    case TP_ERR_RANGE: return "an attention-core operand exceeded the fp16 range";
   }
   return "unknown status";
 }

@@ -8,6 +8,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -16,7 +17,7 @@ namespace tp {
 // ----------------------------------------------------------------- status --
 // Device status word layout: [0] = first error code (0 = none), [1] = site id
 // of the wait that ran out, [2] = block id.  Written once (first error wins).
-enum DeviceError : unsigned { kDevOk = 0, kDevTimeout = 7 };
+enum DeviceError : unsigned { kDevOk = 0, kDevTimeout = 7, kDevRange = 9 };
 
 // About two seconds at the GB300's 2.07 GHz maximum SM clock.
 constexpr long long kWaitTimeoutCycles = 4LL << 30;
@@ -258,6 +259,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
+  __half2 v = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(v);
+}
+// Largest finite fp16 value.
+constexpr float kF16Max = 65504.0f;
+
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
   __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
   return __bfloat1622float2(v);

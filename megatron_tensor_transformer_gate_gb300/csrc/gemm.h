@@ -60,6 +60,9 @@ struct GemmEpilogue {
   uint32_t drop_thr = 0;
   float drop_scale = 1.0f;
   uint64_t seed = 0;
+  // EPI_STORE only: write fp16 instead of bf16 (the attention-core operands);
+  // a value beyond the fp16 range records a range error in the status word
+  int out_f16 = 0;
 };
 
 struct GemmProblem {

@@ -110,6 +110,30 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst,
   }
 }
 
+__device__ __forceinline__ void store32_f16(__half* dst, const float* v,
+                                            int valid, unsigned* status) {
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) bad |= (i < valid) && !(fabsf(v[i]) <= kF16Max);
+  if (bad) record_error(status, kDevRange, 5);
+  if (valid >= 32) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 u;
+      u.x = pack_f16x2(v[8 * q + 0], v[8 * q + 1]);
+      u.y = pack_f16x2(v[8 * q + 2], v[8 * q + 3]);
+      u.z = pack_f16x2(v[8 * q + 4], v[8 * q + 5]);
+      u.w = pack_f16x2(v[8 * q + 6], v[8 * q + 7]);
+      d[q] = u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < valid) dst[i] = __float2half_rn(v[i]);
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p,
                                               uint32_t taddr, int z, int m,
@@ -178,9 +202,12 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p,
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] += rr[i];
         }
-        store32_bf16(static_cast<__nv_bfloat16*>(e.out) +
-                         (int64_t)z * e.out_z_stride + (int64_t)m * e.ldo + n,
-                     v, valid);
+        const int64_t off =
+            (int64_t)z * e.out_z_stride + (int64_t)m * e.ldo + n;
+        if (e.out_f16)
+          store32_f16(static_cast<__half*>(e.out) + off, v, valid, p.status);
+        else
+          store32_bf16(static_cast<__nv_bfloat16*>(e.out) + off, v, valid);
       } else if constexpr (EPI == EPI_GELU) {
         if (e.bias != nullptr) {
           float b[32];

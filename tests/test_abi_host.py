@@ -133,5 +133,5 @@ def test_attn_rejects_before_launch(tp):
 
 def test_status_strings(tp):
     L = tp.lib()
-    for code in range(9):
-        assert L.tp_status_string(code)
+    for code in range(10):
+        assert L.tp_status_string(code) != b"unknown status"

@@ -56,3 +56,18 @@ def test_mqa_single_kv_per_rank(tp, mode):
 @pytest.mark.parametrize("mode", [0, 1])
 def test_gqa_workload(tp, mode):
     run_case(tp, I.workload("attn_gqa_bf16"), mode, 20260004)
+
+
+def test_fp16_overflow_is_reported(tp):
+    # inputs scaled so that Q = X·Wqᵀ exceeds the fp16 range: the library
+    # must report TP_ERR_RANGE through the device status word (no fault)
+    cfg = I.workload("attn_gqa_bf16", b=1, s=64, h=256, n_q=2, n_kv=1, n=1,
+                     w_std="fan_in")
+    x = I.attn_inputs(cfg, 33, "cuda")
+    X = (x["X"].float() * 1e5).to(x["X"].dtype)
+    a = TPAttention(1, 64, 256, 2, 1, 128, 1)
+    a.forward(X, x["Wq"], x["Wk"], x["Wv"], x["Wo"])
+    with pytest.raises(tp.TPError) as e:
+        tp.device_status()
+    assert e.value.code == 9
+    tp.device_status()          # the word was cleared by the read

@@ -35,7 +35,7 @@ def test_gemm_bf16_layouts(tp, a_mn, b_mn, M, N, K):
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
 def test_gemm_f32(tp, a_mn, b_mn):
-    M, N, K = 130, 72, 200
+    M, N, K = 136, 72, 200
     g = torch.Generator().manual_seed(5)
     A = torch.randn(M, K, generator=g)
     Bm = torch.randn(N, K, generator=g)
