@@ -77,19 +77,24 @@ def test_bf16_gelu_bias_dropout_workload(tp, mode):
 
 
 def test_dropout_mask_bit_exact(tp):
-    # no residual: a dropped element is exactly 0, a kept one is
-    # (Z + b2)/(1 − p) ≠ 0; the zero pattern must equal the oracle's mask
+    # no residual: a dropped element must be exactly 0.  A kept element is
+    # (Z + b2)/(1 − p); it can only be 0 through an exact cancellation, which
+    # the materialised mode's bf16 shard partials make possible for values
+    # that are tiny anyway — so a kept zero must be tiny in the oracle too.
     cfg = I.workload("mlp_gelu_bf16", b=2, s=128, h=256, h_ffn=512, n=2,
                      residual=None, p=0.3)
+    keep = oracle.dropout_keep(99, 256, 256, 0.3)
     for mode in (0, 1):
         res, out, fo = run_case(tp, cfg, mode, 99)
-        keep = oracle.dropout_keep(99, 256, 256, 0.3)
         zero = (out == 0).cpu().numpy()
-        kept_zero = int((zero & keep).sum())
-        dropped_nonzero = int((~zero & ~keep).sum())
-        assert kept_zero == 0 and dropped_nonzero == 0, \
-            f"mode {mode}: {kept_zero} kept-but-zero, {dropped_nonzero} " \
-            f"dropped-but-nonzero of {keep.size}"
+        assert not (~zero & ~keep).any(), f"mode {mode}: dropped but nonzero"
+        o = fo["Out"]
+        rms = np.sqrt((o * o).mean(axis=1, keepdims=True))
+        suspicious = zero & keep & (np.abs(o) > 1e-2 * rms)
+        assert not suspicious.any(), \
+            f"mode {mode}: {int(suspicious.sum())} kept elements zeroed"
+        if mode == 0:
+            assert not (zero & keep).any()
 
 
 @pytest.mark.parametrize("mode", [0, 1])
