@@ -186,6 +186,25 @@ tp_status tp_rmsnorm_bwd(int64_t T, int64_t h, float eps, int32_t dtype,
                          void* dgamma, void* scratch, size_t scratch_bytes,
                          tp_stream stream);
 
+/* The same RMSNorm backward for callers that cannot allocate device memory:
+ * code that runs under another framework's memory pool, a real-time loop
+ * where cudaMalloc (which can synchronise the device and stall) is not
+ * allowed after start-up, or an embedding that hands the library only its
+ * input and output tensors.  There is no counterpart on the pages; this is a
+ * service of the library.  The dγ partial sums go to a fixed 8 MiB device
+ * array inside the library instead of a caller scratch buffer, so h must be
+ * at most TP_RMSNORM_NOALLOC_MAX_H (TP_ERR_WORKSPACE otherwise).  The first
+ * call on each device looks up that array's device address (no allocation);
+ * make it before capturing a stream.  All calls share the array: calls that
+ * overlap on the GPU (other streams, other threads) race and must be
+ * serialised by the caller.  Results equal tp_rmsnorm_bwd's. */
+#define TP_RMSNORM_NOALLOC_MAX_H 8192
+tp_status tp_rmsnorm_bwd_noalloc(int64_t T, int64_t h, float eps,
+                                 int32_t dtype, const void* dy, const void* x,
+                                 const void* gamma, const float* rstd,
+                                 const void* dres, void* dx, void* dgamma,
+                                 tp_stream stream);
+
 /* ----------------------------------------------------------- accounting --
  * Host-only, exact integer figures; no GPU needed.
  * Communication ([Grasp-TP] §5; [Troverld] §II.II; [adu-TP] 通信开销): each

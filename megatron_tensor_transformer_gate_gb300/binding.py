@@ -83,6 +83,8 @@ SIGNATURES = {
     "tp_rmsnorm_bwd_scratch_bytes": (_SZ, [_I64, _I64]),
     "tp_rmsnorm_bwd": (_I32, [_I64, _I64, _F, _I32, _P, _P, _P, _P, _P, _P,
                               _P, _P, _SZ, _P]),
+    "tp_rmsnorm_bwd_noalloc": (_I32, [_I64, _I64, _F, _I32, _P, _P, _P, _P,
+                                      _P, _P, _P, _P]),
     "tp_comm_bytes": (_I32, [_I32, _I64, _I64, _I32, _I32,
                              ctypes.POINTER(CommReport)]),
     "tp_mlp_flops": (_I32, [_MP, _U64P, _U64P]),
@@ -258,6 +260,17 @@ def rmsnorm_bwd(dy, x, gamma, rstd, dx, dgamma, scratch, dres=None, eps=1e-5,
                                ptr(dgamma), ptr(scratch),
                                scratch.numel() * scratch.element_size(),
                                stream_handle(stream)), "tp_rmsnorm_bwd")
+
+
+def rmsnorm_bwd_noalloc(dy, x, gamma, rstd, dx, dgamma, dres=None, eps=1e-5,
+                        stream=None):
+    """RMSNorm backward without caller scratch (see tp_rmsnorm_bwd_noalloc)."""
+    T, h = x.shape
+    check(lib().tp_rmsnorm_bwd_noalloc(T, h, eps, dtype_code(x), ptr(dy),
+                                       ptr(x), ptr(gamma), ptr(rstd),
+                                       ptr(dres), ptr(dx), ptr(dgamma),
+                                       stream_handle(stream)),
+          "tp_rmsnorm_bwd_noalloc")
 
 
 def device_status(stream=None):

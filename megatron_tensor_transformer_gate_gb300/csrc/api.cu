@@ -751,6 +751,31 @@ extern "C" tp_status tp_rmsnorm_bwd(int64_t T, int64_t h, float eps,
   });
 }
 
+extern "C" tp_status tp_rmsnorm_bwd_noalloc(int64_t T, int64_t h, float eps,
+                                            int32_t dtype, const void* dy,
+                                            const void* x, const void* gamma,
+                                            const float* rstd,
+                                            const void* dres, void* dx,
+                                            void* dgamma, tp_stream stream) {
+  (void)eps;  // rstd carries ε from the forward call
+  return guarded([&]() -> tp_status {
+    if (dtype != TP_F32 && dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (T < 1 || h < 8 || h % 8 || h > 16384) return TP_ERR_SHAPE;
+    if (h > TP_RMSNORM_NOALLOC_MAX_H) return TP_ERR_WORKSPACE;
+    if (!dy || !x || !gamma || !rstd || !dx || !dgamma) return TP_ERR_NULL;
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) ||
+        !aligned16(rstd) || !aligned16(dx) || !opt_aligned(dres))
+      return TP_ERR_ARG;
+    const int err =
+        dtype == TP_F32
+            ? rmsnorm_bwd_noalloc<float>(dy, x, gamma, rstd, dres, dx, dgamma,
+                                         T, h, stream)
+            : rmsnorm_bwd_noalloc<__nv_bfloat16>(dy, x, gamma, rstd, dres, dx,
+                                                 dgamma, T, h, stream);
+    return cuda_status(err);
+  });
+}
+
 // ----------------------------------------------------------------- GEMM --
 extern "C" tp_status tp_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K,
                              const void* A, int64_t lda, int32_t a_mn_major,

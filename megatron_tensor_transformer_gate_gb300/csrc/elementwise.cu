@@ -12,6 +12,7 @@
 // count and grid-stride.
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "elementwise.h"
@@ -439,5 +440,62 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
 TP_INST(float)
 TP_INST(__nv_bfloat16)
 #undef TP_INST
+
+// ------------------------------------------- RMSNorm backward, no allocation --
+// Callers that cannot allocate device memory (see tp_rmsnorm_bwd_noalloc) get
+// the dγ partial sums in this fixed array instead of a caller scratch buffer:
+// one fp32 row of h partial sums per row chunk, at most 256 chunks × 8192
+// columns = 8 MiB, held by every GPU that loads the library until the process
+// exits.  Every chunk row that a call uses is fully written by that call
+// before it is read, so nothing has to be cleared between calls; calls that
+// overlap on the GPU share the array and race.
+static __device__ __align__(256) float
+    g_norm_scratch[256 * kNoallocNormMaxH];
+
+namespace {
+std::mutex g_norm_mu;
+float* g_norm_ptr[64];
+}  // namespace
+
+// Device address of g_norm_scratch for the current device.  The host-side
+// name of a __device__ array is only a stand-in for it, so the address is
+// looked up once per device (with that device current) and cached.
+int norm_scratch_address(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_norm_mu);
+  if (g_norm_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_norm_scratch);
+    if (e != cudaSuccess) return e;
+    g_norm_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_norm_ptr[dev];
+  return cudaSuccess;
+}
+
+template <typename T>
+int rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* gamma,
+                        const float* rstd, const void* dres, void* dx,
+                        void* dgamma, int64_t rows, int64_t h, void* stream) {
+  if (h > kNoallocNormMaxH ||
+      rmsnorm_bwd_scratch(rows, h) > sizeof(g_norm_scratch))
+    return cudaErrorInvalidValue;
+  float* scratch = nullptr;
+  const int e = norm_scratch_address(&scratch);
+  if (e != cudaSuccess) return e;
+  return rmsnorm_bwd<T>(dy, x, gamma, rstd, dres, dx, dgamma, scratch, rows, h,
+                        stream);
+}
+
+template int rmsnorm_bwd_noalloc<float>(const void*, const void*, const void*,
+                                        const float*, const void*, void*,
+                                        void*, int64_t, int64_t, void*);
+template int rmsnorm_bwd_noalloc<__nv_bfloat16>(const void*, const void*,
+                                                const void*, const float*,
+                                                const void*, void*, void*,
+                                                int64_t, int64_t, void*);
 
 }  // namespace tp

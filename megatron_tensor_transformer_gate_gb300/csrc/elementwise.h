@@ -37,4 +37,12 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
                 const float* rstd, const void* dres, void* dx, void* dgamma,
                 float* scratch, int64_t rows, int64_t h, void* stream);
 
+// The RMSNorm backward with its dγ partial sums in a fixed device array
+// (no caller scratch); h ≤ kNoallocNormMaxH.
+constexpr int64_t kNoallocNormMaxH = 8192;
+template <typename T>
+int rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* gamma,
+                        const float* rstd, const void* dres, void* dx,
+                        void* dgamma, int64_t rows, int64_t h, void* stream);
+
 }  // namespace tp
