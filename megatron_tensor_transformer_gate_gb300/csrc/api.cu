@@ -591,7 +591,8 @@ extern "C" tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X,
     if (!err) err = run_gemm(gk, stream);
     if (!err) err = run_gemm(gv, stream);
     if (err) return cuda_status(err);
-    err = flash_fwd(attn_shape(d), L.q, L.k, L.v, L.o, L.lse, stream);
+    err = flash_fwd(attn_shape(d), L.q, L.k, L.v, L.o, L.lse,
+                    device_status_ptr(), stream);
     if (err) return cuda_status(err);
     // row-parallel output projection + g reduction + bias + residual
     GemmProblem g = proj(T, h, op(L.o, qd, 0, T), op(Wo, qd, 0, h), qd, Out, h);

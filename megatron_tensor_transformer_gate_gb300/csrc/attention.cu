@@ -7,13 +7,13 @@
 //
 // Head dim d = 128.  Tiles live in shared memory with 16-byte chunks XOR-
 // swizzled by (row mod 8) so that ldmatrix reads are bank-conflict free;
-// products use mma.sync m16n8k16 with fp16 operands and fp32 accumulation:
+// The forward pass runs on tcgen05 (attn_fwd_tc.cu); this file holds the
+// backward.  Products use mma.sync m16n8k16 with fp16 operands and fp32
+// accumulation:
 // Q, K, V and dO arrive in fp16 and P, dS are rounded to fp16, because the
 // softmax amplifies score errors and bf16 operands (8-bit mantissa) put the
 // row-wise error of causal outputs above 3e-2 of the row rms; O, dQ, dK, dV
 // are written in bf16 for the bf16 projection GEMMs that consume them.
-//   forward   block = 128 query rows of one (batch, q head), 8 warps × 16
-//             rows, K/V blocks of 64 keys double-buffered with cp.async.
 //   backward  (1) D = rowsum(dO ∘ O);  (2) dK/dV: block = 64 keys of one kv
 //             head, looping over the group's q heads and the query blocks at
 //             or after the keys (GQA sums stay inside the block);
@@ -124,178 +124,6 @@ __device__ __forceinline__ void ldb_frag_kn(uint32_t tile, int k0, int d0,
   const int r = k0 + (lane & 7) + ((lane >> 3) & 1) * 8;
   const int c = d0 + (lane >> 4) * 8;
   ldsm_x4_t(tile + swz(r, c), b[0], b[1], b[2], b[3]);
-}
-
-// ------------------------------------------------------------------ forward --
-constexpr int FQ = 128, FK = 64, FWARPS = 8, FTHREADS = FWARPS * 32;
-constexpr int FWD_SMEM = FQ * ROW_BYTES + 2 * 2 * FK * ROW_BYTES;  // 96 KB
-
-struct FwdArgs {
-  const __half *Q, *K, *V;
-  __nv_bfloat16* O;
-  float* LSE;
-  int64_t s;
-  int nq, nkv, causal;
-  float scale_log2;
-};
-
-__global__ void __launch_bounds__(FTHREADS, 1)
-    flash_fwd_kernel(const FwdArgs a) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  const uint32_t sQ = smem_u32(sm);
-  const uint32_t sK0 = sQ + FQ * ROW_BYTES;
-  const uint32_t sV0 = sK0 + 2 * FK * ROW_BYTES;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int b = blockIdx.z, j = blockIdx.y;
-  const int nqb = gridDim.x;
-  const int64_t q0 = (int64_t)(nqb - 1 - blockIdx.x) * FQ;
-  const int kvh = j / (a.nq / a.nkv);
-  const int64_t ldq = (int64_t)a.nq * HD, ldk = (int64_t)a.nkv * HD;
-  const __half* Qb = a.Q + (int64_t)b * a.s * ldq + j * HD;
-  const __half* Kb = a.K + (int64_t)b * a.s * ldk + kvh * HD;
-  const __half* Vb = a.V + (int64_t)b * a.s * ldk + kvh * HD;
-  const int64_t kv_end = a.causal ? min(a.s, q0 + (int64_t)FQ) : a.s;
-  const int nkb = (int)((kv_end + FK - 1) / FK);
-
-  load_tile<FQ, FTHREADS>(sQ, Qb, ldq, q0, a.s);
-  load_tile<FK, FTHREADS>(sK0, Kb, ldk, 0, a.s);
-  load_tile<FK, FTHREADS>(sV0, Vb, ldk, 0, a.s);
-  cp_commit();
-
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
-  uint32_t qf[8][4];
-  const int64_t row_a = q0 + warp * 16 + g, row_b = row_a + 8;
-
-  for (int kb = 0; kb < nkb; ++kb) {
-    const int st = kb & 1;
-    if (kb + 1 < nkb) {
-      const uint32_t nk = sK0 + (st ^ 1) * FK * ROW_BYTES;
-      const uint32_t nv = sV0 + (st ^ 1) * FK * ROW_BYTES;
-      load_tile<FK, FTHREADS>(nk, Kb, ldk, (int64_t)(kb + 1) * FK, a.s);
-      load_tile<FK, FTHREADS>(nv, Vb, ldk, (int64_t)(kb + 1) * FK, a.s);
-      cp_commit();
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
-    }
-    __syncthreads();
-    if (kb == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) lda_frag(sQ, warp * 16, kk, qf[kk]);
-    }
-    const uint32_t sK = sK0 + st * FK * ROW_BYTES;
-    const uint32_t sV = sV0 + st * FK * ROW_BYTES;
-    float sc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t bf[4];
-        ldb_frag_nk(sK, np * 16, kk, bf);
-        mma16816(sc[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], bf[0],
-                 bf[1]);
-        mma16816(sc[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
-                 bf[2], bf[3]);
-      }
-    }
-    // mask, scale, online softmax
-    const int64_t k0 = (int64_t)kb * FK;
-    const bool need_mask = (k0 + FK > a.s) || (a.causal && k0 + FK - 1 > q0);
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = sc[nt][e] * a.scale_log2;
-        if (need_mask) {
-          const int64_t key = k0 + nt * 8 + 2 * t + (e & 1);
-          const int64_t row = (e < 2) ? row_a : row_b;
-          if (key >= a.s || (a.causal && key > row)) v = -INFINITY;
-        }
-        sc[nt][e] = v;
-        mx[e >> 1] = fmaxf(mx[e >> 1], v);
-      }
-    }
-    float alpha[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float m_new = fmaxf(m_run[r], mx[r]);
-      alpha[r] = exp2f(m_run[r] - m_new);
-      m_run[r] = m_new;
-      l_run[r] *= alpha[r];
-    }
-    uint32_t pf[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const float p0 = exp2f(sc[nt][0] - m_run[0]);
-      const float p1 = exp2f(sc[nt][1] - m_run[0]);
-      const float p2 = exp2f(sc[nt][2] - m_run[1]);
-      const float p3 = exp2f(sc[nt][3] - m_run[1]);
-      l_run[0] += p0 + p1;
-      l_run[1] += p2 + p3;
-      pf[nt >> 1][(nt & 1) * 2 + 0] = pack_f16x2(p0, p1);
-      pf[nt >> 1][(nt & 1) * 2 + 1] = pack_f16x2(p2, p3);
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= alpha[0];
-      o[i][1] *= alpha[0];
-      o[i][2] *= alpha[1];
-      o[i][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        uint32_t bf[4];
-        ldb_frag_kn(sV, kk * 16, dp * 16, bf);
-        mma16816(o[2 * dp], pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3], bf[0],
-                 bf[1]);
-        mma16816(o[2 * dp + 1], pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3],
-                 bf[2], bf[3]);
-      }
-    }
-    __syncthreads();
-  }
-  // finalize: O /= l, LSE = ln(l) + m·ln2 (m in log2 units)
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
-    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
-  }
-  const float inv0 = 1.0f / l_run[0], inv1 = 1.0f / l_run[1];
-  // stage this warp's 16 rows in the (now free) Q tile, then 16-byte stores
-  const int wr = warp * 16;
-#pragma unroll
-  for (int dt = 0; dt < 16; ++dt) {
-    const int col = dt * 8 + 2 * t;
-    *reinterpret_cast<uint32_t*>(sm + swz(wr + g, col)) =
-        pack_bf16x2(o[dt][0] * inv0, o[dt][1] * inv0);
-    *reinterpret_cast<uint32_t*>(sm + swz(wr + g + 8, col)) =
-        pack_bf16x2(o[dt][2] * inv1, o[dt][3] * inv1);
-  }
-  __syncwarp();
-  __nv_bfloat16* Ob = a.O + (int64_t)b * a.s * ldq + j * HD;
-  for (int idx = lane; idx < 16 * 16; idx += 32) {
-    const int r = idx >> 4, c = idx & 15;
-    const int64_t row = q0 + wr + r;
-    if (row < a.s)
-      *reinterpret_cast<uint4*>(Ob + row * ldq + c * 8) =
-          *reinterpret_cast<const uint4*>(sm + swz(wr + r, c * 8));
-  }
-  if (t == 0) {
-    float* L = a.LSE + ((int64_t)b * a.nq + j) * a.s;
-    if (row_a < a.s) L[row_a] = (m_run[0] + log2f(l_run[0])) * 0.69314718055994531f;
-    if (row_b < a.s) L[row_b] = (m_run[1] + log2f(l_run[1])) * 0.69314718055994531f;
-  }
 }
 
 // ------------------------------------------------------------ backward: D --
@@ -679,32 +507,6 @@ cudaError_t set_smem(K kern, int bytes) {
 }
 
 }  // namespace
-
-int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
-              void* O, float* LSE, void* stream) {
-  if (sh.d != HD) return cudaErrorInvalidValue;
-  static cudaError_t e = set_smem(flash_fwd_kernel, FWD_SMEM);
-  if (e != cudaSuccess) return e;
-  FwdArgs a;
-  a.Q = static_cast<const __half*>(Q);
-  a.K = static_cast<const __half*>(K);
-  a.V = static_cast<const __half*>(V);
-  a.O = static_cast<__nv_bfloat16*>(O);
-  a.LSE = LSE;
-  a.s = sh.s;
-  a.nq = sh.nq;
-  a.nkv = sh.nkv;
-  a.causal = sh.causal;
-  a.scale_log2 = sh.scale * LOG2E;
-  dim3 grid((unsigned)((sh.s + FQ - 1) / FQ), (unsigned)sh.nq, (unsigned)sh.b);
-  const double core = 4.0 * sh.b * sh.nq * HD * pairs(sh);
-  ProfScope ps(stream, KF_ATTN_FWD, core,
-               2.0 * sh.b * sh.s * HD * (2.0 * sh.nq + 2.0 * sh.nkv));
-  flash_fwd_kernel<<<grid, FTHREADS, FWD_SMEM,
-                     static_cast<cudaStream_t>(stream)>>>(a);
-  count_launch();
-  return cudaGetLastError();
-}
 
 int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
               const void* O, const void* dO, const float* LSE, float* D,

@@ -15,8 +15,9 @@ struct AttnShape {
   float scale;  // 1/√d
 };
 
+// Forward on tcgen05 (attn_fwd_tc.cu); Q, K, V fp16, O bf16.
 int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
-              void* O, float* LSE, void* stream);
+              void* O, float* LSE, unsigned* status, void* stream);
 // dQ, dK, dV (bf16, GQA groups summed); D [b, nq, s] fp32 scratch;
 // dq_acc [T, nq·d] fp32 scratch.
 int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,

@@ -1,0 +1,345 @@
+// attn_fwd_tc.cu — causal GQA flash-attention forward on tcgen05 / TMEM.
+//
+// The attention core of one rank's local heads ([Grasp-TP] §4: softmax per
+// head over the sequence; [Troverld] §I.O FlashAttention: row-blocked with an
+// online softmax, O(S) statistics written for the backward pass).
+//
+// One CTA = 128 query rows of one (batch, q head); 192 threads:
+//   warp 0     TMA: the Q tile once, then K_j and V_j (128 keys each) into a
+//              2-stage ring (fp16, 128-byte swizzle, two 64-column halves).
+//   warp 1     allocates 512 TMEM columns and issues, per key block j,
+//                S_j = Q·K_jᵀ   (M=128, N=128, K=128) into TMEM S[j mod 2]
+//                O_j = P_j·V_j  (M=128, N=128, K=128) into TMEM O
+//              in the order S_0, S_1, O_0, S_2, O_1, … so the tensor cores
+//              compute S_{j+1} while the softmax works on S_j.
+//   warps 2–5  softmax, one thread per query row (its TMEM lane): running
+//              max m and sum l in fp32, P_j = exp2(S·scale·log2e − m) written
+//              as fp16 into the K-major swizzled layout the MMA reads, and
+//              the output accumulated in registers, o ← o·exp2(m_old − m_new)
+//              + O_j.  The epilogue writes O / l (bf16) and
+//              LSE = (m + log2 l)·ln 2.
+// Operands are fp16 (see attention.cu for why), accumulation fp32.
+#include <cuda_fp16.h>
+
+#include <cstring>
+
+#include "attention.h"
+#include "common.cuh"
+#include "gemm.h"
+#include "profile.h"
+
+namespace tp {
+namespace {
+
+constexpr int HD = 128;
+constexpr int BLK = 128;                 // queries per CTA, keys per block
+constexpr int ATOM = BLK * 128;          // one 64-column half: 128 rows × 128 B
+constexpr int TILE = 2 * ATOM;           // 32 KB fp16 tile [128][128]
+constexpr int THREADS = 192;
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + TILE;      // 2 stages
+constexpr int OFF_V = OFF_K + 2 * TILE;  // 2 stages
+constexpr int OFF_P = OFF_V + 2 * TILE;
+constexpr int OFF_BAR = OFF_P + TILE;
+constexpr int SMEM = OFF_BAR + 256 + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_O = 256;
+
+struct FwdTcArgs {
+  CUtensorMap mq, mk, mv;
+  __nv_bfloat16* O;
+  float* LSE;
+  int s, nq, nkv, causal;
+  float scale_log2;
+  unsigned* status;
+};
+
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk) {
+  // K-major tile of two 64-column halves: K step kk (16 columns)
+  return smem_desc_sw128(base + (kk >> 2) * ATOM + (kk & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
+  // MN-major B (V: rows = keys = K, two 64-wide d halves ATOM apart)
+  return smem_desc_sw128(base + kk * 2048, ATOM, 1024);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ FwdTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint64_t* q_full = bar + 0;
+  uint64_t* kv_full = bar + 1;    // [2]
+  uint64_t* kv_empty = bar + 3;   // [2]
+  uint64_t* s_full = bar + 5;     // [2]
+  uint64_t* p_full = bar + 7;
+  uint64_t* o_full = bar + 8;
+  uint64_t* o_empty = bar + 9;
+  uint64_t* drain = bar + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 11);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, j = blockIdx.y;
+  const int q0 = (gridDim.x - 1 - blockIdx.x) * BLK;
+  const int kvh = j / (a.nq / a.nkv);
+  const int kv_end = a.causal ? min(a.s, q0 + BLK) : a.s;
+  const int nkb = (kv_end + BLK - 1) / BLK;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------- TMA --
+      tma_prefetch_desc(&a.mq);
+      tma_prefetch_desc(&a.mk);
+      tma_prefetch_desc(&a.mv);
+      uint32_t armed = 0, armed_par = 0;
+      mbar_arrive_expect_tx(q_full, TILE);
+      for (int hh = 0; hh < 2; ++hh)
+        tma_load_3d(sm + OFF_Q + hh * ATOM, &a.mq, q_full, j * HD + hh * 64,
+                    q0, b);
+      for (int jb = 0; jb < nkb; ++jb) {
+        const int st = jb & 1;
+        const uint32_t ph = (jb >> 1) & 1;
+        if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, a.status, 11)) break;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * TILE);
+        armed |= 1u << st;
+        armed_par = (armed_par & ~(1u << st)) | (ph << st);
+        for (int hh = 0; hh < 2; ++hh) {
+          tma_load_3d(sm + OFF_K + st * TILE + hh * ATOM, &a.mk, &kv_full[st],
+                      kvh * HD + hh * 64, jb * BLK, b);
+          tma_load_3d(sm + OFF_V + st * TILE + hh * ATOM, &a.mv, &kv_full[st],
+                      kvh * HD + hh * 64, jb * BLK, b);
+        }
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        mbar_wait(q_full, 0, &no_abort, nullptr, 0);
+        for (int st = 0; st < 2; ++st)
+          if (armed & (1u << st))
+            mbar_wait(&kv_full[st], (armed_par >> st) & 1u, &no_abort, nullptr,
+                      0);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------- MMA --
+      constexpr uint32_t IDESC_S = idesc_f16_f32(128, 128, 0, 0);
+      constexpr uint32_t IDESC_O = idesc_f16_f32(128, 128, 0, 1);
+      const uint32_t sQ = smem_u32(sm + OFF_Q), sP = smem_u32(sm + OFF_P);
+      bool ok = mbar_wait(q_full, 0, abort_flag, a.status, 12);
+      auto pv = [&](int i) -> bool {
+        if (!mbar_wait(p_full, i & 1, abort_flag, a.status, 13)) return false;
+        if (i >= 1 &&
+            !mbar_wait(o_empty, (i - 1) & 1, abort_flag, a.status, 14))
+          return false;
+        tc_fence_after();
+        const uint32_t sV = smem_u32(sm + OFF_V + (i & 1) * TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem + COL_O, desc_kmajor(sP, kk), desc_mnmajor(sV, kk),
+                     IDESC_O, kk > 0 ? 1u : 0u);
+        tc_commit(o_full);
+        tc_commit(&kv_empty[i & 1]);
+        return true;
+      };
+      for (int jb = 0; ok && jb < nkb; ++jb) {
+        const int st = jb & 1;
+        if (!mbar_wait(&kv_full[st], (jb >> 1) & 1, abort_flag, a.status, 15)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sK = smem_u32(sm + OFF_K + st * TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem + st * 128, desc_kmajor(sQ, kk), desc_kmajor(sK, kk),
+                     IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(&s_full[st]);
+        if (jb >= 1) ok = pv(jb - 1);
+      }
+      if (ok) pv(nkb - 1);
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        tc_commit(drain);
+        mbar_wait(drain, 0, &no_abort, nullptr, 0);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- softmax --
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qi = q0 + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    uint8_t* sP = sm + OFF_P;
+    float o[HD];
+#pragma unroll
+    for (int i = 0; i < HD; ++i) o[i] = 0.0f;
+    float m_run = -INFINITY, l_run = 0.0f;
+    bool ok = true;
+    for (int jb = 0; jb < nkb; ++jb) {
+      const int st = jb & 1;
+      if (!mbar_wait(&s_full[st], (jb >> 1) & 1, abort_flag, a.status, 16)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = jb * BLK;
+      const bool masked = (k0 + BLK > a.s) || (a.causal && k0 + BLK - 1 > q0);
+      const uint32_t sa = lane_base + st * 128;
+      // pass 1: row max of the scaled, masked scores
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(sa + c * 32, v);
+        tmem_ld_wait(v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = k0 + c * 32 + i;
+          float x = __uint_as_float(v[i]) * a.scale_log2;
+          if (masked && (key >= a.s || (a.causal && key > qi))) x = -INFINITY;
+          mx = fmaxf(mx, x);
+        }
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = exp2f(m_run - m_new);
+      m_run = m_new;
+      // pass 2: P = exp2(x − m), row sum, fp16 into the swizzled K-major tile
+      float sum = 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(sa + c * 32, v);
+        tmem_ld_wait(v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int key = k0 + c * 32 + i;
+          float x0 = __uint_as_float(v[i]) * a.scale_log2;
+          float x1 = __uint_as_float(v[i + 1]) * a.scale_log2;
+          if (masked && (key >= a.s || (a.causal && key > qi))) x0 = -INFINITY;
+          if (masked && (key + 1 >= a.s || (a.causal && key + 1 > qi)))
+            x1 = -INFINITY;
+          const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
+          sum += p0 + p1;
+          pk[i >> 1] = pack_f16x2(p0, p1);
+        }
+        // keys c·32 … c·32+31 = 4 chunks of 8 in half (c >> 1)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = (c & 1) * 4 + q;
+          uint8_t* dst = sP + (c >> 1) * ATOM + r * 128 +
+                         ((chunk ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      l_run = l_run * alpha + sum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      // O_j = P_j·V_j is ready once the MMA warp commits it
+      if (!mbar_wait(o_full, jb & 1, abort_flag, a.status, 17)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + COL_O + c * 32, v);
+        tmem_ld_wait(v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          o[c * 32 + i] = o[c * 32 + i] * alpha + __uint_as_float(v[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(o_empty);
+    }
+    if (ok && qi < a.s) {
+      const float inv = 1.0f / l_run;
+      __nv_bfloat16* dst =
+          a.O + ((int64_t)b * a.s + qi) * (int64_t)(a.nq * HD) + j * HD;
+#pragma unroll
+      for (int q = 0; q < HD / 8; ++q) {
+        uint4 u;
+        u.x = pack_bf16x2(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
+        u.y = pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+        u.z = pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+        u.w = pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+        reinterpret_cast<uint4*>(dst)[q] = u;
+      }
+      a.LSE[((int64_t)b * a.nq + j) * a.s + qi] =
+          (m_run + log2f(l_run)) * 0.69314718055994531f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
+              void* O, float* LSE, unsigned* status, void* stream) {
+  if (sh.d != HD) return cudaErrorInvalidValue;
+  static cudaError_t e = cudaFuncSetAttribute(
+      attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  FwdTcArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t ldq = (uint64_t)sh.nq * HD * 2, ldk = (uint64_t)sh.nkv * HD * 2;
+  // dims {columns, positions, batch}: rows past a sequence's end read as zero
+  if (!encode_tmap_3d_f16(&a.mq, Q, (uint64_t)sh.nq * HD, sh.s, sh.b, ldq,
+                          ldq * sh.s, 64, BLK, 1) ||
+      !encode_tmap_3d_f16(&a.mk, K, (uint64_t)sh.nkv * HD, sh.s, sh.b, ldk,
+                          ldk * sh.s, 64, BLK, 1) ||
+      !encode_tmap_3d_f16(&a.mv, V, (uint64_t)sh.nkv * HD, sh.s, sh.b, ldk,
+                          ldk * sh.s, 64, BLK, 1))
+    return cudaErrorInvalidValue;
+  a.O = static_cast<__nv_bfloat16*>(O);
+  a.LSE = LSE;
+  a.s = (int)sh.s;
+  a.nq = sh.nq;
+  a.nkv = sh.nkv;
+  a.causal = sh.causal;
+  a.scale_log2 = sh.scale * 1.4426950408889634f;
+  a.status = status;
+  dim3 grid((unsigned)((sh.s + BLK - 1) / BLK), (unsigned)sh.nq,
+            (unsigned)sh.b);
+  const double s = (double)sh.s;
+  const double pairs = sh.causal ? s * (s + 1.0) / 2.0 : s * s;
+  {
+    ProfScope ps(stream, KF_ATTN_FWD, 4.0 * sh.b * sh.nq * HD * pairs,
+                 2.0 * sh.b * sh.s * HD * (2.0 * sh.nq + 2.0 * sh.nkv));
+    attn_fwd_tc_kernel<<<grid, THREADS, SMEM,
+                         static_cast<cudaStream_t>(stream)>>>(a);
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace tp

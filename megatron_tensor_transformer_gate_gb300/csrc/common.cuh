@@ -214,6 +214,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr,
   return d;
 }
 
+// The same for fp16 A and B (format code 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn,
+                                                     int b_mn) {
+  return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor-core operand reads) before signalling the MMA issuer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
 // A/B major-ness (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4 at 24.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn,

@@ -13,6 +13,7 @@
 //    its own segments and writes a partial that a reduce kernel sums.
 #pragma once
 
+#include <cuda.h>
 #include <stdint.h>
 
 namespace tp {
@@ -77,6 +78,12 @@ struct GemmProblem {
 // Launchers (return a cudaError_t value; 0 = success).
 int launch_gemm_tc(const GemmProblem& p, void* stream, unsigned* status);
 int launch_gemm_simt(const GemmProblem& p, void* stream);
+
+// 3-D fp16 tensor map with 128-byte swizzle (dims d0 innermost; strides in
+// bytes for d1, d2); false if the driver entry point or the encode fails.
+bool encode_tmap_3d_f16(CUtensorMap* m, const void* base, uint64_t d0,
+                        uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+                        uint32_t b0, uint32_t b1, uint32_t b2);
 
 // Number of SMs of the current device.
 int device_sm_count();

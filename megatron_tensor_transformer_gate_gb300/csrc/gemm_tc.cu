@@ -503,6 +503,21 @@ int launch_inst(const TcParams& prm, int grid, cudaStream_t s, double flops,
 
 }  // namespace
 
+bool encode_tmap_3d_f16(CUtensorMap* m, const void* base, uint64_t d0,
+                        uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+                        uint32_t b0, uint32_t b1, uint32_t b2) {
+  if (!get_encode()) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
   if (!get_encode()) return cudaErrorNotSupported;
   const GemmEpilogue& e = pr.epi;
