@@ -9,14 +9,15 @@
 //              2-stage ring (fp16, 128-byte swizzle, two 64-column halves).
 //   warp 1     allocates 512 TMEM columns and issues, per key block j,
 //                S_j = Q·K_jᵀ   (M=128, N=128, K=128) into TMEM S[j mod 2]
-//                O_j = P_j·V_j  (M=128, N=128, K=128) into TMEM O
-//              in the order S_0, S_1, O_0, S_2, O_1, … so the tensor cores
+//                O += P_j·V_j   (M=128, N=128, K=128) into TMEM O
+//              in the order S_0, S_1, PV_0, S_2, PV_1, … so the tensor cores
 //              compute S_{j+1} while the softmax works on S_j.
-//   warps 2–5  softmax, one thread per query row (its TMEM lane): running
+//   warps 2–5  softmax, one thread per query row (its TMEM lane): reference
 //              max m and sum l in fp32, P_j = exp2(S·scale·log2e − m) written
-//              as fp16 into the K-major swizzled layout the MMA reads, and
-//              the output accumulated in registers, o ← o·exp2(m_old − m_new)
-//              + O_j.  The epilogue writes O / l (bf16) and
+//              as fp16 into the K-major swizzled layout the MMA reads (two
+//              buffers).  O accumulates in TMEM; when a block's max exceeds
+//              m by more than 2^8 the softmax rescales O and l by
+//              exp2(m − m_new) first.  The epilogue writes O / l (bf16) and
 //              LSE = (m + log2 l)·ln 2.
 // Operands are fp16 (see attention.cu for why), accumulation fp32.
 #include <cuda_fp16.h>
@@ -39,11 +40,16 @@ constexpr int THREADS = 192;
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + TILE;      // 2 stages
 constexpr int OFF_V = OFF_K + 2 * TILE;  // 2 stages
-constexpr int OFF_P = OFF_V + 2 * TILE;
-constexpr int OFF_BAR = OFF_P + TILE;
+constexpr int OFF_P = OFF_V + 2 * TILE;  // 2 buffers
+constexpr int OFF_BAR = OFF_P + 2 * TILE;
 constexpr int SMEM = OFF_BAR + 256 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
+// The output accumulates in TMEM against a reference max m; it is rescaled
+// only when a block's row max exceeds m by more than this (log2 units), which
+// keeps the fp16 probabilities ≤ 2^8 and the fp32 accumulator far from
+// overflow.
+constexpr float RESCALE_LOG2 = 8.0f;
 
 struct FwdTcArgs {
   CUtensorMap mq, mk, mv;
@@ -73,11 +79,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* kv_full = bar + 1;    // [2]
   uint64_t* kv_empty = bar + 3;   // [2]
   uint64_t* s_full = bar + 5;     // [2]
-  uint64_t* p_full = bar + 7;
-  uint64_t* o_full = bar + 8;
-  uint64_t* o_empty = bar + 9;
-  uint64_t* drain = bar + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 11);
+  uint64_t* p_full = bar + 7;     // [2]
+  uint64_t* pv_done = bar + 9;    // [2]
+  uint64_t* drain = bar + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -93,10 +98,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
       mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&pv_done[i], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(o_full, 1);
-    mbar_init(o_empty, 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -148,18 +152,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t IDESC_O = idesc_f16_f32(128, 128, 0, 1);
       const uint32_t sQ = smem_u32(sm + OFF_Q), sP = smem_u32(sm + OFF_P);
       bool ok = mbar_wait(q_full, 0, abort_flag, a.status, 12);
+      // O += P_i·V_i; the softmax rescaled O (if needed) before p_full[i]
       auto pv = [&](int i) -> bool {
-        if (!mbar_wait(p_full, i & 1, abort_flag, a.status, 13)) return false;
-        if (i >= 1 &&
-            !mbar_wait(o_empty, (i - 1) & 1, abort_flag, a.status, 14))
+        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, a.status, 13))
           return false;
         tc_fence_after();
         const uint32_t sV = smem_u32(sm + OFF_V + (i & 1) * TILE);
+        const uint32_t sPi = sP + (i & 1) * TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem + COL_O, desc_kmajor(sP, kk), desc_mnmajor(sV, kk),
-                     IDESC_O, kk > 0 ? 1u : 0u);
-        tc_commit(o_full);
+          tc_mma_f16(tmem + COL_O, desc_kmajor(sPi, kk), desc_mnmajor(sV, kk),
+                     IDESC_O, (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&pv_done[i & 1]);
         tc_commit(&kv_empty[i & 1]);
         return true;
       };
@@ -191,61 +195,92 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = quarter * 32 + lane;
     const int qi = q0 + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint8_t* sP = sm + OFF_P;
-    float o[HD];
-#pragma unroll
-    for (int i = 0; i < HD; ++i) o[i] = 0.0f;
-    float m_run = -INFINITY, l_run = 0.0f;
+    float m_ref = -INFINITY, l_run = 0.0f;
     bool ok = true;
     for (int jb = 0; jb < nkb; ++jb) {
       const int st = jb & 1;
-      if (!mbar_wait(&s_full[st], (jb >> 1) & 1, abort_flag, a.status, 16)) {
+      if (!mbar_wait_warp(&s_full[st], (jb >> 1) & 1, abort_flag, a.status, 16)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      uint32_t v[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + st * 128 + c * 32, v[c]);
+      tmem_ld_wait(v[0]);
+      reg_fence32(v[1]);
+      reg_fence32(v[2]);
+      reg_fence32(v[3]);
+      // scaled scores (log2 units), masked; row max with 8 independent chains
       const int k0 = jb * BLK;
       const bool masked = (k0 + BLK > a.s) || (a.causal && k0 + BLK - 1 > q0);
-      const uint32_t sa = lane_base + st * 128;
-      // pass 1: row max of the scaled, masked scores
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(sa + c * 32, v);
-        tmem_ld_wait(v);
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int key = k0 + c * 32 + i;
-          float x = __uint_as_float(v[i]) * a.scale_log2;
-          if (masked && (key >= a.s || (a.causal && key > qi))) x = -INFINITY;
-          mx = fmaxf(mx, x);
+          float x = __uint_as_float(v[c][i]) * a.scale_log2;
+          if (masked) {
+            const int key = k0 + c * 32 + i;
+            if (key >= a.s || (a.causal && key > qi)) x = -INFINITY;
+          }
+          v[c][i] = __float_as_uint(x);
+          mx8[i & 7] = fmaxf(mx8[i & 7], x);
         }
-      }
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = exp2f(m_run - m_new);
-      m_run = m_new;
-      // pass 2: P = exp2(x − m), row sum, fp16 into the swizzled K-major tile
-      float sum = 0.0f;
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      if (jb == 0) {
+        m_ref = mx;
+      } else if (__any_sync(0xffffffffu, mx > m_ref + RESCALE_LOG2)) {
+        // rescale the TMEM accumulator once O += P_{j-1}·V_{j-1} has landed;
+        // the whole warp takes part (TMEM access is warp-collective), rows
+        // that keep their reference scale by 1
+        const int pj = jb - 1;
+        if (!mbar_wait_warp(&pv_done[pj & 1], (pj >> 1) & 1, abort_flag,
+                            a.status, 17)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float m_new = mx > m_ref + RESCALE_LOG2 ? mx : m_ref;
+        const float alpha = ex2_approx(m_ref - m_new);
 #pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + COL_O + c * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(lane_base + COL_O + c * 32, o);
+        }
+        l_run *= alpha;
+        m_ref = m_new;
+      }
+      // P buffer st is free once O += P_{j-2}·V_{j-2} has completed
+      if (jb >= 2 && !mbar_wait_warp(&pv_done[st], ((jb - 2) >> 1) & 1,
+                                     abort_flag, a.status, 18)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sP = sm + OFF_P + st * TILE;
+      float sum8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(sa + c * 32, v);
-        tmem_ld_wait(v);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const int key = k0 + c * 32 + i;
-          float x0 = __uint_as_float(v[i]) * a.scale_log2;
-          float x1 = __uint_as_float(v[i + 1]) * a.scale_log2;
-          if (masked && (key >= a.s || (a.causal && key > qi))) x0 = -INFINITY;
-          if (masked && (key + 1 >= a.s || (a.causal && key + 1 > qi)))
-            x1 = -INFINITY;
-          const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
-          sum += p0 + p1;
+          const float p0 = ex2_approx(__uint_as_float(v[c][i]) - m_ref);
+          const float p1 = ex2_approx(__uint_as_float(v[c][i + 1]) - m_ref);
+          sum8[i & 7] += p0;
+          sum8[(i + 1) & 7] += p1;
           pk[i >> 1] = pack_f16x2(p0, p1);
         }
-        // keys c·32 … c·32+31 = 4 chunks of 8 in half (c >> 1)
+        // keys c·32 … c·32+31 = four 8-key chunks of half (c >> 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int chunk = (c & 1) * 4 + q;
@@ -255,43 +290,45 @@ __global__ void __launch_bounds__(THREADS, 1)
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
-      l_run = l_run * alpha + sum;
+      l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+               ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
-      // O_j = P_j·V_j is ready once the MMA warp commits it
-      if (!mbar_wait(o_full, jb & 1, abort_flag, a.status, 17)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + COL_O + c * 32, v);
-        tmem_ld_wait(v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          o[c * 32 + i] = o[c * 32 + i] * alpha + __uint_as_float(v[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(o_empty);
+      mbar_arrive(&p_full[st]);
     }
-    if (ok && qi < a.s) {
+    // epilogue: wait for the last O += P·V, then O / l and the LSE
+    const int last = nkb - 1;
+    if (__all_sync(0xffffffffu, ok) &&
+        mbar_wait_warp(&pv_done[last & 1], (last >> 1) & 1, abort_flag,
+                       a.status, 19)) {
+      tc_fence_after();
       const float inv = 1.0f / l_run;
       __nv_bfloat16* dst =
           a.O + ((int64_t)b * a.s + qi) * (int64_t)(a.nq * HD) + j * HD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + COL_O + c * 32, o);
+        tmem_ld_wait(o);
+        if (qi < a.s) {
 #pragma unroll
-      for (int q = 0; q < HD / 8; ++q) {
-        uint4 u;
-        u.x = pack_bf16x2(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
-        u.y = pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-        u.z = pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-        u.w = pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
-        reinterpret_cast<uint4*>(dst)[q] = u;
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv,
+                              __uint_as_float(o[8 * q + 1]) * inv);
+            u.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv,
+                              __uint_as_float(o[8 * q + 3]) * inv);
+            u.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv,
+                              __uint_as_float(o[8 * q + 5]) * inv);
+            u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv,
+                              __uint_as_float(o[8 * q + 7]) * inv);
+            reinterpret_cast<uint4*>(dst)[c * 4 + q] = u;
+          }
+        }
       }
-      a.LSE[((int64_t)b * a.nq + j) * a.s + qi] =
-          (m_run + log2f(l_run)) * 0.69314718055994531f;
+      if (qi < a.s)
+        a.LSE[((int64_t)b * a.nq + j) * a.s + qi] =
+            (m_ref + log2f(l_run)) * 0.69314718055994531f;
     }
   }
 

@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       decode_tile(p, t, z, mt, nt);
       const int buf = it & 1;
       const uint32_t aphase = (it >> 1) & 1;
-      if (!mbar_wait(&tfull[buf], aphase, abort_flag, p.status, 4)) break;
+      if (!mbar_wait_warp(&tfull[buf], aphase, abort_flag, p.status, 4)) break;
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN;
