@@ -12,10 +12,11 @@
 //                O += P_j·V_j   (M=128, N=128, K=128) into TMEM O
 //              in the order S_0, S_1, PV_0, S_2, PV_1, … so the tensor cores
 //              compute S_{j+1} while the softmax works on S_j.
-//   warps 2–5  softmax, one thread per query row (its TMEM lane): reference
+//   warps 2–9  softmax, two threads per query row (same TMEM lane, one per
+//              64-column half), reference
 //              max m and sum l in fp32, P_j = exp2(S·scale·log2e − m) written
-//              as fp16 into the K-major swizzled layout the MMA reads (two
-//              buffers).  O accumulates in TMEM; when a block's max exceeds
+//              as fp16 into the K-major swizzled layout the MMA reads.
+//              O accumulates in TMEM; when a block's max exceeds
 //              m by more than 2^8 the softmax rescales O and l by
 //              exp2(m − m_new) first.  The epilogue writes O / l (bf16) and
 //              LSE = (m + log2 l)·ln 2.
@@ -36,13 +37,16 @@ constexpr int HD = 128;
 constexpr int BLK = 128;                 // queries per CTA, keys per block
 constexpr int ATOM = BLK * 128;          // one 64-column half: 128 rows × 128 B
 constexpr int TILE = 2 * ATOM;           // 32 KB fp16 tile [128][128]
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;   // TMA, MMA, 8 softmax warps
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + TILE;      // 2 stages
 constexpr int OFF_V = OFF_K + 2 * TILE;  // 2 stages
-constexpr int OFF_P = OFF_V + 2 * TILE;  // 2 buffers
-constexpr int OFF_BAR = OFF_P + 2 * TILE;
-constexpr int SMEM = OFF_BAR + 256 + 1024;
+constexpr int OFF_P = OFF_V + 2 * TILE;
+constexpr int OFF_BAR = OFF_P + TILE;
+constexpr int OFF_RED = OFF_BAR + 256;   // row-max / row-sum exchange
+constexpr int RED_SLOTS = 3;             // 2 for block parity, 1 for the end
+constexpr int OFF_SEQ = OFF_RED + RED_SLOTS * 2 * 128 * 4;
+constexpr int SMEM = OFF_SEQ + RED_SLOTS * 2 * 128 * 4 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
 // The output accumulates in TMEM against a reference max m; it is rescaled
@@ -50,6 +54,35 @@ constexpr uint32_t COL_O = 256;
 // keeps the fp16 probabilities ≤ 2^8 and the fp32 accumulator far from
 // overflow.
 constexpr float RESCALE_LOG2 = 8.0f;
+
+// Exchange of one float between the two threads that own a query row: write
+// this thread's value with a sequence tag, then wait (bounded, abort-aware)
+// until the partner's entry carries the same tag.  Returns false when it gave
+// up.
+__device__ __forceinline__ bool pair_exchange(float* val, int* seq, int self,
+                                              int other, float mine, int tag,
+                                              float* theirs,
+                                              volatile int* abort_flag,
+                                              unsigned* status) {
+  val[self] = mine;
+  __threadfence_block();
+  reinterpret_cast<volatile int*>(seq)[self] = tag;
+  volatile int* ps = reinterpret_cast<volatile int*>(seq) + other;
+  if (*ps != tag) {
+    const long long t0 = clock64();
+    while (*ps != tag) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitTimeoutCycles) {
+        record_error(status, kDevTimeout, 20);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+  __threadfence_block();
+  *theirs = reinterpret_cast<volatile float*>(val)[other];
+  return true;
+}
 
 struct FwdTcArgs {
   CUtensorMap mq, mk, mv;
@@ -98,13 +131,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 256);
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  for (int i = threadIdx.x; i < RED_SLOTS * 2 * 128; i += THREADS)
+    reinterpret_cast<int*>(sm + OFF_SEQ)[i] = 0;
   if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -158,10 +193,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           return false;
         tc_fence_after();
         const uint32_t sV = smem_u32(sm + OFF_V + (i & 1) * TILE);
-        const uint32_t sPi = sP + (i & 1) * TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem + COL_O, desc_kmajor(sPi, kk), desc_mnmajor(sV, kk),
+          tc_mma_f16(tmem + COL_O, desc_kmajor(sP, kk), desc_mnmajor(sV, kk),
                      IDESC_O, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&pv_done[i & 1]);
         tc_commit(&kv_empty[i & 1]);
@@ -191,52 +225,71 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // --------------------------------------------------------- softmax --
+    // Two warps per row: `half` 0 owns key columns and output columns 0-63,
+    // half 1 owns 64-127; the two threads of a row (same TMEM lane) exchange
+    // the row max through shared memory each block, tagged with the block
+    // index (slots alternate by block parity; slot 2 carries the final sums).
+    const int sw = warp - 2;
+    const int half = sw >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int qi = q0 + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float m_ref = -INFINITY, l_run = 0.0f;
+    float* red = reinterpret_cast<float*>(sm + OFF_RED);  // [slot][half][row]
+    int* seq = reinterpret_cast<int*>(sm + OFF_SEQ);
+    const float c = a.scale_log2;
+    const float thr = RESCALE_LOG2 / c;   // the rescale threshold in raw units
+    float m_ref = -INFINITY, l_part = 0.0f;
     bool ok = true;
     for (int jb = 0; jb < nkb; ++jb) {
       const int st = jb & 1;
-      if (!mbar_wait_warp(&s_full[st], (jb >> 1) & 1, abort_flag, a.status, 16)) {
+      if (!mbar_wait_warp(&s_full[st], (jb >> 1) & 1, abort_flag, a.status,
+                          16)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t v[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + st * 128 + c * 32, v[c]);
+      uint32_t v[2][32];
+      tmem_ld32(lane_base + st * 128 + half * 64, v[0]);
+      tmem_ld32(lane_base + st * 128 + half * 64 + 32, v[1]);
       tmem_ld_wait(v[0]);
       reg_fence32(v[1]);
-      reg_fence32(v[2]);
-      reg_fence32(v[3]);
-      // scaled scores (log2 units), masked; row max with 8 independent chains
-      const int k0 = jb * BLK;
-      const bool masked = (k0 + BLK > a.s) || (a.causal && k0 + BLK - 1 > q0);
+      const int k0 = jb * BLK + half * 64;
+      if ((jb + 1) * BLK > a.s || (a.causal && (jb + 1) * BLK - 1 > q0)) {
+        // diagonal or ragged block: invalid keys become −inf (branch-free)
+        const int kmax = a.causal ? min(qi, a.s - 1) : a.s - 1;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[cc][i] = (k0 + cc * 32 + i <= kmax) ? v[cc][i]
+                                                  : __float_as_uint(-INFINITY);
+      }
       float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+      for (int i = 0; i < 8; ++i)
+        mx8[i] = fmaxf(__uint_as_float(v[0][i]), __uint_as_float(v[0][i + 8]));
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float x = __uint_as_float(v[c][i]) * a.scale_log2;
-          if (masked) {
-            const int key = k0 + c * 32 + i;
-            if (key >= a.s || (a.causal && key > qi)) x = -INFINITY;
-          }
-          v[c][i] = __float_as_uint(x);
-          mx8[i & 7] = fmaxf(mx8[i & 7], x);
-        }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int i = 16; i < 64; ++i)
+        mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(v[i >> 5][i & 31]));
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      float mx_other;
+      const bool got = pair_exchange(red, seq, (st * 2 + half) * 128 + r,
+                                     (st * 2 + (half ^ 1)) * 128 + r, mx,
+                                     jb + 1, &mx_other, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, mx_other);
       if (jb == 0) {
         m_ref = mx;
-      } else if (__any_sync(0xffffffffu, mx > m_ref + RESCALE_LOG2)) {
-        // rescale the TMEM accumulator once O += P_{j-1}·V_{j-1} has landed;
-        // the whole warp takes part (TMEM access is warp-collective), rows
-        // that keep their reference scale by 1
+      } else if (__any_sync(0xffffffffu, mx > m_ref + thr)) {
+        // rescale this warp's half of the TMEM accumulator once
+        // O += P_{j-1}·V_{j-1} has landed; the whole warp takes part (TMEM
+        // access is warp-collective), rows that keep their reference scale
+        // by 1.  Both warps of a pair see the same rows and decide alike.
         const int pj = jb - 1;
         if (!mbar_wait_warp(&pv_done[pj & 1], (pj >> 1) & 1, abort_flag,
                             a.status, 17)) {
@@ -244,71 +297,79 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        const float m_new = mx > m_ref + RESCALE_LOG2 ? mx : m_ref;
-        const float alpha = ex2_approx(m_ref - m_new);
+        const float m_new = mx > m_ref + thr ? mx : m_ref;
+        const float alpha = ex2_approx((m_ref - m_new) * c);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t o[32];
-          tmem_ld32(lane_base + COL_O + c * 32, o);
+          const uint32_t ta = lane_base + COL_O + half * 64 + cc * 32;
+          tmem_ld32(ta, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(lane_base + COL_O + c * 32, o);
+          tmem_st32(ta, o);
         }
-        l_run *= alpha;
+        l_part *= alpha;
         m_ref = m_new;
       }
-      // P buffer st is free once O += P_{j-2}·V_{j-2} has completed
-      if (jb >= 2 && !mbar_wait_warp(&pv_done[st], ((jb - 2) >> 1) & 1,
+      // the P tile is free once O += P_{j-1}·V_{j-1} has completed
+      if (jb >= 1 && !mbar_wait_warp(&pv_done[(jb - 1) & 1], ((jb - 1) >> 1) & 1,
                                      abort_flag, a.status, 18)) {
         ok = false;
         break;
       }
-      uint8_t* sP = sm + OFF_P + st * TILE;
+      // P = exp2(c·(s − m)), fp16, into key half `half` of the swizzled tile
+      const float neg = -m_ref * c;
+      uint8_t* prow = sm + OFF_P + half * ATOM + r * 128;
       float sum8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2_approx(__uint_as_float(v[c][i]) - m_ref);
-          const float p1 = ex2_approx(__uint_as_float(v[c][i + 1]) - m_ref);
+          const float p0 = ex2_approx(fmaf(__uint_as_float(v[cc][i]), c, neg));
+          const float p1 =
+              ex2_approx(fmaf(__uint_as_float(v[cc][i + 1]), c, neg));
           sum8[i & 7] += p0;
           sum8[(i + 1) & 7] += p1;
           pk[i >> 1] = pack_f16x2(p0, p1);
         }
-        // keys c·32 … c·32+31 = four 8-key chunks of half (c >> 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int chunk = (c & 1) * 4 + q;
-          uint8_t* dst = sP + (c >> 1) * ATOM + r * 128 +
-                         ((chunk ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) =
+          const int chunk = cc * 4 + q;
+          *reinterpret_cast<uint4*>(prow + ((chunk ^ (r & 7)) << 4)) =
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
-      l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-               ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      l_part += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[st]);
     }
-    // epilogue: wait for the last O += P·V, then O / l and the LSE
+    // epilogue: the row sum is the two halves' partial sums; wait for the
+    // last O += P·V, then O / l for this warp's 64 columns and the LSE
+    float l_other = 0.0f;
+    if (__all_sync(0xffffffffu, ok))
+      ok = pair_exchange(red, seq, (4 + half) * 128 + r,
+                         (4 + (half ^ 1)) * 128 + r, l_part, nkb + 1, &l_other,
+                         abort_flag, a.status);
     const int last = nkb - 1;
     if (__all_sync(0xffffffffu, ok) &&
         mbar_wait_warp(&pv_done[last & 1], (last >> 1) & 1, abort_flag,
                        a.status, 19)) {
       tc_fence_after();
+      const float l_run = l_part + l_other;
       const float inv = 1.0f / l_run;
-      __nv_bfloat16* dst =
-          a.O + ((int64_t)b * a.s + qi) * (int64_t)(a.nq * HD) + j * HD;
+      __nv_bfloat16* dst = a.O + ((int64_t)b * a.s + qi) * (int64_t)(a.nq * HD) +
+                           j * HD + half * 64;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t o[32];
-        tmem_ld32(lane_base + COL_O + c * 32, o);
+        tmem_ld32(lane_base + COL_O + half * 64 + cc * 32, o);
         tmem_ld_wait(o);
         if (qi < a.s) {
 #pragma unroll
@@ -322,13 +383,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                               __uint_as_float(o[8 * q + 5]) * inv);
             u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv,
                               __uint_as_float(o[8 * q + 7]) * inv);
-            reinterpret_cast<uint4*>(dst)[c * 4 + q] = u;
+            reinterpret_cast<uint4*>(dst)[cc * 4 + q] = u;
           }
         }
       }
-      if (qi < a.s)
+      if (half == 0 && qi < a.s)
         a.LSE[((int64_t)b * a.nq + j) * a.s + qi] =
-            (m_ref + log2f(l_run)) * 0.69314718055994531f;
+            (m_ref * c + log2f(l_run)) * 0.69314718055994531f;
     }
   }
 
