@@ -151,7 +151,8 @@ typedef struct {
  * |Q|, |K|, |V|, |dO| must stay below 65504, else tp_device_status reports
  * TP_ERR_RANGE. */
 size_t tp_attn_workspace_bytes(const tp_attn_desc* d);
-/* scratch: dO, dQ, dK, dV, D = rowsum(dO∘O) [b, n_q, s] fp32, partials and
+/* scratch: dO (fp16), dQ, dK, dV (bf16), D = rowsum(dO∘O) and LSE·log2e
+ * (fp32, [b, n_q, s rounded up to 128]), partials and
  * column-sum partials. */
 size_t tp_attn_bwd_scratch_bytes(const tp_attn_desc* d);
 

@@ -501,7 +501,7 @@ AttnFwdLayout attn_fwd_layout(const tp_attn_desc* d, void* ws) {
 
 struct AttnBwdLayout {
   void *dO = nullptr, *dQ = nullptr, *dK = nullptr, *dV = nullptr;
-  float* D = nullptr;
+  float *D = nullptr, *L2 = nullptr;
   void* partials = nullptr;
   float* colsum = nullptr;
   size_t bytes = 0;
@@ -516,7 +516,9 @@ AttnBwdLayout attn_bwd_layout(const tp_attn_desc* d, void* scratch) {
   L.dQ = c.take(T * qd * 2);
   L.dK = c.take(T * kd * 2);
   L.dV = c.take(T * kd * 2);
-  L.D = static_cast<float*>(c.take((size_t)d->b * d->n_q * d->s * 4));
+  const size_t stats = (size_t)d->b * d->n_q * attn_stats_pad(d->s) * 4;
+  L.D = static_cast<float*>(c.take(stats));
+  L.L2 = static_cast<float*>(c.take(stats));
   if (d->mode == TP_REDUCE_MATERIALISED)
     L.partials = c.take((size_t)d->n * T * (size_t)d->h * 2);
   L.colsum = static_cast<float*>(c.take(colsum_scratch_bytes(T, d->h)));
@@ -655,8 +657,8 @@ extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
                           qd),
                      stream);
     if (err) return cuda_status(err);
-    err = flash_bwd(attn_shape(d), F.q, F.k, F.v, F.o, L.dO, F.lse, L.D,
-                    nullptr, L.dQ, L.dK, L.dV, stream);
+    err = flash_bwd(attn_shape(d), F.q, F.k, F.v, F.o, L.dO, F.lse, L.D, L.L2,
+                    L.dQ, L.dK, L.dV, device_status_ptr(), stream);
     if (err) return cuda_status(err);
     err = run_gemm(proj(qd, h, op(L.dQ, qd, 1, qd), op(X, h, 1, h), T, dWq, h),
                    stream);

@@ -18,10 +18,13 @@ struct AttnShape {
 // Forward on tcgen05 (attn_fwd_tc.cu); Q, K, V fp16, O bf16.
 int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
               void* O, float* LSE, unsigned* status, void* stream);
-// dQ, dK, dV (bf16, GQA groups summed); D [b, nq, s] fp32 scratch;
-// dq_acc [T, nq·d] fp32 scratch.
+// Backward on tcgen05 (attn_bwd_tc.cu): dQ, dK, dV (bf16, GQA groups summed).
+// Dp and L2p are fp32 scratch of b·nq·attn_stats_pad(s) elements each
+// (D = rowsum(dO∘O) and LSE·log2e, zero-padded); dO is fp16.
+int64_t attn_stats_pad(int64_t s);
 int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
-              const void* O, const void* dO, const float* LSE, float* D,
-              float* dq_acc, void* dQ, void* dK, void* dV, void* stream);
+              const void* O, const void* dO, const float* LSE, float* Dp,
+              float* L2p, void* dQ, void* dK, void* dV, unsigned* status,
+              void* stream);
 
 }  // namespace tp

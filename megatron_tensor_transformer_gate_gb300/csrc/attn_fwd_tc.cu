@@ -20,7 +20,12 @@
 //              m by more than 2^8 the softmax rescales O and l by
 //              exp2(m − m_new) first.  The epilogue writes O / l (bf16) and
 //              LSE = (m + log2 l)·ln 2.
-// Operands are fp16 (see attention.cu for why), accumulation fp32.
+// Operands are fp16 and accumulation fp32: the softmax amplifies score
+// errors, and bf16 operands (8-bit mantissa) put the row-wise error of causal
+// outputs above 3e-2 of the row rms, while fp16 (10-bit mantissa, same bytes)
+// stays near the bf16 output-rounding floor.  Q, K, V (and dO) are written in
+// fp16 by the projection GEMMs; O is written in bf16 for the bf16 out-
+// projection GEMM.
 #include <cuda_fp16.h>
 
 #include <cstring>
