@@ -99,7 +99,8 @@ typedef struct {
 
 /* Bytes of `ws` for tp_mlp_fwd/tp_mlp_bwd: saved activations (H and A for
  * GeLU; G, U and A for SwiGLU; each [T, h_ffn] in dtype) followed by the
- * forward scratch (n partial [T, h] tensors in materialised mode). */
+ * forward scratch (n partial [T, h] tensors in materialised mode).  Every
+ * region starts at the next 256-byte boundary, in the order listed. */
 size_t tp_mlp_workspace_bytes(const tp_mlp_desc* d);
 /* Bytes of `scratch` for tp_mlp_bwd: dZ [T, h] (when p > 0), the
  * activation-input gradient ([T, h_ffn] or [T, 2·h_ffn]), partial input
@@ -144,8 +145,10 @@ typedef struct {
   int32_t mode;       /* tp_reduce_mode */
 } tp_attn_desc;
 
-/* ws: Q, K, V (fp16), O (bf16) and LSE [b, n_q, s] fp32 saved for backward,
- * then the forward scratch (n partial [T, h] tensors in materialised mode).
+/* ws: Q [T, n_q·d], K, V [T, n_kv·d] (fp16), O [T, n_q·d] (bf16) and LSE
+ * [b, n_q, s] fp32 saved for backward, then the forward scratch (n partial
+ * [T, h] tensors in materialised mode); each region starts at the next
+ * 256-byte boundary, in this order.
  * The attention core multiplies fp16 operands with fp32 accumulation (Q, K,
  * V, dO in fp16; the probabilities and their gradients rounded to fp16):
  * |Q|, |K|, |V|, |dO| must stay below 65504, else tp_device_status reports

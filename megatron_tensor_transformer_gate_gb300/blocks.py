@@ -20,6 +20,21 @@ def _buf(nbytes, device):
     return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
 
 
+def _views(ws, specs):
+    """Tensors viewing consecutive 256-byte-aligned regions of a workspace
+    (the layout include/tp.h documents); specs = [(name, shape, dtype)]."""
+    out, off = {}, 0
+    for name, shape, dt in specs:
+        off = (off + 255) // 256 * 256
+        n = 1
+        for d in shape:
+            n *= d
+        nbytes = n * torch.empty((), dtype=dt).element_size()
+        out[name] = ws[off:off + nbytes].view(dt).view(*shape)
+        off += nbytes
+    return out
+
+
 class TPMLP:
     def __init__(self, T, h, h_ffn, n, *, dtype=B.BF16, act=B.GELU,
                  mode=B.FUSED, dropout_p=0.0, seed=0, device="cuda"):
@@ -50,6 +65,12 @@ class TPMLP:
                   dres=dres, stream=stream)
         return g
 
+    def saved(self):
+        """Views of the activations the forward call saved for backward."""
+        tf = (self.T, self.f)
+        names = ("H", "A") if self.act == B.GELU else ("G", "U", "A")
+        return _views(self.ws, [(n, tf, self.dtype) for n in names])
+
     def alloc_grads(self, W1, W2, want_db1=False, want_db2=False):
         kw = dict(dtype=self.dtype, device=self.device)
         g = {"dX": torch.empty((self.T, self.h), **kw),
@@ -67,6 +88,7 @@ class TPAttention:
         self.desc = B.attn_desc(b, s, h, n_q, n_kv, d, n, B.BF16, causal,
                                 mode)
         self.T, self.h = b * s, h
+        self.shape = (b, s, n_q, n_kv, d)
         self.device = device
         self.ws = _buf(B.attn_workspace_bytes(self.desc), device)
         self.scratch = _buf(B.attn_bwd_scratch_bytes(self.desc), device)
@@ -88,6 +110,16 @@ class TPAttention:
                    g["dWq"], g["dWk"], g["dWv"], g["dWo"], self.scratch,
                    dbo=g.get("dbo"), dres=dres, stream=stream)
         return g
+
+    def saved(self):
+        """Views of Q, K, V (fp16), O (bf16) and LSE saved by the forward."""
+        b, s, nq, nkv, d = self.shape
+        T = b * s
+        return _views(self.ws, [("Q", (T, nq * d), torch.float16),
+                                ("K", (T, nkv * d), torch.float16),
+                                ("V", (T, nkv * d), torch.float16),
+                                ("O", (T, nq * d), torch.bfloat16),
+                                ("LSE", (b, nq, s), torch.float32)])
 
     def alloc_grads(self, Wq, Wk, Wv, Wo, want_dbo=False):
         g = {"dX": torch.empty((self.T, self.h), dtype=torch.bfloat16,

@@ -9,6 +9,15 @@ scale: in causal attention the first tokens attend to few keys and are 15–18×
 the tensor rms, so even the exact result rounded to bf16 has a tensor-wide
 max/rms of ≈4e-2.
 fp32 workloads: max|g − o| / max|o| ≤ 1e-4 per tensor.
+
+A composed layer stores bf16 activations between its blocks (its GEMMs take
+bf16 operands), and the downstream softmax and SwiGLU amplify those
+roundings: simulating exactly those roundings on the CPU reproduces the
+layer's end-to-end error (Frobenius 7.4e-3, row max/rms 4.1e-2 on the layer
+workload's widths).  The layer is therefore checked end to end with the
+Frobenius bound (`check_fro`) and block by block, each block against the
+oracle fed the same bf16 activations that the block consumed, with both
+bounds.
 """
 
 import numpy as np
@@ -48,4 +57,10 @@ def check(g, o, name, dtype="bf16"):
     else:
         assert fro <= BF16_FRO and maxrms <= BF16_MAXRMS, \
             f"{name}: fro {fro:.3e}, row max/rms {maxrms:.3e}"
+    return fro, maxrms, maxrel
+
+
+def check_fro(g, o, name):
+    fro, maxrms, maxrel = errors(g, o)
+    assert fro <= BF16_FRO, f"{name}: fro {fro:.3e}"
     return fro, maxrms, maxrel
