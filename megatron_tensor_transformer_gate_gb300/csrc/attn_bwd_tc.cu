@@ -17,8 +17,10 @@
 //               dV += Pᵀ·dO,  dK += dSᵀ·Q        (M=128, N=128, K=64) → TMEM
 // Both: warp 0 TMA, warp 1 TMEM allocation + single-thread MMA issue, warps
 // 2–9 elementwise (two threads per TMEM lane, 32 of the 64 columns each).
-// Score tiles are double-buffered in TMEM so the tensor cores compute block
-// j+1 while the elementwise warps work on block j.  No atomics: reruns are
+// Score tiles are double-buffered in TMEM and issued two blocks ahead of the
+// gradient MMAs (gated only by the elementwise warps having copied the older
+// tile to registers), so the tensor cores compute blocks j+1 and j+2 while
+// the elementwise warps work on block j.  No atomics: reruns are
 // bit-identical, and the GQA sums of dK, dV stay inside one CTA.
 // Operands fp16, accumulation fp32; dQ, dK, dV are written in bf16.
 #include <cuda_fp16.h>
@@ -132,9 +134,10 @@ __global__ void __launch_bounds__(256)
 namespace dq {
 constexpr int OFF_Q = 0;
 constexpr int OFF_DO = 2 * A128;
-constexpr int OFF_KV = 4 * A128;              // 3 stages of K (16 KB) + V
+constexpr int OFF_KV = 4 * A128;              // 4 stages of K (16 KB) + V
 constexpr int STAGE = 4 * A64;
-constexpr int OFF_DS = OFF_KV + 3 * STAGE;    // 2 buffers of 16 KB
+constexpr int NST = 4;
+constexpr int OFF_DS = OFF_KV + NST * STAGE;  // 2 buffers of 16 KB
 constexpr int OFF_BAR = OFF_DS + 2 * A128;
 constexpr int SMEM = OFF_BAR + 256 + 1024;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
@@ -159,15 +162,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* q_full = bar;          // Q and dO
-  uint64_t* kv_full = bar + 1;     // [3]
-  uint64_t* kv_empty = bar + 4;    // [3]
-  uint64_t* sdp_full = bar + 7;    // [2]
-  uint64_t* sdp_free = bar + 9;    // [2]
-  uint64_t* ds_full = bar + 11;    // [2]
-  uint64_t* ds_free = bar + 13;    // [2]
-  uint64_t* dq_done = bar + 15;
-  uint64_t* drain = bar + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 17);
+  uint64_t* kv_full = bar + 1;     // [NST]
+  uint64_t* kv_empty = bar + 5;    // [NST]
+  uint64_t* sdp_full = bar + 9;    // [2]
+  uint64_t* sdp_free = bar + 11;   // [2] S, dP copied to registers
+  uint64_t* ds_full = bar + 13;    // [2]
+  uint64_t* ds_free = bar + 15;    // [2]
+  uint64_t* dq_done = bar + 17;
+  uint64_t* drain = bar + 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     q0, b);
       }
       for (int jb = 0; jb < nkb; ++jb) {
-        const int st = jb % 3;
-        const uint32_t ph = (jb / 3) & 1;
+        const int st = jb % NST;
+        const uint32_t ph = (jb / NST) & 1;
         if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, a.status, 31)) break;
         mbar_arrive_expect_tx(&kv_full[st], STAGE);
         armed |= 1u << st;
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (*abort_flag) {
         volatile int no_abort = 0;
         mbar_wait(q_full, 0, &no_abort, nullptr, 0);
-        for (int st = 0; st < 3; ++st)
+        for (int st = 0; st < NST; ++st)
           if (armed & (1u << st))
             mbar_wait(&kv_full[st], (armed_par >> st) & 1u, &no_abort, nullptr,
                       0);
@@ -244,29 +247,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t IDESC_Q = idesc_f16_f32(128, 128, 0, 1);
       const uint32_t sQ = smem_u32(sm + OFF_Q), sdO = smem_u32(sm + OFF_DO);
       bool ok = mbar_wait(q_full, 0, abort_flag, a.status, 32);
-      auto dq_mma = [&](int i) -> bool {
-        const int bb = i & 1;
-        if (!mbar_wait(&ds_full[bb], (i >> 1) & 1, abort_flag, a.status, 33))
+      // S and dP run two blocks ahead of dQ += dS·K (see the file header)
+      auto sdp_mma = [&](int jb) -> bool {
+        const int st = jb % NST, bb = jb & 1;
+        if (!mbar_wait(&kv_full[st], (jb / NST) & 1, abort_flag, a.status, 34))
           return false;
-        tc_fence_after();
-        const uint32_t sK = smem_u32(sm + OFF_KV + (i % 3) * STAGE);
-        const uint32_t sdS = smem_u32(sm + OFF_DS + bb * A128);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_f16(tmem + COL_DQ, dk64(sdS, kk), dmn(sK, kk, A64), IDESC_Q,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&ds_free[bb]);
-        tc_commit(&kv_empty[i % 3]);
-        return true;
-      };
-      for (int jb = 0; ok && jb < nkb; ++jb) {
-        const int st = jb % 3, bb = jb & 1;
-        if (!mbar_wait(&kv_full[st], (jb / 3) & 1, abort_flag, a.status, 34) ||
-            (jb >= 2 && !mbar_wait(&sdp_free[bb], ((jb - 2) >> 1) & 1,
-                                   abort_flag, a.status, 35))) {
-          ok = false;
-          break;
-        }
         tc_fence_after();
         const uint32_t sK = smem_u32(sm + OFF_KV + st * STAGE);
         const uint32_t sV = sK + 2 * A64;
@@ -279,9 +264,35 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_mma_f16(tmem + COL_DP + bb * 64, dk128(sdO, kk, A128),
                      dk128(sV, kk, A64), IDESC_S, kk > 0 ? 1u : 0u);
         tc_commit(&sdp_full[bb]);
-        if (jb >= 1) ok = dq_mma(jb - 1);
+        return true;
+      };
+      auto dq_mma = [&](int i) -> bool {
+        const int bb = i & 1;
+        if (!mbar_wait(&ds_full[bb], (i >> 1) & 1, abort_flag, a.status, 33))
+          return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(sm + OFF_KV + (i % NST) * STAGE);
+        const uint32_t sdS = smem_u32(sm + OFF_DS + bb * A128);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_f16(tmem + COL_DQ, dk64(sdS, kk), dmn(sK, kk, A64), IDESC_Q,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&ds_free[bb]);
+        tc_commit(&kv_empty[i % NST]);
+        return true;
+      };
+      if (ok) ok = sdp_mma(0);
+      if (ok && nkb > 1) ok = sdp_mma(1);
+      for (int jb = 0; ok && jb < nkb; ++jb) {
+        if (jb + 2 < nkb) {
+          ok = mbar_wait(&sdp_free[jb & 1], (jb >> 1) & 1, abort_flag,
+                         a.status, 35) &&
+               sdp_mma(jb + 2);
+          if (!ok) break;
+        }
+        ok = dq_mma(jb);
       }
-      if (ok && dq_mma(nkb - 1)) tc_commit(dq_done);
+      if (ok) tc_commit(dq_done);
       if (*abort_flag) {
         volatile int no_abort = 0;
         tc_commit(drain);
@@ -365,11 +376,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 namespace dkv {
 constexpr int OFF_K = 0;
 constexpr int OFF_V = 2 * A128;
-constexpr int OFF_QS = 4 * A128;                 // 2 stages
-constexpr int STAGE = 4 * A64 + 1024;            // Q 16 KB, dO 16 KB, stats
-constexpr int OFF_P = OFF_QS + 2 * STAGE;        // 2 buffers of 16 KB
+constexpr int OFF_QS = 4 * A128;                 // NST stages
+constexpr int STAGE = 4 * A64;                   // Q 16 KB, dO 16 KB
+constexpr int NST = 3;
+constexpr int OFF_P = OFF_QS + NST * STAGE;      // 2 buffers of 16 KB
 constexpr int OFF_DS = OFF_P + 2 * A128;         // 2 buffers of 16 KB
-constexpr int OFF_BAR = OFF_DS + 2 * A128;
+constexpr int OFF_ST = OFF_DS + 2 * A128;        // NST × (64 L2, 64 D) fp32
+constexpr int OFF_BAR = OFF_ST + NST * 512;
 constexpr int SMEM = OFF_BAR + 256 + 1024;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
 }  // namespace dkv
@@ -382,15 +395,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* kv_full = bar;         // K and V
-  uint64_t* qs_full = bar + 1;     // [2] Q, dO, stats
-  uint64_t* qs_empty = bar + 3;    // [2]
-  uint64_t* sdp_full = bar + 5;    // [2]
-  uint64_t* sdp_free = bar + 7;    // [2]
-  uint64_t* pds_full = bar + 9;    // [2]
-  uint64_t* pds_free = bar + 11;   // [2]
-  uint64_t* done = bar + 13;
-  uint64_t* drain = bar + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 15);
+  uint64_t* qs_full = bar + 1;     // [NST] Q, dO, stats
+  uint64_t* qs_empty = bar + 4;    // [NST]
+  uint64_t* sdp_full = bar + 7;    // [2]
+  uint64_t* sdp_free = bar + 9;    // [2] Sᵀ, dPᵀ copied to registers
+  uint64_t* pds_full = bar + 11;   // [2]
+  uint64_t* pds_free = bar + 13;   // [2]
+  uint64_t* done = bar + 15;
+  uint64_t* drain = bar + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -404,9 +417,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(&qs_full[i], 1);
       mbar_init(&qs_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1);
       mbar_init(&sdp_free[i], 256);
       mbar_init(&pds_full[i], 256);
@@ -438,8 +453,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     k0, b);
       }
       for (int it = 0; it < iters; ++it) {
-        const int st = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
+        const int st = it % NST;
+        const uint32_t ph = (it / NST) & 1;
         if (!mbar_wait(&qs_empty[st], ph ^ 1, abort_flag, a.status, 41)) break;
         const int jq = kvh * group + it / per_head;
         const int qb = qb_first + it % per_head;
@@ -454,13 +469,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                       jq * HD + hh * 64, qb * 64, b);
         }
         const int64_t soff = ((int64_t)b * a.nq + jq) * a.s_pad + qb * 64;
-        bulk_load(stg + 4 * A64, a.L2p + soff, 256, &qs_full[st]);
-        bulk_load(stg + 4 * A64 + 256, a.Dp + soff, 256, &qs_full[st]);
+        uint8_t* sst = sm + OFF_ST + st * 512;
+        bulk_load(sst, a.L2p + soff, 256, &qs_full[st]);
+        bulk_load(sst + 256, a.Dp + soff, 256, &qs_full[st]);
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
         mbar_wait(kv_full, 0, &no_abort, nullptr, 0);
-        for (int st = 0; st < 2; ++st)
+        for (int st = 0; st < NST; ++st)
           if (armed & (1u << st))
             mbar_wait(&qs_full[st], (armed_par >> st) & 1u, &no_abort, nullptr,
                       0);
@@ -472,12 +488,30 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t IDESC_G = idesc_f16_f32(128, 128, 0, 1);
       const uint32_t sK = smem_u32(sm + OFF_K), sV = smem_u32(sm + OFF_V);
       bool ok = mbar_wait(kv_full, 0, abort_flag, a.status, 42);
+      // Sᵀ and dPᵀ run two iterations ahead of the gradient MMAs
+      auto sdp_mma = [&](int it) -> bool {
+        const int st = it % NST, bb = it & 1;
+        if (!mbar_wait(&qs_full[st], (it / NST) & 1, abort_flag, a.status, 44))
+          return false;
+        tc_fence_after();
+        const uint32_t stg = smem_u32(sm + OFF_QS + st * STAGE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem + COL_S + bb * 64, dk128(sK, kk, A128),
+                     dk128(stg, kk, A64), IDESC_S, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem + COL_DP + bb * 64, dk128(sV, kk, A128),
+                     dk128(stg + 2 * A64, kk, A64), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(&sdp_full[bb]);
+        return true;
+      };
       auto grads = [&](int i) -> bool {
-        const int bb = i & 1;
+        const int bb = i & 1, st = i % NST;
         if (!mbar_wait(&pds_full[bb], (i >> 1) & 1, abort_flag, a.status, 43))
           return false;
         tc_fence_after();
-        const uint32_t stg = smem_u32(sm + OFF_QS + bb * STAGE);
+        const uint32_t stg = smem_u32(sm + OFF_QS + st * STAGE);
         const uint32_t sP = smem_u32(sm + OFF_P + bb * A128);
         const uint32_t sdS = smem_u32(sm + OFF_DS + bb * A128);
 #pragma unroll
@@ -489,31 +523,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_mma_f16(tmem + COL_DK, dk64(sdS, kk), dmn(stg, kk, A64), IDESC_G,
                      (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&pds_free[bb]);
-        tc_commit(&qs_empty[bb]);
+        tc_commit(&qs_empty[st]);
         return true;
       };
+      if (ok) ok = sdp_mma(0);
+      if (ok && iters > 1) ok = sdp_mma(1);
       for (int it = 0; ok && it < iters; ++it) {
-        const int st = it & 1;
-        if (!mbar_wait(&qs_full[st], (it >> 1) & 1, abort_flag, a.status, 44) ||
-            (it >= 2 && !mbar_wait(&sdp_free[st], ((it - 2) >> 1) & 1,
-                                   abort_flag, a.status, 45))) {
-          ok = false;
-          break;
+        if (it + 2 < iters) {
+          ok = mbar_wait(&sdp_free[it & 1], (it >> 1) & 1, abort_flag,
+                         a.status, 45) &&
+               sdp_mma(it + 2);
+          if (!ok) break;
         }
-        tc_fence_after();
-        const uint32_t stg = smem_u32(sm + OFF_QS + st * STAGE);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem + COL_S + st * 64, dk128(sK, kk, A128),
-                     dk128(stg, kk, A64), IDESC_S, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem + COL_DP + st * 64, dk128(sV, kk, A128),
-                     dk128(stg + 2 * A64, kk, A64), IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(&sdp_full[st]);
-        if (it >= 1) ok = grads(it - 1);
+        ok = grads(it);
       }
-      if (ok && iters > 0 && grads(iters - 1)) tc_commit(done);
+      if (ok) tc_commit(done);
       if (*abort_flag) {
         volatile int no_abort = 0;
         tc_commit(drain);
@@ -547,7 +571,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int qb = qb_first + it % per_head;
       const int qc0 = qb * 64 + half * 32;   // first query column of this half
       const float* stats =
-          reinterpret_cast<const float*>(sm + OFF_QS + st * STAGE + 4 * A64);
+          reinterpret_cast<const float*>(sm + OFF_ST + (it % NST) * 512);
       const bool masked = (qb * 64 + 64 > a.s) || (k0 + 128 > a.s) ||
                           (a.causal && qb * 64 < k0 + 127);
       uint32_t pp[16], pd[16];

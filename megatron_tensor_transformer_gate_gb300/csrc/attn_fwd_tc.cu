@@ -5,13 +5,14 @@
 // online softmax, O(S) statistics written for the backward pass).
 //
 // One CTA = 128 query rows of one (batch, q head); 192 threads:
-//   warp 0     TMA: the Q tile once, then K_j and V_j (128 keys each) into a
-//              2-stage ring (fp16, 128-byte swizzle, two 64-column halves).
+//   warp 0     TMA: the Q tile once, then K_j and V_j (128 keys each) into
+//              two independent 2-stage rings (fp16, 128-byte swizzle, two
+//              64-column halves); lane 0 feeds K, lane 1 feeds V.
 //   warp 1     allocates 512 TMEM columns and issues, per key block j,
 //                S_j = Q·K_jᵀ   (M=128, N=128, K=128) into TMEM S[j mod 2]
 //                O += P_j·V_j   (M=128, N=128, K=128) into TMEM O
-//              in the order S_0, S_1, PV_0, S_2, PV_1, … so the tensor cores
-//              compute S_{j+1} while the softmax works on S_j.
+//              with the scores two blocks ahead (S_0, S_1, S_2, PV_0, S_3,
+//              PV_1, …) so the tensor cores never wait for a softmax block.
 //   warps 2–9  softmax, two threads per query row (same TMEM lane, one per
 //              64-column half), reference
 //              max m and sum l in fp32, P_j = exp2(S·scale·log2e − m) written
@@ -114,13 +115,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;    // [2]
-  uint64_t* kv_empty = bar + 3;   // [2]
-  uint64_t* s_full = bar + 5;     // [2]
-  uint64_t* p_full = bar + 7;     // [2]
-  uint64_t* pv_done = bar + 9;    // [2]
-  uint64_t* drain = bar + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 12);
+  uint64_t* k_full = bar + 1;     // [2]
+  uint64_t* k_empty = bar + 3;    // [2]
+  uint64_t* v_full = bar + 5;     // [2]
+  uint64_t* v_empty = bar + 7;    // [2]
+  uint64_t* s_full = bar + 9;     // [2]
+  uint64_t* s_free = bar + 11;    // [2] scores copied to registers
+  uint64_t* p_full = bar + 13;    // [2]
+  uint64_t* pv_done = bar + 15;   // [2]
+  uint64_t* drain = bar + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,9 +137,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 256);
       mbar_init(&p_full[i], 256);
       mbar_init(&pv_done[i], 1);
     }
@@ -152,49 +159,72 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane < 2) {
       // ------------------------------------------------------------- TMA --
-      tma_prefetch_desc(&a.mq);
-      tma_prefetch_desc(&a.mk);
-      tma_prefetch_desc(&a.mv);
+      // lane 0: Q, then the K ring; lane 1: the V ring.  K_j is released as
+      // soon as S_j is done, V_j only after O += P_j·V_j, so the two rings
+      // advance independently.
+      const bool is_k = lane == 0;
+      const CUtensorMap* map = is_k ? &a.mk : &a.mv;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* ring = sm + (is_k ? OFF_K : OFF_V);
+      tma_prefetch_desc(map);
       uint32_t armed = 0, armed_par = 0;
-      mbar_arrive_expect_tx(q_full, TILE);
-      for (int hh = 0; hh < 2; ++hh)
-        tma_load_3d(sm + OFF_Q + hh * ATOM, &a.mq, q_full, j * HD + hh * 64,
-                    q0, b);
+      if (is_k) {
+        tma_prefetch_desc(&a.mq);
+        mbar_arrive_expect_tx(q_full, TILE);
+        for (int hh = 0; hh < 2; ++hh)
+          tma_load_3d(sm + OFF_Q + hh * ATOM, &a.mq, q_full, j * HD + hh * 64,
+                      q0, b);
+      }
       for (int jb = 0; jb < nkb; ++jb) {
         const int st = jb & 1;
         const uint32_t ph = (jb >> 1) & 1;
-        if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, a.status, 11)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * TILE);
+        if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, a.status, 11)) break;
+        mbar_arrive_expect_tx(&full[st], TILE);
         armed |= 1u << st;
         armed_par = (armed_par & ~(1u << st)) | (ph << st);
-        for (int hh = 0; hh < 2; ++hh) {
-          tma_load_3d(sm + OFF_K + st * TILE + hh * ATOM, &a.mk, &kv_full[st],
+        for (int hh = 0; hh < 2; ++hh)
+          tma_load_3d(ring + st * TILE + hh * ATOM, map, &full[st],
                       kvh * HD + hh * 64, jb * BLK, b);
-          tma_load_3d(sm + OFF_V + st * TILE + hh * ATOM, &a.mv, &kv_full[st],
-                      kvh * HD + hh * 64, jb * BLK, b);
-        }
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
-        mbar_wait(q_full, 0, &no_abort, nullptr, 0);
+        if (is_k) mbar_wait(q_full, 0, &no_abort, nullptr, 0);
         for (int st = 0; st < 2; ++st)
           if (armed & (1u << st))
-            mbar_wait(&kv_full[st], (armed_par >> st) & 1u, &no_abort, nullptr,
-                      0);
+            mbar_wait(&full[st], (armed_par >> st) & 1u, &no_abort, nullptr, 0);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------- MMA --
+      // Score tiles run two blocks ahead of O += P·V: S_{j+2} is issued as
+      // soon as the softmax has copied S_j to registers, so the tensor
+      // cores never wait for the softmax to finish a block.
       constexpr uint32_t IDESC_S = idesc_f16_f32(128, 128, 0, 0);
       constexpr uint32_t IDESC_O = idesc_f16_f32(128, 128, 0, 1);
       const uint32_t sQ = smem_u32(sm + OFF_Q), sP = smem_u32(sm + OFF_P);
       bool ok = mbar_wait(q_full, 0, abort_flag, a.status, 12);
+      auto s_mma = [&](int jb) -> bool {
+        const int st = jb & 1;
+        if (!mbar_wait(&k_full[st], (jb >> 1) & 1, abort_flag, a.status, 15))
+          return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(sm + OFF_K + st * TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem + st * 128, desc_kmajor(sQ, kk), desc_kmajor(sK, kk),
+                     IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(&s_full[st]);
+        tc_commit(&k_empty[st]);
+        return true;
+      };
       // O += P_i·V_i; the softmax rescaled O (if needed) before p_full[i]
       auto pv = [&](int i) -> bool {
-        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, a.status, 13))
+        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, a.status, 13) ||
+            !mbar_wait(&v_full[i & 1], (i >> 1) & 1, abort_flag, a.status, 14))
           return false;
         tc_fence_after();
         const uint32_t sV = smem_u32(sm + OFF_V + (i & 1) * TILE);
@@ -203,25 +233,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_mma_f16(tmem + COL_O, desc_kmajor(sP, kk), desc_mnmajor(sV, kk),
                      IDESC_O, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&pv_done[i & 1]);
-        tc_commit(&kv_empty[i & 1]);
+        tc_commit(&v_empty[i & 1]);
         return true;
       };
+      if (ok) ok = s_mma(0);
+      if (ok && nkb > 1) ok = s_mma(1);
       for (int jb = 0; ok && jb < nkb; ++jb) {
-        const int st = jb & 1;
-        if (!mbar_wait(&kv_full[st], (jb >> 1) & 1, abort_flag, a.status, 15)) {
-          ok = false;
-          break;
+        if (jb + 2 < nkb) {
+          ok = mbar_wait(&s_free[jb & 1], (jb >> 1) & 1, abort_flag, a.status,
+                         16) &&
+               s_mma(jb + 2);
+          if (!ok) break;
         }
-        tc_fence_after();
-        const uint32_t sK = smem_u32(sm + OFF_K + st * TILE);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem + st * 128, desc_kmajor(sQ, kk), desc_kmajor(sK, kk),
-                     IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(&s_full[st]);
-        if (jb >= 1) ok = pv(jb - 1);
+        ok = pv(jb);
       }
-      if (ok) pv(nkb - 1);
       if (*abort_flag) {
         volatile int no_abort = 0;
         tc_commit(drain);
@@ -259,6 +284,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld32(lane_base + st * 128 + half * 64 + 32, v[1]);
       tmem_ld_wait(v[0]);
       reg_fence32(v[1]);
+      tc_fence_before();
+      mbar_arrive(&s_free[st]);   // S buffer st may take S_{j+2} now
       const int k0 = jb * BLK + half * 64;
       if ((jb + 1) * BLK > a.s || (a.causal && (jb + 1) * BLK - 1 > q0)) {
         // diagonal or ragged block: invalid keys become −inf (branch-free)
