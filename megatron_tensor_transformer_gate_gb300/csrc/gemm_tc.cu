@@ -1,14 +1,21 @@
 // gemm_tc.cu — tcgen05 (5th-generation tensor core) GEMM of the TP block.
 //
-// One persistent kernel per GEMM launch: 192 threads per CTA, one CTA per SM.
-//   warp 0   TMA producer: one thread streams A and B tiles of 64 K-elements
-//            into a 4-stage shared-memory ring (128-byte swizzle).
-//   warp 1   allocates 512 TMEM columns (two 128×256 fp32 accumulators) and
-//            one thread issues tcgen05.mma (M=128, N=256, K=16) into them.
-//   warps 2–5 epilogue: tcgen05.ld of the finished accumulator (one TMEM lane
-//            = one output row per thread), the fused elementwise work of the
-//            launch, and 16-byte stores.  Double-buffered accumulators let
-//            the epilogue of tile i overlap the main loop of tile i+1.
+// One persistent kernel per GEMM launch over clusters of two CTAs (one CTA
+// per SM): the pair computes a 256×256 output tile with tcgen05.mma of
+// M=256 (cta_group::2), each CTA holding its 128 rows of A and half of the
+// B tile, so every SM streams 32 KB per 64-deep K block instead of 48 KB
+// and six stages fit in shared memory.  192 threads per CTA:
+//   warp 0   TMA producer: one thread streams this CTA's A rows and B half
+//            into a 6-stage ring (128-byte swizzle); the bytes of both CTAs
+//            are counted on the leader's (rank 0) barrier.
+//   warp 1   allocates 512 TMEM columns in both SMs (two 128×256 fp32
+//            accumulators per SM); one thread of the leader issues the MMAs
+//            and multicasts their completion to both CTAs.
+//   warps 2–5 epilogue (both CTAs): tcgen05.ld of the finished accumulator
+//            (one TMEM lane = one output row per thread), the fused
+//            elementwise work of the launch, 16-byte stores.  Double-
+//            buffered accumulators let the epilogue of tile i overlap the
+//            main loop of tile i+1.
 // The segment / part structure of the K loop is described in gemm.h; it is
 // how the shard sum of a row-parallel projection (g) or of an input gradient
 // (f) is taken in the accumulator ([Grasp-TP] §2–§3, [adu-TP] 算子 f 和 g).
@@ -25,12 +32,13 @@
 namespace tp {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;                        // rows per CTA (256 per pair)
+constexpr int BN = 256;                        // columns per tile
+constexpr int BNH = BN / 2;                    // B rows held by each CTA
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;           // 16 KB
-constexpr int B_BYTES = BN * BK * 2;           // 32 KB
+constexpr int B_BYTES = BNH * BK * 2;          // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int THREADS = 192;
@@ -252,7 +260,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p,
 
 // ------------------------------------------------------------------ kernel --
 template <int A_MN, int B_MN, int EPI>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -269,16 +277,21 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank() & 1u;
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
   constexpr int BN_LOG = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
 
   if (threadIdx.x == 0) {
+    // full: the leader's counts both CTAs' bytes; empty, tfull: one arrival
+    // from the leader's commits; tempty (leader's): both epilogues
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 2 * 128);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -291,21 +304,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (EPI == EPI_SWIGLU) tma_prefetch_desc(&p.mb2);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
+  cluster_sync();   // barriers of both CTAs initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------- TMA producer --
+      const uint32_t full0 = cluster_addr(full, 0);   // the leader's full[0]
       uint32_t stage = 0, phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+      for (int t = cid; ok && t < p.total_tiles; t += ncl) {
         int z, mt, nt;
         decode_tile(p, t, z, mt, nt);
-        const int m0 = mt * BM, n0 = nt * BN_LOG;
+        const int m0 = mt * 2 * BM + (int)rank * BM, n0 = nt * BN_LOG;
         for (int pi = 0; ok && pi < p.nparts; ++pi) {
           const TcPart& pt = p.part[pi];
           for (int j = 0; ok && j < pt.nsub; ++j) {
@@ -316,29 +331,33 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ok = false;
                 break;
               }
-              mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-              armed |= 1u << stage;
-              armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+              if (leader) {
+                mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+                armed |= 1u << stage;
+                armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+              }
+              const uint32_t fb = full0 + stage * 8;
               uint8_t* sa = smA + stage * A_BYTES;
               uint8_t* sb = smB + stage * B_BYTES;
               const int k0 = kb * BK;
               if (A_MN) {
-                tma_load_3d(sa, &p.ma[pi], &full[stage], m0, k0, seg);
-                tma_load_3d(sa + 8192, &p.ma[pi], &full[stage], m0 + 64, k0,
-                            seg);
+                tma_load_3d_pair(sa, &p.ma[pi], fb, m0, k0, seg);
+                tma_load_3d_pair(sa + 8192, &p.ma[pi], fb, m0 + 64, k0, seg);
               } else {
-                tma_load_3d(sa, &p.ma[pi], &full[stage], k0, seg, m0);
+                tma_load_3d_pair(sa, &p.ma[pi], fb, k0, seg, m0);
               }
               if (EPI == EPI_SWIGLU) {
-                tma_load_3d(sb, &p.mb[pi], &full[stage], k0, seg, n0);
-                tma_load_3d(sb + 16384, &p.mb2, &full[stage], k0, seg, n0);
+                // rank 0: the gate rows, rank 1: the up rows of the same units
+                tma_load_3d_pair(sb, leader ? &p.mb[pi] : &p.mb2, fb, k0, seg,
+                                 n0);
               } else if (B_MN) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  tma_load_3d(sb + q * 8192, &p.mb[pi], &full[stage],
-                              n0 + 64 * q, k0, seg);
+                tma_load_3d_pair(sb, &p.mb[pi], fb, n0 + (int)rank * BNH, k0,
+                                 seg);
+                tma_load_3d_pair(sb + 8192, &p.mb[pi], fb,
+                                 n0 + (int)rank * BNH + 64, k0, seg);
               } else {
-                tma_load_3d(sb, &p.mb[pi], &full[stage], k0, seg, n0);
+                tma_load_3d_pair(sb, &p.mb[pi], fb, k0, seg,
+                                 n0 + (int)rank * BNH);
               }
               if (++stage == STAGES) {
                 stage = 0;
@@ -348,8 +367,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (*abort_flag) {
-        // let every copy this thread started land before the CTA exits
+      if (ok) {
+        // the leader's last commits land on this CTA's empty barriers before
+        // the CTA may exit
+        for (int i = 0; i < STAGES; ++i) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status, 6))
+            break;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (*abort_flag && leader) {
+        // let every copy counted on this CTA's barriers land
         volatile int no_abort = 0;
         for (int s = 0; s < STAGES; ++s)
           if (armed & (1u << s))
@@ -357,16 +388,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (leader && lane == 0) {
       // -------------------------------------------------------- MMA issue --
-      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int it = 0;
-      for (int t = blockIdx.x; ok && t < p.total_tiles;
-           t += gridDim.x, ++it) {
-        int z, mt, nt;
-        decode_tile(p, t, z, mt, nt);
+      for (int t = cid; ok && t < p.total_tiles; t += ncl, ++it) {
         const int buf = it & 1;
         const uint32_t aphase = (it >> 1) & 1;
         if (!mbar_wait(&tempty[buf], aphase ^ 1, abort_flag, p.status, 2)) {
@@ -395,10 +423,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint64_t bd =
                     B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
                          : smem_desc_sw128(b0 + kk * 32, 16, 1024);
-                tc_mma_f16(d_tmem, ad, bd, IDESC, acc);
+                tc_mma_f16_pair(d_tmem, ad, bd, IDESC, acc);
                 acc = 1;
               }
-              tc_commit(&empty[stage]);
+              tc_commit_pair(&empty[stage], 3);
               if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1;
@@ -406,11 +434,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         }
-        if (ok) tc_commit(&tfull[buf]);
+        if (ok) tc_commit_pair(&tfull[buf], 3);
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
-        tc_commit(drain);
+        tc_commit_pair(drain, 1);
         mbar_wait(drain, 0, &no_abort, nullptr, 0);
       }
     }
@@ -418,8 +446,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue --
     const int quarter = warp & 3;   // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
+    const uint32_t tempty0 = cluster_addr(tempty, 0);   // the leader's
     int it = 0;
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+    for (int t = cid; t < p.total_tiles; t += ncl, ++it) {
       int z, mt, nt;
       decode_tile(p, t, z, mt, nt);
       const int buf = it & 1;
@@ -428,16 +457,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN;
-      epilogue_tile<EPI>(p, taddr, z, mt * BM + row, nt * BN_LOG);
+      epilogue_tile<EPI>(p, taddr, z, mt * 2 * BM + (int)rank * BM + row,
+                         nt * BN_LOG);
       tc_fence_before();
-      mbar_arrive(&tempty[buf]);
+      mbar_arrive_cluster(tempty0 + buf * 8);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();   // neither CTA leaves while the pair still uses it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ------------------------------------------------------------------- host --
@@ -482,17 +513,30 @@ bool encode_operand(CUtensorMap* m, const GemmOperand& o, int64_t kseg,
                    box_rows);
 }
 
+// One CTA pair per two SMs: the grid is as many pairs as can be resident
+// at once (clusters need both CTAs on SMs of one GPC), capped by the tiles.
 template <int A_MN, int B_MN, int EPI>
-int launch_inst(const TcParams& prm, int grid, cudaStream_t s, double flops,
+int launch_inst(const TcParams& prm, cudaStream_t s, double flops,
                 double bytes) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int clusters = 0;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(gemm_tc_kernel<A_MN, B_MN, EPI>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     SMEM_BYTES);
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)(device_sm_count() & ~1));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    attr_err = cudaOccupancyMaxActiveClusters(
+        &clusters, gemm_tc_kernel<A_MN, B_MN, EPI>, &cfg);
+    if (attr_err == cudaSuccess && clusters < 1) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
+  const int grid = 2 * std::min(prm.total_tiles, clusters);
   {
     ProfScope ps(s, KF_GEMM_TC, flops, bytes);
     gemm_tc_kernel<A_MN, B_MN, EPI><<<grid, THREADS, SMEM_BYTES, s>>>(prm);
@@ -535,7 +579,7 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
     const GemmPart& pt = pr.parts[i];
     if (!encode_operand(&prm.ma[i], pt.a, pt.kseg, pt.nseg, BM))
       return cudaErrorInvalidValue;
-    const uint32_t brows = (e.kind == EPI_SWIGLU) ? BN / 2 : BN;
+    const uint32_t brows = BNH;   // each CTA of the pair loads half of B
     if (!encode_operand(&prm.mb[i], pt.b, pt.kseg, pt.nseg, brows))
       return cudaErrorInvalidValue;
     if (e.kind == EPI_SWIGLU &&
@@ -549,15 +593,14 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
   const int bn_log = (e.kind == EPI_SWIGLU) ? BN / 2 : BN;
   prm.M = (int)pr.M;
   prm.N = (int)pr.N;
-  prm.m_tiles = (int)((pr.M + BM - 1) / BM);
+  prm.m_tiles = (int)((pr.M + 2 * BM - 1) / (2 * BM));   // CTA-pair tiles
   prm.n_tiles = (int)((pr.N + bn_log - 1) / bn_log);
   prm.nz = pr.nz;
   prm.total_tiles = prm.m_tiles * prm.n_tiles * pr.nz;
-  prm.group_m = 16;
+  prm.group_m = 8;
   prm.epi = e;
   prm.status = status;
   if (prm.total_tiles == 0) return cudaSuccess;
-  const int grid = std::min(prm.total_tiles, device_sm_count());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // algorithmic work of the launch: 2·M·N·K per batch, both B halves for
   // SwiGLU; bytes = operands read once + outputs written once
@@ -573,21 +616,21 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
 
   switch (e.kind) {
     case EPI_STORE:
-      if (!a_mn && !b_mn) return launch_inst<0, 0, EPI_STORE>(prm, grid, s, flops, bytes);
-      if (!a_mn && b_mn) return launch_inst<0, 1, EPI_STORE>(prm, grid, s, flops, bytes);
-      if (a_mn && b_mn) return launch_inst<1, 1, EPI_STORE>(prm, grid, s, flops, bytes);
-      return launch_inst<1, 0, EPI_STORE>(prm, grid, s, flops, bytes);
+      if (!a_mn && !b_mn) return launch_inst<0, 0, EPI_STORE>(prm, s, flops, bytes);
+      if (!a_mn && b_mn) return launch_inst<0, 1, EPI_STORE>(prm, s, flops, bytes);
+      if (a_mn && b_mn) return launch_inst<1, 1, EPI_STORE>(prm, s, flops, bytes);
+      return launch_inst<1, 0, EPI_STORE>(prm, s, flops, bytes);
     case EPI_GELU:
       if (a_mn || b_mn) return cudaErrorInvalidValue;
-      return launch_inst<0, 0, EPI_GELU>(prm, grid, s, flops, bytes);
+      return launch_inst<0, 0, EPI_GELU>(prm, s, flops, bytes);
     case EPI_SWIGLU:
-      return launch_inst<0, 0, EPI_SWIGLU>(prm, grid, s, flops, bytes);
+      return launch_inst<0, 0, EPI_SWIGLU>(prm, s, flops, bytes);
     case EPI_DGELU:
       if (a_mn || !b_mn) return cudaErrorInvalidValue;
-      return launch_inst<0, 1, EPI_DGELU>(prm, grid, s, flops, bytes);
+      return launch_inst<0, 1, EPI_DGELU>(prm, s, flops, bytes);
     case EPI_DSWIGLU:
       if (a_mn || !b_mn) return cudaErrorInvalidValue;
-      return launch_inst<0, 1, EPI_DSWIGLU>(prm, grid, s, flops, bytes);
+      return launch_inst<0, 1, EPI_DSWIGLU>(prm, s, flops, bytes);
   }
   return cudaErrorInvalidValue;
 }
