@@ -13,14 +13,20 @@
 //               dQ += dS·K                       (M=128, N=128, K=128) → TMEM
 //             Q and dO sit in TMEM as the A operands of S and dP.
 //   dK, dV    CTA = 128 keys of one (batch, kv head); per q head of the GQA
-//             group and block of 64 queries at or after the keys
-//               Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ          (M=128, N=64, K=128) → TMEM
-//               dV += Pᵀ·dO,  dK += dSᵀ·Q        (M=128, N=128, K=64) → TMEM
+//             group and block of 128 queries at or after the keys
+//               Sᵀ = K·Qᵀ, then dPᵀ = V·dOᵀ      (M=128, N=128, K=128) → TMEM
+//               dV += Pᵀ·dO,  dK += dSᵀ·Q        (M=128, N=128, K=128) → TMEM
+//             K and V sit in TMEM as the A operands; Sᵀ and dPᵀ of a block
+//             take turns in one 128-column TMEM buffer, which leaves room
+//             for both accumulators.
 // Both: warp 0 TMA, warp 1 TMEM allocation + single-thread MMA issue, warps
 // 2–9 elementwise (two threads per TMEM lane, half of the columns each).
 // The score MMAs of the next block are issued as soon as the elementwise
 // warps have copied the current scores to registers, ahead of the gradient
-// MMAs, so the tensor cores work while the elementwise warps do.  K and V
+// MMAs, so the tensor cores work while the elementwise warps do.  The
+// elementwise loops are unrolled but branch-free (masks come from padding
+// and a fix-up of the causal diagonal on packed words): a per-block body
+// that outgrows the instruction cache runs several times slower.  K and V
 // (dQ) or Q and dO (dK, dV) stream through rings of their own, each tile
 // freed by the last MMA that reads it.  A tcgen05.mma of M=128 costs about
 // the same for N=64 as for N=128, so the wider blocks do twice the work per
@@ -41,10 +47,8 @@ namespace {
 
 constexpr int HD = 128;
 constexpr int A128 = 128 * 128;   // one 64-column half of a 128-row tile
-constexpr int A64 = 64 * 128;     // one 64-column half of a 64-row tile
 constexpr int THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr float LN2 = 0.69314718055994531f;
 constexpr float LOG2E_F = 1.4426950408889634f;
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src,
@@ -60,24 +64,9 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src,
 __device__ __forceinline__ uint64_t dk128(uint32_t base, int kk, int atom) {
   return smem_desc_sw128(base + (kk >> 2) * atom + (kk & 3) * 32, 16, 1024);
 }
-// K-major operand with K = 64 (one 128-byte-wide half).
-__device__ __forceinline__ uint64_t dk64(uint32_t base, int kk) {
-  return smem_desc_sw128(base + kk * 32, 16, 1024);
-}
 // MN-major B: rows are K, N = 128 in two 64-wide halves `atom` bytes apart.
 __device__ __forceinline__ uint64_t dmn(uint32_t base, int kk, int atom) {
   return smem_desc_sw128(base + kk * 2048, atom, 1024);
-}
-
-// Write 32 fp16 values (16 packed words) as four 16-byte chunks of row r of
-// a K-major swizzled tile whose rows are 128 bytes (64 columns), starting at
-// 8-column chunk `c0`.
-__device__ __forceinline__ void st_row_chunks(uint8_t* tile, int r, int c0,
-                                              const uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    *reinterpret_cast<uint4*>(tile + r * 128 + (((c0 + q) ^ (r & 7)) << 4)) =
-        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
 __device__ __forceinline__ void store_bf16_row64(__nv_bfloat16* dst,
@@ -103,7 +92,8 @@ __device__ __forceinline__ void store_bf16_row64(__nv_bfloat16* dst,
 
 // ---------------------------------------------------------------- pre-pass --
 // One warp per (batch, head, padded position): D = Σ_d dO·O (dO fp16, O
-// bf16) and L2 = LSE·log2e; zeros past the sequence end.
+// bf16) and L2 = LSE·log2e.  Past the sequence end D = 0 and L2 = +∞, so
+// that P = exp2(S·c − L2) of a padded query is exactly 0 without a mask.
 __global__ void __launch_bounds__(256)
     attn_bwd_prepass_kernel(const __nv_bfloat16* __restrict__ O,
                             const __half* __restrict__ dO,
@@ -130,7 +120,7 @@ __global__ void __launch_bounds__(256)
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) {
     Dp[w] = acc;
-    L2p[w] = pos < s ? LSE[bh * s + pos] * LOG2E_F : 0.0f;
+    L2p[w] = pos < s ? LSE[bh * s + pos] * LOG2E_F : __int_as_float(0x7f800000);
   }
 }
 
@@ -153,6 +143,8 @@ struct BwdTcArgs {
   CUtensorMap mq, mk, mv, mdo;
   const __half* q;       // [b, s, nq·d] as the tensor maps
   const __half* dout;
+  const __half* k;       // [b, s, nkv·d]
+  const __half* v;
   const float* Dp;
   const float* L2p;
   __nv_bfloat16* out0;   // dQ, or dK
@@ -172,23 +164,32 @@ __device__ __forceinline__ void st_row8(uint8_t* tile, int r,
         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
-// dS for 32 keys of one query row: P = exp2(S·c − L2) (0 past the last key
-// this row may see), dS = P·(dP − D), packed in fp16 pairs.
+// dS for 32 keys of one query row: P = exp2(S·c − L2), dS = P·(dP − D),
+// packed in fp16 pairs (element 2j in the low half of word j).
 __device__ __forceinline__ void ds_chunk(const uint32_t (&sv)[32],
                                          const uint32_t (&pv)[32], float c,
-                                         float l2, float dd, bool masked,
-                                         int k0, int kmax, uint32_t* pk) {
+                                         float l2, float dd, uint32_t* pk) {
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
-    float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), c, -l2));
-    float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), c, -l2));
-    if (masked) {
-      p0 = (k0 + i <= kmax) ? p0 : 0.0f;
-      p1 = (k0 + i + 1 <= kmax) ? p1 : 0.0f;
-    }
+    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), c, -l2));
+    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), c, -l2));
     pk[i >> 1] = pack_f16x2(p0 * (__uint_as_float(pv[i]) - dd),
                             p1 * (__uint_as_float(pv[i + 1]) - dd));
   }
+}
+
+// Causal masks of a diagonal block on 64 fp16 values in 32 packed words:
+// keep elements [0, t] (keep_upto) or [t, 64) (keep_from), zero the rest.
+// Applied to packed words so the unrolled hot loops stay branch-free.
+__device__ __forceinline__ void keep_upto(uint32_t (&w)[32], int t) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    w[j] &= (2 * j > t) ? 0u : (2 * j + 1 > t ? 0x0000ffffu : 0xffffffffu);
+}
+__device__ __forceinline__ void keep_from(uint32_t (&w)[32], int t) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    w[j] &= (2 * j + 1 < t) ? 0u : (2 * j < t ? 0xffff0000u : 0xffffffffu);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -366,7 +367,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(q_full);
     }
-    const int kmax = a.causal ? min(qi, a.s - 1) : a.s - 1;
     bool ok = true;
     for (int jb = 0; jb < nkb; ++jb) {
       const int bb = jb & 1;
@@ -386,12 +386,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       reg_fence32(p1);
       tc_fence_before();
       mbar_arrive(sdp_free);
-      const int k0 = jb * 128 + half * 64;
-      const bool masked =
-          (jb * 128 + 128 > a.s) || (a.causal && jb * 128 + 127 > q0);
+      // keys past the end need no mask: their K rows are zero, so they add
+      // nothing to dS·K; on the causal diagonal keep keys ≤ the query
       uint32_t pk[32];
-      ds_chunk(s0, p0, c, l2, dd, masked, k0, kmax, pk);
-      ds_chunk(s1, p1, c, l2, dd, masked, k0 + 32, kmax, pk + 16);
+      ds_chunk(s0, p0, c, l2, dd, pk);
+      ds_chunk(s1, p1, c, l2, dd, pk + 16);
+      if (a.causal && jb * 128 == q0) keep_upto(pk, r - half * 64);
       // the dS buffer is free once dQ += dS_{j-2}·K_{j-2} has completed
       if (jb >= 2 && !mbar_wait_warp(&ds_free[bb], ((jb - 2) >> 1) & 1,
                                      abort_flag, a.status, 37)) {
@@ -425,19 +425,22 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ------------------------------------------------------------------ dK, dV --
 namespace dkv {
-constexpr int OFF_K = 0;
-constexpr int OFF_V = 2 * A128;
-constexpr int OFF_QS = 4 * A128;                 // NST stages
-constexpr int STAGE = 4 * A64;                   // Q 16 KB, dO 16 KB
-constexpr int NST = 4;
-constexpr int OFF_P = OFF_QS + NST * STAGE;      // 16 KB
-constexpr int OFF_DS = OFF_P + A128;             // 16 KB
-constexpr int OFF_ST = OFF_DS + A128;            // NST × (64 L2, 64 D) fp32
-constexpr int OFF_BAR = OFF_ST + NST * 512;
+constexpr int NQ = 3, NO = 2;                  // Q ring and dO ring depths
+constexpr int TILE = 2 * A128;                 // 128 rows × 128 d, 32 KB
+constexpr int OFF_Q = 0;
+constexpr int OFF_O = OFF_Q + NQ * TILE;
+constexpr int OFF_P = OFF_O + NO * TILE;       // Pᵀ: 128 keys × 128 queries
+constexpr int OFF_DS = OFF_P + TILE;           // dSᵀ
+constexpr int OFF_QST = OFF_DS + TILE;         // NQ × 128 LSE·log2e
+constexpr int OFF_OST = OFF_QST + NQ * 512;    // NO × 128 D
+constexpr int OFF_BAR = OFF_OST + NO * 512;
 // No alignment slack: the kernel checks that the dynamic shared memory
 // starts on a 1024-byte boundary (as the 128-byte swizzle requires).
 constexpr int SMEM = OFF_BAR + 256;
-constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
+// K and V in TMEM as the A operands of Sᵀ and dPᵀ; Sᵀ and then dPᵀ of each
+// block take turns in X; dV and dK accumulate in the last 256 columns.
+constexpr uint32_t COL_K = 0, COL_V = 64, COL_X = 128, COL_DV = 256,
+                   COL_DK = 384;
 }  // namespace dkv
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -450,39 +453,47 @@ __global__ void __launch_bounds__(THREADS, 1)
     return;
   }
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint64_t* kv_full = bar;         // K and V
-  uint64_t* qs_full = bar + 1;     // [NST] Q, dO, stats
-  uint64_t* qs_empty = bar + 5;    // [NST]
-  uint64_t* sdp_full = bar + 9;    // [2]
-  uint64_t* sdp_free = bar + 11;   // [2] Sᵀ, dPᵀ copied to registers
-  uint64_t* pds_full = bar + 13;   // Pᵀ and dSᵀ written
-  uint64_t* pds_free = bar + 14;   // gradient MMAs done with them
-  uint64_t* done = bar + 15;
-  uint64_t* drain = bar + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 17);
+  uint64_t* q_full = bar;              // [NQ] Q tile + its LSE·log2e
+  uint64_t* q_empty = q_full + NQ;     // [NQ]
+  uint64_t* o_full = q_empty + NQ;     // [NO] dO tile + its D
+  uint64_t* o_empty = o_full + NO;     // [NO]
+  uint64_t* kv_full = o_empty + NO;    // K and V written to TMEM
+  uint64_t* x_full = kv_full + 1;      // Sᵀ, then dPᵀ, in X
+  uint64_t* x_free = x_full + 1;       // X copied to registers
+  uint64_t* p_full = x_free + 1;       // Pᵀ written
+  uint64_t* p_free = p_full + 1;       // dV += Pᵀ·dO done with it
+  uint64_t* ds_full = p_free + 1;      // dSᵀ written
+  uint64_t* ds_free = ds_full + 1;     // dK += dSᵀ·Q done with it
+  uint64_t* done = ds_free + 1;
+  uint64_t* drain = done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, kvh = blockIdx.y;
   const int k0 = blockIdx.x * 128;
   const int group = a.nq / a.nkv;
-  const int nqb = (a.s + 63) / 64;
-  const int qb_first = a.causal ? k0 / 64 : 0;
+  const int nqb = (a.s + 127) / 128;
+  const int qb_first = a.causal ? k0 / 128 : 0;
   const int per_head = nqb - qb_first;
   const int iters = per_head * group;
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&qs_full[i], 1);
-      mbar_init(&qs_empty[i], 1);
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&sdp_free[i], 256);
+    for (int i = 0; i < NO; ++i) {
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_empty[i], 1);
     }
-    mbar_init(pds_full, 256);
-    mbar_init(pds_free, 1);
+    mbar_init(kv_full, 256);
+    mbar_init(x_full, 1);
+    mbar_init(x_free, 256);
+    mbar_init(p_full, 256);
+    mbar_init(p_free, 1);
+    mbar_init(ds_full, 256);
+    mbar_init(ds_free, 1);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -495,101 +506,105 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch_desc(&a.mq);
-      tma_prefetch_desc(&a.mdo);
-      tma_prefetch_desc(&a.mk);
-      tma_prefetch_desc(&a.mv);
+    if (lane < 2) {
+      // lane 0: Q tiles and their LSE (freed after dK += dSᵀ·Q);
+      // lane 1: dO tiles and their D (freed after dV += Pᵀ·dO)
+      const bool is_q = lane == 0;
+      const CUtensorMap* map = is_q ? &a.mq : &a.mdo;
+      uint64_t* full = is_q ? q_full : o_full;
+      uint64_t* empty = is_q ? q_empty : o_empty;
+      uint8_t* ring = sm + (is_q ? OFF_Q : OFF_O);
+      uint8_t* stats = sm + (is_q ? OFF_QST : OFF_OST);
+      const float* src_stats = is_q ? a.L2p : a.Dp;
+      const int depth = is_q ? NQ : NO;
+      tma_prefetch_desc(map);
       uint32_t armed = 0, armed_par = 0;
-      mbar_arrive_expect_tx(kv_full, 4 * A128);
-      for (int hh = 0; hh < 2; ++hh) {
-        tma_load_3d(sm + OFF_K + hh * A128, &a.mk, kv_full, kvh * HD + hh * 64,
-                    k0, b);
-        tma_load_3d(sm + OFF_V + hh * A128, &a.mv, kv_full, kvh * HD + hh * 64,
-                    k0, b);
-      }
       for (int it = 0; it < iters; ++it) {
-        const int st = it % NST;
-        const uint32_t ph = (it / NST) & 1;
-        if (!mbar_wait(&qs_empty[st], ph ^ 1, abort_flag, a.status, 41)) break;
+        const int st = it % depth;
+        const uint32_t ph = (it / depth) & 1;
+        if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, a.status, 41)) break;
         const int jq = kvh * group + it / per_head;
         const int qb = qb_first + it % per_head;
-        mbar_arrive_expect_tx(&qs_full[st], 4 * A64 + 512);
+        mbar_arrive_expect_tx(&full[st], TILE + 512);
         armed |= 1u << st;
         armed_par = (armed_par & ~(1u << st)) | (ph << st);
-        uint8_t* stg = sm + OFF_QS + st * STAGE;
-        for (int hh = 0; hh < 2; ++hh) {
-          tma_load_3d(stg + hh * A64, &a.mq, &qs_full[st], jq * HD + hh * 64,
-                      qb * 64, b);
-          tma_load_3d(stg + 2 * A64 + hh * A64, &a.mdo, &qs_full[st],
-                      jq * HD + hh * 64, qb * 64, b);
-        }
-        const int64_t soff = ((int64_t)b * a.nq + jq) * a.s_pad + qb * 64;
-        uint8_t* sst = sm + OFF_ST + st * 512;
-        bulk_load(sst, a.L2p + soff, 256, &qs_full[st]);
-        bulk_load(sst + 256, a.Dp + soff, 256, &qs_full[st]);
+        for (int hh = 0; hh < 2; ++hh)
+          tma_load_3d(ring + st * TILE + hh * A128, map, &full[st],
+                      jq * HD + hh * 64, qb * 128, b);
+        const int64_t soff = ((int64_t)b * a.nq + jq) * a.s_pad + qb * 128;
+        bulk_load(stats + st * 512, src_stats + soff, 512, &full[st]);
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
-        mbar_wait(kv_full, 0, &no_abort, nullptr, 0);
-        for (int st = 0; st < NST; ++st)
+        for (int st = 0; st < depth; ++st)
           if (armed & (1u << st))
-            mbar_wait(&qs_full[st], (armed_par >> st) & 1u, &no_abort, nullptr,
-                      0);
+            mbar_wait(&full[st], (armed_par >> st) & 1u, &no_abort, nullptr, 0);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_f16_f32(128, 64, 0, 0);
+      constexpr uint32_t IDESC_S = idesc_f16_f32(128, 128, 0, 0);
       constexpr uint32_t IDESC_G = idesc_f16_f32(128, 128, 0, 1);
-      const uint32_t sK = smem_u32(sm + OFF_K), sV = smem_u32(sm + OFF_V);
       bool ok = mbar_wait(kv_full, 0, abort_flag, a.status, 42);
-      // Sᵀ and dPᵀ run two iterations ahead of the gradient MMAs
-      auto sdp_mma = [&](int it) -> bool {
-        const int st = it % NST, bb = it & 1;
-        if (!mbar_wait(&qs_full[st], (it / NST) & 1, abort_flag, a.status, 44))
-          return false;
+      tc_fence_after();
+      // dV += Pᵀ·dO of block i (releases Pᵀ and the dO tile)
+      auto dv_mma = [&](int i) -> bool {
+        if (!mbar_wait(p_full, i & 1, abort_flag, a.status, 43)) return false;
         tc_fence_after();
-        const uint32_t stg = smem_u32(sm + OFF_QS + st * STAGE);
+        const uint32_t sdO = smem_u32(sm + OFF_O + (i % NO) * TILE);
+        const uint32_t sP = smem_u32(sm + OFF_P);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {   // the two chains interleaved
-          tc_mma_f16(tmem + COL_S + bb * 64, dk128(sK, kk, A128),
-                     dk128(stg, kk, A64), IDESC_S, kk > 0 ? 1u : 0u);
-          tc_mma_f16(tmem + COL_DP + bb * 64, dk128(sV, kk, A128),
-                     dk128(stg + 2 * A64, kk, A64), IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&sdp_full[bb]);
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem + COL_DV, dk128(sP, kk, A128), dmn(sdO, kk, A128),
+                     IDESC_G, (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(p_free);
+        tc_commit(&o_empty[i % NO]);
         return true;
       };
-      auto grads = [&](int i) -> bool {
-        const int st = i % NST;
-        if (!mbar_wait(pds_full, i & 1, abort_flag, a.status, 43)) return false;
+      // dK += dSᵀ·Q of block i (releases dSᵀ and the Q tile)
+      auto dk_mma = [&](int i) -> bool {
+        if (!mbar_wait(ds_full, i & 1, abort_flag, a.status, 52)) return false;
         tc_fence_after();
-        const uint32_t stg = smem_u32(sm + OFF_QS + st * STAGE);
-        const uint32_t sP = smem_u32(sm + OFF_P);
+        const uint32_t sQ = smem_u32(sm + OFF_Q + (i % NQ) * TILE);
         const uint32_t sdS = smem_u32(sm + OFF_DS);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {   // the two chains interleaved
-          tc_mma_f16(tmem + COL_DV, dk64(sP, kk), dmn(stg + 2 * A64, kk, A64),
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem + COL_DK, dk128(sdS, kk, A128), dmn(sQ, kk, A128),
                      IDESC_G, (i > 0 || kk > 0) ? 1u : 0u);
-          tc_mma_f16(tmem + COL_DK, dk64(sdS, kk), dmn(stg, kk, A64), IDESC_G,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(pds_free);
-        tc_commit(&qs_empty[st]);
+        tc_commit(ds_free);
+        tc_commit(&q_empty[i % NQ]);
         return true;
       };
-      if (ok) ok = sdp_mma(0);
-      if (ok && iters > 1) ok = sdp_mma(1);
+      // per block: Sᵀ(it); dPᵀ(it) as soon as Sᵀ(it) is in registers; dK of
+      // it−1 (its dSᵀ was written while Sᵀ(it) ran); dV of it (Pᵀ(it) is
+      // written while dPᵀ(it) and dK(it−1) run)
       for (int it = 0; ok && it < iters; ++it) {
-        if (it + 2 < iters) {
-          ok = mbar_wait(&sdp_free[it & 1], (it >> 1) & 1, abort_flag,
-                         a.status, 45) &&
-               sdp_mma(it + 2);
-          if (!ok) break;
-        }
-        ok = grads(it);
+        ok = mbar_wait(&q_full[it % NQ], (it / NQ) & 1, abort_flag, a.status,
+                       44) &&
+             (it == 0 || mbar_wait(x_free, 1, abort_flag, a.status, 45));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(sm + OFF_Q + (it % NQ) * TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16_ts(tmem + COL_X, tmem + COL_K + kk * 8,
+                        dk128(sQ, kk, A128), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(x_full);
+        ok = mbar_wait(&o_full[it % NO], (it / NO) & 1, abort_flag, a.status,
+                       49) &&
+             mbar_wait(x_free, 0, abort_flag, a.status, 50);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sdO = smem_u32(sm + OFF_O + (it % NO) * TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16_ts(tmem + COL_X, tmem + COL_V + kk * 8,
+                        dk128(sdO, kk, A128), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(x_full);
+        if (it > 0 && !(ok = dk_mma(it - 1))) break;
+        if (!(ok = dv_mma(it))) break;
       }
+      if (ok && iters > 0) ok = dk_mma(iters - 1);
       if (ok) tc_commit(done);
       if (*abort_flag) {
         volatile int no_abort = 0;
@@ -599,75 +614,131 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------ elementwise --
+    // thread: key row r (TMEM lane), queries [64·half, 64·half + 64) of
+    // each block
     const int half = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int key = k0 + r;
     const uint32_t lanes = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c = a.scale_log2;
+    const int64_t ldk = (int64_t)a.nkv * HD;
+    const int64_t row = ((int64_t)b * a.s + key) * ldk + kvh * HD + half * 64;
+    {
+      // this thread's half row of K and of V into TMEM (zeros past the end)
+      uint32_t kv[32];
+      const __half* const srcs[2] = {a.k, a.v};
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint4* src = reinterpret_cast<const uint4*>(srcs[t] + row);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 u = key < a.s ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+          kv[4 * i] = u.x;
+          kv[4 * i + 1] = u.y;
+          kv[4 * i + 2] = u.z;
+          kv[4 * i + 3] = u.w;
+        }
+        tmem_st32(lanes + (t == 0 ? COL_K : COL_V) + half * 32, kv);
+      }
+      tc_fence_before();
+      mbar_arrive(kv_full);
+    }
     bool ok = true;
     for (int it = 0; it < iters; ++it) {
-      const int st = it & 1;
-      if (!mbar_wait_warp(&sdp_full[st], (it >> 1) & 1, abort_flag, a.status,
-                          46)) {
+      const int qb = qb_first + it % per_head;
+      // queries past the end have L2 = +∞ (P = 0); keys past the end feed
+      // only dK, dV rows that are never stored; the causal diagonal block
+      // keeps queries ≥ the key
+      const bool diag = a.causal && qb * 128 == k0;
+      // Sᵀ → P, kept in fp16
+      if (!mbar_wait_warp(x_full, 0, abort_flag, a.status, 46)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sv[32], pv[32];
-      tmem_ld32(lanes + COL_S + st * 64 + half * 32, sv);
-      tmem_ld32(lanes + COL_DP + st * 64 + half * 32, pv);
-      tmem_ld_wait(sv);
-      reg_fence32(pv);
+      uint32_t x0[32], x1[32];
+      tmem_ld32(lanes + COL_X + half * 64, x0);
+      tmem_ld32(lanes + COL_X + half * 64 + 32, x1);
+      tmem_ld_wait(x0);
+      reg_fence32(x1);
       tc_fence_before();
-      mbar_arrive(&sdp_free[st]);
-      const int qb = qb_first + it % per_head;
-      const int qc0 = qb * 64 + half * 32;   // first query column of this half
-      const float* stats =
-          reinterpret_cast<const float*>(sm + OFF_ST + (it % NST) * 512);
-      const bool masked = (qb * 64 + 64 > a.s) || (k0 + 128 > a.s) ||
-                          (a.causal && qb * 64 < k0 + 127);
-      uint32_t pp[16], pd[16];
+      mbar_arrive(x_free);
+      // LSE·log2e of this half's 64 queries: all loads issued before use
+      const float4* lst = reinterpret_cast<const float4*>(
+                              sm + OFF_QST + (it % NQ) * 512) +
+                          half * 16;
+      uint32_t pp[32];   // P in fp16 pairs (Pᵀ row of this key)
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(stats + half * 32 + i);
-        const float4 d4 =
-            *reinterpret_cast<const float4*>(stats + 64 + half * 32 + i);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-        float p[4], ds[4];
+      for (int ch = 0; ch < 2; ++ch) {
+        float lv[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          p[e] = ex2_approx(fmaf(__uint_as_float(sv[i + e]), c, -lv[e]));
-          if (masked) {
-            const int q = qc0 + i + e;
-            const bool valid =
-                q < a.s && key < a.s && (!a.causal || key <= q);
-            p[e] = valid ? p[e] : 0.0f;
-          }
-          ds[e] = p[e] * (__uint_as_float(pv[i + e]) - dv[e]);
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4*>(&lv[4 * i]) = lst[ch * 8 + i];
+        const uint32_t(&xs)[32] = ch == 0 ? x0 : x1;
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(xs[i]), c, -lv[i]));
+          const float p1 =
+              ex2_approx(fmaf(__uint_as_float(xs[i + 1]), c, -lv[i + 1]));
+          pp[ch * 16 + (i >> 1)] = pack_f16x2(p0, p1);
         }
-        pp[i >> 1] = pack_f16x2(p[0], p[1]);
-        pp[(i >> 1) + 1] = pack_f16x2(p[2], p[3]);
-        pd[i >> 1] = pack_f16x2(ds[0], ds[1]);
-        pd[(i >> 1) + 1] = pack_f16x2(ds[2], ds[3]);
       }
-      // the P / dS tiles are free once the gradient MMAs of it−1 finished
-      if (it >= 1 && !mbar_wait_warp(pds_free, (it - 1) & 1, abort_flag,
-                                     a.status, 47)) {
+      if (diag) keep_from(pp, r - half * 64);
+      // Pᵀ(it) out now: the tile is free once dV of it−1 has completed
+      if (it >= 1 &&
+          !mbar_wait_warp(p_free, (it - 1) & 1, abort_flag, a.status, 47)) {
         ok = false;
         break;
       }
-      st_row_chunks(sm + OFF_P, r, half * 4, pp);
-      st_row_chunks(sm + OFF_DS, r, half * 4, pd);
+      st_row8(sm + OFF_P + half * A128, r, pp);
       fence_proxy_async_smem();
-      mbar_arrive(pds_full);
+      mbar_arrive(p_full);
+      // dPᵀ → dS = P ⊙ (dP − D), P taken in its fp16 form
+      if (!mbar_wait_warp(x_full, 1, abort_flag, a.status, 51)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_ld32(lanes + COL_X + half * 64, x0);
+      tmem_ld32(lanes + COL_X + half * 64 + 32, x1);
+      tmem_ld_wait(x0);
+      reg_fence32(x1);
+      tc_fence_before();
+      mbar_arrive(x_free);
+      const float4* dst = reinterpret_cast<const float4*>(
+                              sm + OFF_OST + (it % NO) * 512) +
+                          half * 16;
+      uint32_t pd[32];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        float dv[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(&dv[4 * i]) = dst[ch * 4 + i];
+        const uint32_t(&xs)[32] = ch < 2 ? x0 : x1;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const int e = (ch & 1) * 16 + i;   // index within xs
+          const float2 pf = unpack_f16x2(pp[ch * 8 + (i >> 1)]);
+          pd[ch * 8 + (i >> 1)] =
+              pack_f16x2(pf.x * (__uint_as_float(xs[e]) - dv[i]),
+                         pf.y * (__uint_as_float(xs[e + 1]) - dv[i + 1]));
+        }
+      }
+      // dSᵀ(it) out: the tile is free once dK of it−1 has completed
+      if (it >= 1 &&
+          !mbar_wait_warp(ds_free, (it - 1) & 1, abort_flag, a.status, 53)) {
+        ok = false;
+        break;
+      }
+      st_row8(sm + OFF_DS + half * A128, r, pd);
+      fence_proxy_async_smem();
+      mbar_arrive(ds_full);
     }
     if (iters > 0 && __all_sync(0xffffffffu, ok) &&
         mbar_wait_warp(done, 0, abort_flag, a.status, 48)) {
       tc_fence_after();
-      const int64_t ldk = (int64_t)a.nkv * HD;
-      const int64_t row = ((int64_t)b * a.s + key) * ldk + kvh * HD + half * 64;
       uint32_t o0[32], o1[32];
       tmem_ld32(lanes + COL_DK + half * 64, o0);
       tmem_ld32(lanes + COL_DK + half * 64 + 32, o1);
@@ -723,13 +794,13 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   }
   BwdTcArgs a;
   memset(&a, 0, sizeof(a));
-  // Q and dO in 64-row boxes (the dK/dV kernel), K and V in 128-row boxes
+  // all four in 128-row boxes of 64 columns
   const uint64_t ldq = (uint64_t)sh.nq * HD * 2, ldk = (uint64_t)sh.nkv * HD * 2;
   const bool ok =
       encode_tmap_3d_f16(&a.mq, Q, (uint64_t)sh.nq * HD, sh.s, sh.b, ldq,
-                         ldq * sh.s, 64, 64, 1) &&
+                         ldq * sh.s, 64, 128, 1) &&
       encode_tmap_3d_f16(&a.mdo, dO, (uint64_t)sh.nq * HD, sh.s, sh.b, ldq,
-                         ldq * sh.s, 64, 64, 1) &&
+                         ldq * sh.s, 64, 128, 1) &&
       encode_tmap_3d_f16(&a.mk, K, (uint64_t)sh.nkv * HD, sh.s, sh.b, ldk,
                          ldk * sh.s, 64, 128, 1) &&
       encode_tmap_3d_f16(&a.mv, V, (uint64_t)sh.nkv * HD, sh.s, sh.b, ldk,
@@ -737,6 +808,8 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   if (!ok) return cudaErrorInvalidValue;
   a.q = static_cast<const __half*>(Q);
   a.dout = static_cast<const __half*>(dO);
+  a.k = static_cast<const __half*>(K);
+  a.v = static_cast<const __half*>(V);
   a.Dp = Dp;
   a.L2p = L2p;
   a.s = (int)sh.s;
