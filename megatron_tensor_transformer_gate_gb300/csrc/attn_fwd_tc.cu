@@ -10,13 +10,15 @@
 //              64-column halves); lane 0 feeds K, lane 1 feeds V.
 //   warp 1     allocates 512 TMEM columns and issues, per key block j,
 //                S_j = Q·K_jᵀ   (M=128, N=128, K=128) into TMEM S[j mod 2]
-//                O += P_j·V_j   (M=128, N=128, K=128) into TMEM O
+//                O += P_j·V_j   (M=128, N=128, K=128) into TMEM O, with
+//                               P_j read from TMEM P[j mod 2]
 //              with the scores two blocks ahead (S_0, S_1, S_2, PV_0, S_3,
 //              PV_1, …) so the tensor cores never wait for a softmax block.
 //   warps 2–9  softmax, two threads per query row (same TMEM lane, one per
 //              64-column half), reference
-//              max m and sum l in fp32, P_j = exp2(S·scale·log2e − m) written
-//              as fp16 into the K-major swizzled layout the MMA reads.
+//              max m and sum l in fp32, P_j = exp2(S·scale·log2e − m) stored
+//              as fp16 pairs into TMEM (double-buffered, so block j+1 is
+//              written while O += P_j·V_j runs).
 //              O accumulates in TMEM; when a block's max exceeds
 //              m by more than 2^8 the softmax rescales O and l by
 //              exp2(m − m_new) first.  The epilogue writes O / l (bf16) and
@@ -47,14 +49,15 @@ constexpr int THREADS = 320;   // TMA, MMA, 8 softmax warps
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + TILE;      // 2 stages
 constexpr int OFF_V = OFF_K + 2 * TILE;  // 2 stages
-constexpr int OFF_P = OFF_V + 2 * TILE;
-constexpr int OFF_BAR = OFF_P + TILE;
+constexpr int OFF_BAR = OFF_V + 2 * TILE;
 constexpr int OFF_RED = OFF_BAR + 256;   // row-max / row-sum exchange
 constexpr int RED_SLOTS = 3;             // 2 for block parity, 1 for the end
 constexpr int OFF_SEQ = OFF_RED + RED_SLOTS * 2 * 128 * 4;
 constexpr int SMEM = OFF_SEQ + RED_SLOTS * 2 * 128 * 4 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_O = 256;
+// TMEM: S[2] in columns 0-255, O in 256-383, P[2] (fp16 pairs, the A
+// operand of O += P·V) in 384-511.
+constexpr uint32_t COL_O = 256, COL_P = 384;
 // The output accumulates in TMEM against a reference max m; it is rescaled
 // only when a block's row max exceeds m by more than this (log2 units), which
 // keeps the fp16 probabilities ≤ 2^8 and the fp32 accumulator far from
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // cores never wait for the softmax to finish a block.
       constexpr uint32_t IDESC_S = idesc_f16_f32(128, 128, 0, 0);
       constexpr uint32_t IDESC_O = idesc_f16_f32(128, 128, 0, 1);
-      const uint32_t sQ = smem_u32(sm + OFF_Q), sP = smem_u32(sm + OFF_P);
+      const uint32_t sQ = smem_u32(sm + OFF_Q);
       bool ok = mbar_wait(q_full, 0, abort_flag, a.status, 12);
       auto s_mma = [&](int jb) -> bool {
         const int st = jb & 1;
@@ -230,8 +233,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t sV = smem_u32(sm + OFF_V + (i & 1) * TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem + COL_O, desc_kmajor(sP, kk), desc_mnmajor(sV, kk),
-                     IDESC_O, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16_ts(tmem + COL_O, tmem + COL_P + (i & 1) * 64 + kk * 8,
+                        desc_mnmajor(sV, kk), IDESC_O,
+                        (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&pv_done[i & 1]);
         tc_commit(&v_empty[i & 1]);
         return true;
@@ -345,21 +349,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         l_part *= alpha;
         m_ref = m_new;
       }
-      // the P tile is free once O += P_{j-1}·V_{j-1} has completed
-      if (jb >= 1 && !mbar_wait_warp(&pv_done[(jb - 1) & 1], ((jb - 1) >> 1) & 1,
+      // P buffer st is free once O += P_{j-2}·V_{j-2} has completed
+      if (jb >= 2 && !mbar_wait_warp(&pv_done[st], ((jb - 2) >> 1) & 1,
                                      abort_flag, a.status, 18)) {
         ok = false;
         break;
       }
-      // P = exp2(c·(s − m)), fp16, into key half `half` of the swizzled tile
+      // P = exp2(c·(s − m)) in fp16 pairs into this half's 32 columns of P[st]
       const float neg = -m_ref * c;
-      uint8_t* prow = sm + OFF_P + half * ATOM + r * 128;
       float sum8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
+      uint32_t pk[32];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(v[cc][i]), c, neg));
@@ -367,18 +370,12 @@ __global__ void __launch_bounds__(THREADS, 1)
               ex2_approx(fmaf(__uint_as_float(v[cc][i + 1]), c, neg));
           sum8[i & 7] += p0;
           sum8[(i + 1) & 7] += p1;
-          pk[i >> 1] = pack_f16x2(p0, p1);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk = cc * 4 + q;
-          *reinterpret_cast<uint4*>(prow + ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          pk[cc * 16 + (i >> 1)] = pack_f16x2(p0, p1);
         }
       }
+      tmem_st32(lane_base + COL_P + st * 64 + half * 32, pk);
       l_part += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
                 ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[st]);
     }
