@@ -27,6 +27,13 @@ struct Vec;  // 16-byte vector of T
 template <>
 struct Vec<float> {
   static constexpr int N = 4;
+  __device__ static void from_raw(uint4 u, float* v) {
+    v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+  }
+  __device__ static void store_f32(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
   __device__ static void load(const float* p, float* v) {
     const float4 u = *reinterpret_cast<const float4*>(p);
     v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
@@ -38,6 +45,16 @@ struct Vec<float> {
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int N = 8;
+  __device__ static void from_raw(uint4 u, float* v) {
+    float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y),
+           c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
+  }
+  __device__ static void store_f32(float* p, const float* v) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
   __device__ static void load(const __nv_bfloat16* p, float* v) {
     const uint4 u = *reinterpret_cast<const uint4*>(p);
     float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y),
@@ -170,15 +187,26 @@ __global__ void __launch_bounds__(256)
 }
 
 // Stage 2: out[c] = Σ_chunk partial[chunk][c] in chunk order.
+// Stage 2: out[c] = Σ_k partial[k][c].  A block of 8 warps takes 32
+// columns; warp w adds chunks w, w + 8, … for its lane's column, then warp 0
+// adds the 8 warp sums in order (fixed order: reruns are bit-identical).
 template <typename T>
 __global__ void __launch_bounds__(256)
     colsum_stage2(const float* __restrict__ partial, int chunks, int64_t cols,
                   T* __restrict__ out) {
-  for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols;
-       c += (int64_t)gridDim.x * blockDim.x) {
-    float s = 0.0f;
-    for (int k = 0; k < chunks; ++k) s += partial[(int64_t)k * cols + c];
-    out[c] = from_f<T>(s);
+  __shared__ float red[8][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 32 + lane;
+  float s = 0.0f;
+  if (c < cols)
+    for (int k = w; k < chunks; k += 8) s += partial[(int64_t)k * cols + c];
+  red[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && c < cols) {
+    float t = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += red[i][lane];
+    out[c] = from_f<T>(t);
   }
 }
 
@@ -222,11 +250,14 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Block = rows [chunk·rpc, …); per row: g = dy⊙γ, dot = Σ g·x,
-// dx = rstd·g − x·rstd³·dot/h (+ dres); dγ partial Σ_rows dy·x·rstd kept in
-// registers (each thread owns at most MAXC columns) and written per chunk.
-template <typename T, int MAXC>
-__global__ void __launch_bounds__(256)
+// One block of 512 threads per chunk of consecutive rows (about one chunk
+// per SM); each thread owns the 16-byte column vectors {V·(tid + 512·j)},
+// keeps γ and its dγ partial sums in registers, and loads the next row's dy
+// and x while it finishes the current one.  Per row: dot = Σ dy·γ·x (block
+// reduction through a double-buffered slot, one barrier),
+//   dx = dres + rstd·dy·γ − x·rstd³·dot / h,   dγ_partial += dy·x·rstd.
+template <typename T, int NV>
+__global__ void __launch_bounds__(512, 1)
     rmsnorm_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
                        const T* __restrict__ gamma,
                        const float* __restrict__ rstd,
@@ -234,68 +265,96 @@ __global__ void __launch_bounds__(256)
                        float* __restrict__ dg_partial, int64_t rows, int64_t h,
                        int64_t rpc) {
   constexpr int V = Vec<T>::N;
-  __shared__ float red[8];
-  float dgacc[MAXC];
+  __shared__ float red[2][16];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int64_t col[NV];
+  bool on[NV];
 #pragma unroll
-  for (int j = 0; j < MAXC; ++j) dgacc[j] = 0.0f;
+  for (int j = 0; j < NV; ++j) {
+    col[j] = ((int64_t)threadIdx.x + 512 * j) * V;
+    on[j] = col[j] < h;
+  }
+  float g[NV * V], dgacc[NV * V];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    if (on[j]) {
+      Vec<T>::load(gamma + col[j], g + j * V);
+    } else {
+#pragma unroll
+      for (int q = 0; q < V; ++q) g[j * V + q] = 0.0f;
+    }
+#pragma unroll
+    for (int q = 0; q < V; ++q) dgacc[j * V + q] = 0.0f;
+  }
   const int64_t r_begin = (int64_t)blockIdx.x * rpc;
   const int64_t r_end = min(rows, r_begin + rpc);
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 cd[NV], cx[NV];   // current row, raw 16-byte vectors
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const bool ld = on[j] && r_begin < r_end;
+    cd[j] = ld ? *reinterpret_cast<const uint4*>(dy + r_begin * h + col[j])
+               : zero;
+    cx[j] = ld ? *reinterpret_cast<const uint4*>(x + r_begin * h + col[j])
+               : zero;
+  }
   for (int64_t r = r_begin; r < r_end; ++r) {
+    uint4 nd[NV], nx[NV], dr[NV];
+    const bool more = r + 1 < r_end;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      nd[j] = (more && on[j])
+                  ? *reinterpret_cast<const uint4*>(dy + (r + 1) * h + col[j])
+                  : zero;
+      nx[j] = (more && on[j])
+                  ? *reinterpret_cast<const uint4*>(x + (r + 1) * h + col[j])
+                  : zero;
+      dr[j] = (dres != nullptr && on[j])
+                  ? *reinterpret_cast<const uint4*>(dres + r * h + col[j])
+                  : zero;
+    }
     const float rs = rstd[r];
+    float d[NV * V], xv[NV * V];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      Vec<T>::from_raw(cd[j], d + j * V);
+      Vec<T>::from_raw(cx[j], xv + j * V);
+    }
     float dot = 0.0f;
 #pragma unroll
-    for (int j = 0; j < MAXC / V; ++j) {
-      const int64_t c = ((int64_t)threadIdx.x + 256 * j) * V;
-      if (c < h) {
-        float d[V], xv[V], g[V];
-        Vec<T>::load(dy + r * h + c, d);
-        Vec<T>::load(x + r * h + c, xv);
-        Vec<T>::load(gamma + c, g);
-#pragma unroll
-        for (int q = 0; q < V; ++q) {
-          dot += d[q] * g[q] * xv[q];
-          dgacc[j * V + q] += d[q] * xv[q] * rs;
-        }
-      }
+    for (int i = 0; i < NV * V; ++i) {
+      dot = fmaf(d[i] * g[i], xv[i], dot);
+      dgacc[i] = fmaf(d[i] * xv[i], rs, dgacc[i]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = dot;
+    if (lane == 0) red[r & 1][w] = dot;
     __syncthreads();
     float tot = 0.0f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w];
-    __syncthreads();
+    for (int i = 0; i < 16; ++i) tot += red[r & 1][i];
     const float coef = rs * rs * rs * tot / (float)h;
 #pragma unroll
-    for (int j = 0; j < MAXC / V; ++j) {
-      const int64_t c = ((int64_t)threadIdx.x + 256 * j) * V;
-      if (c < h) {
-        float d[V], xv[V], g[V], o[V];
-        Vec<T>::load(dy + r * h + c, d);
-        Vec<T>::load(x + r * h + c, xv);
-        Vec<T>::load(gamma + c, g);
-        if (dres != nullptr) {
-          Vec<T>::load(dres + r * h + c, o);
-        } else {
-#pragma unroll
-          for (int q = 0; q < V; ++q) o[q] = 0.0f;
-        }
-#pragma unroll
-        for (int q = 0; q < V; ++q) o[q] += rs * d[q] * g[q] - xv[q] * coef;
-        Vec<T>::store(dx + r * h + c, o);
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < MAXC / V; ++j) {
-    const int64_t c = ((int64_t)threadIdx.x + 256 * j) * V;
-    if (c < h) {
+    for (int j = 0; j < NV; ++j) {
+      if (!on[j]) continue;
+      float o[V];
+      Vec<T>::from_raw(dr[j], o);
 #pragma unroll
       for (int q = 0; q < V; ++q)
-        dg_partial[(int64_t)blockIdx.x * h + c + q] = dgacc[j * V + q];
+        o[q] += rs * d[j * V + q] * g[j * V + q] - xv[j * V + q] * coef;
+      Vec<T>::store(dx + r * h + col[j], o);
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      cd[j] = nd[j];
+      cx[j] = nx[j];
     }
   }
+#pragma unroll
+  for (int j = 0; j < NV; ++j)
+    if (on[j])
+      Vec<T>::store_f32(dg_partial + (int64_t)blockIdx.x * h + col[j],
+                        dgacc + j * V);
 }
 
 int grid_for(int64_t work_items, int per_block) {
@@ -359,7 +418,7 @@ int colsum(const void* X, int64_t rows, int64_t cols, int64_t ld, void* out,
                (double)sizeof(T) * rows * cols);
   colsum_stage1<T><<<g1, 256, 0, s>>>(static_cast<const T*>(X), rows, cols, ld,
                                       rpc, scratch);
-  colsum_stage2<T><<<grid_for(cols, 256), 256, 0, s>>>(scratch, chunks, cols,
+  colsum_stage2<T><<<(unsigned)((cols + 31) / 32), 256, 0, s>>>(scratch, chunks, cols,
                                                        static_cast<T*>(out));
   count_launch(2);
   return cudaGetLastError();
@@ -393,12 +452,14 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
                 float* scratch, int64_t rows, int64_t h, void* stream) {
   if (rows == 0) return cudaSuccess;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int chunks = rmsnorm_bwd_chunks(rows);
+  // at most one chunk per SM (the scratch holds rmsnorm_bwd_chunks rows)
+  const int chunks = (int)std::min<int64_t>(rmsnorm_bwd_chunks(rows),
+                                            device_sm_count());
   const int64_t rpc = (rows + chunks - 1) / chunks;
   constexpr int V = Vec<T>::N;
-  // columns per thread: 256 threads × V per sweep
-  const int64_t sweeps = (h + 256 * V - 1) / (256 * V);
-  if (sweeps > 8) return cudaErrorInvalidValue;
+  // 16-byte vectors per thread: 512 threads × V columns per sweep
+  const int64_t sweeps = (h + 512 * V - 1) / (512 * V);
+  if (sweeps > 4) return cudaErrorInvalidValue;
   ProfScope ps(stream, KF_NORM, 8.0 * rows * h,
                (double)sizeof(T) * rows * h * (dres != nullptr ? 4 : 3));
   const T* dyp = static_cast<const T*>(dy);
@@ -406,19 +467,16 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
   const T* gp = static_cast<const T*>(gamma);
   const T* rp = static_cast<const T*>(dres);
   T* dxp = static_cast<T*>(dx);
-  if (sweeps <= 2)
-    rmsnorm_bwd_kernel<T, 2 * V><<<chunks, 256, 0, s>>>(dyp, xp, gp, rstd, rp,
-                                                        dxp, scratch, rows, h,
-                                                        rpc);
-  else if (sweeps <= 4)
-    rmsnorm_bwd_kernel<T, 4 * V><<<chunks, 256, 0, s>>>(dyp, xp, gp, rstd, rp,
-                                                        dxp, scratch, rows, h,
-                                                        rpc);
+  if (sweeps <= 1)
+    rmsnorm_bwd_kernel<T, 1><<<chunks, 512, 0, s>>>(dyp, xp, gp, rstd, rp, dxp,
+                                                    scratch, rows, h, rpc);
+  else if (sweeps <= 2)
+    rmsnorm_bwd_kernel<T, 2><<<chunks, 512, 0, s>>>(dyp, xp, gp, rstd, rp, dxp,
+                                                    scratch, rows, h, rpc);
   else
-    rmsnorm_bwd_kernel<T, 8 * V><<<chunks, 256, 0, s>>>(dyp, xp, gp, rstd, rp,
-                                                        dxp, scratch, rows, h,
-                                                        rpc);
-  colsum_stage2<T><<<grid_for(h, 256), 256, 0, s>>>(scratch, chunks, h,
+    rmsnorm_bwd_kernel<T, 4><<<chunks, 512, 0, s>>>(dyp, xp, gp, rstd, rp, dxp,
+                                                    scratch, rows, h, rpc);
+  colsum_stage2<T><<<(unsigned)((h + 31) / 32), 256, 0, s>>>(scratch, chunks, h,
                                                     static_cast<T*>(dgamma));
   count_launch(2);
   return cudaGetLastError();
