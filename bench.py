@@ -20,6 +20,7 @@ workload.  `--impl reference` times that oracle alone (the reference arm).
 """
 
 import argparse
+import hashlib
 import json
 import os
 import subprocess
@@ -354,7 +355,43 @@ def reference_arm(args, cfg, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def roofline(prof, steps, peaks, peaks_src):
+# DRAM bytes per launch of the dominant kernel, from a committed ncu capture
+# of the same workload (profiles/): used only while the kernel's sources still
+# hash to the value recorded with the counters, else the traffic is unknown.
+TRAFFIC_PROFILES = {
+    ("gemm_tc", "layer_bf16"): (
+        "profiles/gemm_tc_traffic_layer_bf16_s8192.md",
+        ["megatron_tensor_transformer_gate_gb300/csrc/gemm_tc.cu",
+         "megatron_tensor_transformer_gate_gb300/csrc/gemm.h",
+         "megatron_tensor_transformer_gate_gb300/csrc/common.cuh"]),
+}
+
+
+def committed_traffic(kernel, workload):
+    entry = TRAFFIC_PROFILES.get((kernel, workload))
+    if entry is None:
+        return None, None
+    summary, sources = entry
+    root = os.path.dirname(os.path.abspath(__file__))
+    try:
+        fields = {}
+        for line in open(os.path.join(root, summary)):
+            if ":" in line and line.split(":")[0] in (
+                    "traffic_per_launch_bytes", "source_sha256"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        h = hashlib.sha256()
+        for f in sources:
+            with open(os.path.join(root, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None, None
+    if fields.get("source_sha256") != h.hexdigest():
+        return None, f"{summary} (stale: kernel sources changed since capture)"
+    return float(fields["traffic_per_launch_bytes"]), summary
+
+
+def roofline(prof, steps, peaks, peaks_src, workload=None):
     fams = {k: v for k, v in prof.items() if v["launches"]}
     total_ms = max(sum(v["ms"] for v in fams.values()), 1e-9)
     kernels = {}
@@ -373,9 +410,12 @@ def roofline(prof, steps, peaks, peaks_src):
         peak = float(peaks.get("bf16_tflops_sustained",
                                peaks.get("bf16_tflops")))
         ach = (v["flops"] / v["launches"]) / (per_ms / 1e3) / 1e12
+        traffic, tsrc = committed_traffic(dom, workload)
+        burst = float(peaks.get("bf16_tflops", peak))
         return {"bound": "tensor", "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
-                "kernel": dom,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
+                "traffic_source": tsrc, "kernel": dom,
+                "peak_burst": burst, "frac_burst": ach / burst,
                 "peak_source": f"{peaks_src} bf16_tflops_sustained",
                 "flops_per_launch": v["flops"] / v["launches"],
                 "ms_per_launch": per_ms}, kernels
@@ -487,7 +527,7 @@ def main():
                "ms_per_step": ems, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
-    roof, kernels = roofline(prof, args.steps, peaks, peaks_src)
+    roof, kernels = roofline(prof, args.steps, peaks, peaks_src, args.workload)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, 20260000)

@@ -1,0 +1,63 @@
+"""Host logic of bench.py that needs no GPU: the roofline record and the
+DRAM traffic taken from a committed ncu capture."""
+
+import hashlib
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _prof(ms_gemm=24.0, ms_attn=3.0):
+    return {
+        "gemm_tc": {"launches": 32, "ms": 2 * ms_gemm, "flops": 84e12,
+                    "bytes": 2.6e10},
+        "attn_bwd_dkdv": {"launches": 2, "ms": 2 * ms_attn, "flops": 3.3e12,
+                          "bytes": 6e8},
+        "rmsnorm": {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0},
+    }
+
+
+PEAKS = {"bf16_tflops": 1907.0, "bf16_tflops_sustained": 1714.4,
+         "hbm_gbs": 6796.9}
+
+
+def test_roofline_picks_the_dominant_family_and_divides_per_launch():
+    roof, kernels = bench.roofline(_prof(), 2, PEAKS, "measured")
+    assert roof["kernel"] == "gemm_tc" and roof["bound"] == "tensor"
+    per_launch_s = 24.0 * 2 / 32 / 1e3
+    assert abs(roof["achieved"] - 84e12 / 32 / per_launch_s / 1e12) < 1e-6
+    assert abs(roof["frac"] - roof["achieved"] / 1714.4) < 1e-12
+    assert abs(roof["frac_burst"] - roof["achieved"] / 1907.0) < 1e-12
+    assert "rmsnorm" not in kernels   # families without launches are dropped
+    assert abs(sum(k["share"] for k in kernels.values()) - 1.0) < 1e-12
+
+
+def test_traffic_only_for_a_captured_workload():
+    assert bench.committed_traffic("gemm_tc", "mlp_swiglu_bf16") == (None, None)
+    assert bench.committed_traffic("attn_fwd", "layer_bf16") == (None, None)
+
+
+def test_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    # a capture whose hash matches the sources gives its bytes; any change to
+    # a source file turns it into (None, "... stale ...")
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    digest = hashlib.sha256(b"kernel v1").hexdigest()
+    summ = tmp_path / "summary.md"
+    summ.write_text(f"traffic_per_launch_bytes: 1234\nsource_sha256: {digest}\n")
+    monkeypatch.setitem(bench.TRAFFIC_PROFILES, ("k", "w"),
+                        (str(summ), [str(src)]))
+    assert bench.committed_traffic("k", "w") == (1234.0, str(summ))
+    src.write_text("kernel v2")
+    traffic, note = bench.committed_traffic("k", "w")
+    assert traffic is None and "stale" in note
+
+
+def test_committed_gemm_capture_is_well_formed():
+    traffic, note = bench.committed_traffic("gemm_tc", "layer_bf16")
+    # either current (bytes per launch) or flagged stale, never an exception
+    assert (traffic is not None and traffic > 0) or "stale" in note
