@@ -214,8 +214,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, j = blockIdx.y;
-  const int q0 = (gridDim.x - 1 - blockIdx.x) * 128;
+  // 1-D grid, block rank slowest: the heaviest query blocks first
+  const int nblk = (a.s + 127) / 128;
+  const int per = gridDim.x / nblk;   // n_q · batch
+  const int rank = blockIdx.x / per, rem = blockIdx.x % per;
+  const int b = rem / a.nq, j = rem % a.nq;
+  const int q0 = (nblk - 1 - rank) * 128;
   const int kvh = j / (a.nq / a.nkv);
   const int kv_end = a.causal ? min(a.s, q0 + 128) : a.s;
   const int nkb = (kv_end + 127) / 128;
@@ -470,8 +474,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, kvh = blockIdx.y;
-  const int k0 = blockIdx.x * 128;
+  // 1-D grid, block rank slowest: the heaviest (first, under the causal
+  // mask) key blocks of every kv head start first; in (kv head, key block)
+  // order the last heads' heavy blocks would start late and set the tail
+  const int nblk = (a.s + 127) / 128;
+  const int per = gridDim.x / nblk;   // n_kv · batch
+  const int rank = blockIdx.x / per, rem = blockIdx.x % per;
+  const int b = rem / a.nkv, kvh = rem % a.nkv;
+  const int k0 = rank * 128;
   const int group = a.nq / a.nkv;
   const int nqb = (a.s + 127) / 128;
   const int qb_first = a.causal ? k0 / 128 : 0;
@@ -822,7 +832,7 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   a.status = status;
   a.out0 = static_cast<__nv_bfloat16*>(dQ);
   {
-    dim3 grid((unsigned)((sh.s + 127) / 128), (unsigned)sh.nq, (unsigned)sh.b);
+    const unsigned grid = (unsigned)(((sh.s + 127) / 128) * sh.nq * sh.b);
     ProfScope ps(stream, KF_ATTN_BWD_DQ, 0.5 * core,
                  io * (3.0 * sh.nq + 2.0 * sh.nkv));
     attn_bwd_dq_tc_kernel<<<grid, THREADS, dq::SMEM, s>>>(a);
@@ -830,8 +840,7 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   a.out0 = static_cast<__nv_bfloat16*>(dK);
   a.out1 = static_cast<__nv_bfloat16*>(dV);
   {
-    dim3 grid((unsigned)((sh.s + 127) / 128), (unsigned)sh.nkv,
-              (unsigned)sh.b);
+    const unsigned grid = (unsigned)(((sh.s + 127) / 128) * sh.nkv * sh.b);
     ProfScope ps(stream, KF_ATTN_BWD_DKDV, 1.5 * core,
                  io * (2.0 * sh.nq + 4.0 * sh.nkv));
     attn_bwd_dkdv_tc_kernel<<<grid, THREADS, dkv::SMEM, s>>>(a);

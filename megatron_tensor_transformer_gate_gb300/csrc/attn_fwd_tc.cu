@@ -131,8 +131,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, j = blockIdx.y;
-  const int q0 = (gridDim.x - 1 - blockIdx.x) * BLK;
+  // 1-D grid, block rank slowest: the heaviest (last, under the causal
+  // mask) query blocks of every head start first, which shortens the tail
+  const int nblk = (a.s + BLK - 1) / BLK;
+  const int per = gridDim.x / nblk;   // n_q · batch
+  const int rank = blockIdx.x / per, rem = blockIdx.x % per;
+  const int b = rem / a.nq, j = rem % a.nq;
+  const int q0 = (nblk - 1 - rank) * BLK;
   const int kvh = j / (a.nq / a.nkv);
   const int kv_end = a.causal ? min(a.s, q0 + BLK) : a.s;
   const int nkb = (kv_end + BLK - 1) / BLK;
@@ -455,8 +460,7 @@ int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   a.causal = sh.causal;
   a.scale_log2 = sh.scale * 1.4426950408889634f;
   a.status = status;
-  dim3 grid((unsigned)((sh.s + BLK - 1) / BLK), (unsigned)sh.nq,
-            (unsigned)sh.b);
+  const unsigned grid = (unsigned)(((sh.s + BLK - 1) / BLK) * sh.nq * sh.b);
   const double s = (double)sh.s;
   const double pairs = sh.causal ? s * (s + 1.0) / 2.0 : s * s;
   {
