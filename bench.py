@@ -482,7 +482,12 @@ def main():
     prof = B.profile_read()
     B.profile_enable(0)
     B.device_status()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    step_times = sorted(a.elapsed_time(b) for a, b in ev)
+    ms = sum(step_times) / args.steps
+    step_stats = {"p50": step_times[(len(step_times) - 1) // 2],
+                  "p95": step_times[min(len(step_times) - 1,
+                                        int(0.95 * len(step_times)))],
+                  "min": step_times[0], "max": step_times[-1]}
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -542,7 +547,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": warmup,
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": ms, "step_ms": step_stats,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": conf,
             "pct_of_bf16_peak": 100.0 * value / world / burst,
