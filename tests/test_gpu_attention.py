@@ -71,3 +71,11 @@ def test_fp16_overflow_is_reported(tp):
         tp.device_status()
     assert e.value.code == 9
     tp.device_status()          # the word was cleared by the read
+
+
+def test_gqa_layer_widths(tp):
+    # the attention block of the layer workload (h 8192, 64 q / 8 kv heads,
+    # n 8) at s = 512 on its own seeded inputs, both bounds
+    cfg = I.workload("attn_gqa_bf16", b=1, s=512, h=8192, n_q=64, n_kv=8,
+                     n=8)
+    run_case(tp, cfg, 0, 20260005)

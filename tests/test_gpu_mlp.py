@@ -134,3 +134,11 @@ def test_fused_and_materialised_agree(tp):
     b, ob, _ = run_case(tp, cfg, 1, 5)
     # same inputs: the two reduction modes differ only by rounding order
     assert np.abs(f64(oa) - f64(ob)).max() <= 0.05 * np.abs(f64(oa)).max()
+
+
+def test_bf16_swiglu_layer_widths(tp):
+    # the MLP block of the layer workload (h 8192, h_ffn 28672, n 8, weights
+    # std 0.02, residual) at T = 512 on its own seeded inputs, both bounds
+    cfg = I.workload("mlp_swiglu_bf16", b=1, s=512, h=8192, h_ffn=28672,
+                     n=8, w_std=0.02, residual="X")
+    run_case(tp, cfg, 0, 20260005)

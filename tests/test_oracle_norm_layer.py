@@ -77,3 +77,41 @@ def test_layer_backward_finite_differences():
     assert_grad(g["dX"], loss, x)
     for k in ("g1", "Wq", "Wk", "Wv", "Wo", "g2", "W1", "W2"):
         assert_grad(g["d" + k], loss, P[k], max_entries=24)
+
+
+def test_sampled_layer_with_sparse_upstream_matches_dense_oracle():
+    # oracle.sampled.layer_sparse_upstream restates the layer for the
+    # full-size GPU check; on small shapes (two sequences, GQA groups of 2,
+    # rows in both sequences, a row at a sequence start) it must equal the
+    # dense layer oracle given the same sparse upstream gradient
+    rng = np.random.default_rng(11)
+    b, s, h, nq, nkv, d, f = 2, 24, 64, 4, 2, 16, 96
+    T = b * s
+    P = {"g1": 1 + 0.1 * rng.standard_normal(h),
+         "g2": 1 + 0.1 * rng.standard_normal(h),
+         "Wq": 0.2 * rng.standard_normal((nq * d, h)),
+         "Wk": 0.2 * rng.standard_normal((nkv * d, h)),
+         "Wv": 0.2 * rng.standard_normal((nkv * d, h)),
+         "Wo": 0.2 * rng.standard_normal((h, nq * d)),
+         "W1": 0.2 * rng.standard_normal((2 * f, h)),
+         "W2": 0.2 * rng.standard_normal((h, f))}
+    x = rng.standard_normal((T, h))
+    rows = [47, 30, 24, 23, 5]
+    dOut = np.zeros((T, h))
+    dOut[rows] = rng.standard_normal((len(rows), h))
+    kw = dict(b=b, s=s, n_q=nq, n_kv=nkv, d=d)
+    fo = oracle.layer_forward(x, P, **kw)
+    go = oracle.layer_backward(dOut, x, P, fo, **kw)
+    sm = oracle.sampled.layer_sparse_upstream(x, P, rows, dOut[rows],
+                                              [0, 23, 24, 40], **kw)
+
+    def rel(a, ref):
+        return np.abs(a - ref).max() / np.abs(ref).max()
+
+    for t in (0, 23, 24, 40):
+        assert rel(sm["Out"][t], fo["Out"][t]) < 1e-12
+    for k in ("dX", "dg1", "dg2", "dWk", "dWv"):
+        assert rel(sm[k], go[k]) < 1e-12, k
+    for k in ("dWq", "dWo", "dW1", "dW2"):
+        L, R = sm[k]
+        assert rel(L.T @ R, go[k]) < 1e-12, k
