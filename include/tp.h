@@ -224,10 +224,58 @@ typedef struct {
   uint64_t total_payload;               /* (fwd+bwd)·P */
   uint64_t total_ring_num;              /* (fwd+bwd)·ring, over ring_bytes_den */
   uint64_t total_page2;                 /* (fwd+bwd)·2·P */
+  /* Megatron-SP ([Troverld] §III.III): each all-reduce position becomes a
+   * reduce-scatter to (b, s/n, H) at a block's end and an all-gather back to
+   * (b, s, H) at the next block's start (in backward the conjugates).  Per
+   * rank in a ring each moves (n−1)·P/n, kept as the reduced fraction
+   * num/sp_bytes_den; rs + ag equals the ring all-reduce.  Counts per
+   * microbatch, forward + backward. */
+  uint64_t sp_rs_bytes_num, sp_ag_bytes_num, sp_bytes_den;
+  uint64_t sp_reduce_scatters, sp_all_gathers;
+  uint64_t sp_total_num;                /* over sp_bytes_den */
 } tp_comm_report;
 
 tp_status tp_comm_bytes(int32_t scope, int64_t T, int64_t h, int32_t n,
                         int32_t dtype, tp_comm_report* out);
+
+/* Saved activations per rank ([hjcheng-TP] MLP and Attention: the tensors
+ * each block keeps for its backward, single card and TP; TP divides the
+ * column- / head-sharded ones by n, the block input stays whole).
+ *
+ * Element counts per rank (T = b·s, f = h_ffn, q = n_q/n, k = n_kv/n):
+ *   MLP:   x T·h; hidden H (GeLU) T·f/n or G and U (SwiGLU) 2·T·f/n;
+ *          activation A T·f/n; dropout mask T·h (if dropout)
+ *   attention: x T·h; Q T·q·d; K and V T·k·d each; the page's score matrix
+ *          S b·q·s² (unfused) or the log-sum-exp b·q·s (flash); AV T·q·d
+ *   layer (pre-norm, flash): both blocks plus each RMSNorm's input T·h and
+ *          rstd T, and the dropout masks after the two reductions.
+ * Megatron-SP ([Troverld] §III.III): the token-wise region (norm input and
+ * rstd, dropout masks) holds s/n positions per rank, rounded up; the block
+ * inputs stay whole.
+ * Bytes: activations δ (2 bf16 / 4 fp32), masks 1 byte, S δ, LSE and rstd
+ * 4.  The flash attention figure is what this library's attention
+ * workspace holds (Q, K, V in fp16 as δ = 2, O, LSE) plus x. */
+typedef struct {
+  int64_t b, s, h, h_ffn;
+  int32_t n_q, n_kv, d, n;
+  int32_t dtype;          /* TP_F32 | TP_BF16 */
+  int32_t act;            /* TP_GELU | TP_SWIGLU */
+  int32_t dropout;        /* 1: a mask after each block's reduction */
+  int32_t seq_parallel;   /* 1: Megatron-SP token-wise region */
+} tp_act_desc;
+typedef struct {
+  uint64_t mlp_x, mlp_hidden, mlp_act, mlp_mask;                  /* elements */
+  uint64_t attn_x, attn_q, attn_kv, attn_scores, attn_lse, attn_o; /* elements */
+  uint64_t norm_x, norm_rstd;                                      /* per norm */
+  uint64_t mlp_bytes;          /* MLP block */
+  uint64_t attn_bytes_pages;   /* attention with the score matrix S */
+  uint64_t attn_bytes_flash;   /* attention with LSE instead of S */
+  uint64_t layer_bytes_flash;  /* pre-norm layer: norms + flash attn + MLP */
+} tp_act_report;
+
+/* TP_ERR_NULL, TP_ERR_SHAPE (negative sizes, n < 1, n∤n_q, n∤n_kv, n∤h_ffn),
+ * TP_ERR_DTYPE (dtype / act). */
+tp_status tp_act_memory(const tp_act_desc* d, tp_act_report* out);
 
 /* Algorithmic FLOPs ([hjcheng-TP] 单卡forward/backward tables): GeLU MLP
  * 4·T·h·f forward, SwiGLU 6·T·h·f; attention projections

@@ -49,7 +49,25 @@ class CommReport(ctypes.Structure):
     _fields_ = [(k, ctypes.c_uint64) for k in (
         "reductions_fwd", "reductions_bwd", "payload_bytes", "ring_bytes_num",
         "ring_bytes_den", "page2_bytes", "total_payload", "total_ring_num",
-        "total_page2")]
+        "total_page2", "sp_rs_bytes_num", "sp_ag_bytes_num", "sp_bytes_den",
+        "sp_reduce_scatters", "sp_all_gathers", "sp_total_num")]
+
+
+class ActDesc(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("s", ctypes.c_int64),
+                ("h", ctypes.c_int64), ("h_ffn", ctypes.c_int64),
+                ("n_q", ctypes.c_int32), ("n_kv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("n", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
+                ("dropout", ctypes.c_int32), ("seq_parallel", ctypes.c_int32)]
+
+
+class ActReport(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_uint64) for k in (
+        "mlp_x", "mlp_hidden", "mlp_act", "mlp_mask", "attn_x", "attn_q",
+        "attn_kv", "attn_scores", "attn_lse", "attn_o", "norm_x", "norm_rstd",
+        "mlp_bytes", "attn_bytes_pages", "attn_bytes_flash",
+        "layer_bytes_flash")]
 
 
 class ProfileEntry(ctypes.Structure):
@@ -87,6 +105,8 @@ SIGNATURES = {
                                       _P, _P, _P, _P]),
     "tp_comm_bytes": (_I32, [_I32, _I64, _I64, _I32, _I32,
                              ctypes.POINTER(CommReport)]),
+    "tp_act_memory": (_I32, [ctypes.POINTER(ActDesc),
+                             ctypes.POINTER(ActReport)]),
     "tp_mlp_flops": (_I32, [_MP, _U64P, _U64P]),
     "tp_attn_flops": (_I32, [_AP, _U64P, _U64P]),
     "tp_gemm": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _I32, _P, _I64, _I32,
@@ -153,6 +173,17 @@ def comm_bytes(scope, T, h, n, dtype):
     check(lib().tp_comm_bytes(scope, T, h, n, dtype, ctypes.byref(r)),
           "tp_comm_bytes")
     return {k: getattr(r, k) for k, _ in CommReport._fields_}
+
+
+def act_memory(b, s, h, h_ffn, n_q, n_kv, d, n, dtype=BF16, act=SWIGLU,
+               dropout=False, seq_parallel=False):
+    """Saved activations per rank (elements by tensor, bytes by block)."""
+    r = ActReport()
+    desc = ActDesc(b, s, h, h_ffn, n_q, n_kv, d, n, dtype, act, int(dropout),
+                   int(seq_parallel))
+    check(lib().tp_act_memory(ctypes.byref(desc), ctypes.byref(r)),
+          "tp_act_memory")
+    return {k: getattr(r, k) for k, _ in ActReport._fields_}
 
 
 def mlp_flops(desc):

@@ -38,7 +38,8 @@ from .attention import (attention_forward, attention_backward,
                         attention_forward_sharded, attention_backward_sharded)
 from .norm import rmsnorm_forward, rmsnorm_backward
 from .layer import layer_forward, layer_backward
-from .accounting import comm_report, mlp_flops, attn_flops, layer_flops
+from .accounting import (comm_report, mlp_flops, attn_flops, layer_flops,
+                         act_memory)
 from . import sampled
 
 __all__ = [
@@ -48,5 +49,5 @@ __all__ = [
     "attention_forward", "attention_backward", "attention_forward_sharded",
     "attention_backward_sharded", "rmsnorm_forward", "rmsnorm_backward",
     "layer_forward", "layer_backward", "comm_report", "mlp_flops",
-    "attn_flops", "layer_flops", "sampled",
+    "attn_flops", "layer_flops", "act_memory", "sampled",
 ]

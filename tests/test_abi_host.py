@@ -50,6 +50,12 @@ def test_comm_bytes_bit_exact(tp, scope, T, h, n, dt):
     assert r["total_payload"] == o["total_payload"]
     assert Fraction(r["total_ring_num"], r["ring_bytes_den"]) == o["total_ring"]
     assert r["total_page2"] == o["total_page2"]
+    sp = Fraction(r["sp_rs_bytes_num"], r["sp_bytes_den"])
+    assert sp == o["sp_rs_bytes"]
+    assert Fraction(r["sp_ag_bytes_num"], r["sp_bytes_den"]) == o["sp_ag_bytes"]
+    assert r["sp_reduce_scatters"] == o["sp_reduce_scatters"]
+    assert r["sp_all_gathers"] == o["sp_all_gathers"]
+    assert Fraction(r["sp_total_num"], r["sp_bytes_den"]) == o["sp_total"]
 
 
 def test_comm_bytes_named_workloads(tp):
@@ -135,3 +141,51 @@ def test_status_strings(tp):
     L = tp.lib()
     for code in range(10):
         assert L.tp_status_string(code) != b"unknown status"
+
+
+ACT_CONFIGS = [  # b, s, h, h_ffn, n_q, n_kv, d, n, dtype, act
+    (1, 64, 128, 512, 2, 2, 64, 2, "f32", "gelu"),
+    (4, 1024, 1024, 4096, 8, 8, 128, 4, "bf16", "gelu"),
+    (2, 4096, 4096, 11008, 32, 8, 128, 8, "bf16", "swiglu"),
+    (2, 2048, 4096, 11008, 32, 8, 128, 4, "bf16", "swiglu"),
+    (1, 8192, 8192, 28672, 64, 8, 128, 8, "bf16", "swiglu"),
+    (3, 37, 96, 384, 6, 3, 16, 3, "f32", "swiglu"),   # s not a multiple of n
+]
+
+
+@pytest.mark.parametrize("cfg", ACT_CONFIGS)
+@pytest.mark.parametrize("dropout", [False, True])
+@pytest.mark.parametrize("sp", [False, True])
+def test_act_memory_bit_exact(tp, cfg, dropout, sp):
+    b, s, h, f, nq, nkv, d, n, dt, act = cfg
+    r = tp.act_memory(b, s, h, f, nq, nkv, d, n,
+                      dtype={"f32": tp.F32, "bf16": tp.BF16}[dt],
+                      act={"gelu": tp.GELU, "swiglu": tp.SWIGLU}[act],
+                      dropout=dropout, seq_parallel=sp)
+    o = oracle.act_memory(b, s, h, f, nq, nkv, d, n, dtype=dt, act=act,
+                          dropout=dropout, seq_parallel=sp)
+    assert r == o
+
+
+def test_act_memory_matches_this_librarys_workspaces(tp):
+    # the flash attention and MLP figures (all n ranks, without the block
+    # input x and the masks) are what the library's fused-mode workspaces
+    # hold, up to the 256-byte alignment of each region
+    b, s, h, f, nq, nkv, d, n = 1, 8192, 8192, 28672, 64, 8, 128, 8
+    r = tp.act_memory(b, s, h, f, nq, nkv, d, n)
+    attn = n * ((r["attn_q"] + r["attn_kv"] + r["attn_o"]) * 2
+                + r["attn_lse"] * 4)
+    ws = tp.attn_workspace_bytes(tp.attn_desc(b, s, h, nq, nkv, d, n))
+    assert 0 <= ws - attn < 5 * 256
+    mlp = n * (r["mlp_hidden"] + r["mlp_act"]) * 2
+    ws = tp.mlp_workspace_bytes(tp.mlp_desc(b * s, h, f, n, act=tp.SWIGLU))
+    assert 0 <= ws - mlp < 3 * 256
+
+
+def test_act_memory_rejects(tp):
+    with pytest.raises(tp.TPError) as e:
+        tp.act_memory(1, 64, 128, 512, 3, 3, 64, 2)     # n ∤ n_q
+    assert e.value.code == 2
+    with pytest.raises(tp.TPError) as e:
+        tp.act_memory(1, 64, 128, 512, 2, 2, 64, 2, dtype=7)
+    assert e.value.code == 3
