@@ -63,7 +63,9 @@ typedef enum {
   TP_ERR_RANGE = 9            /* an fp16 attention operand overflowed */
 } tp_status;
 
-typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;            /* δ = 4 or 2 */
+/* TP_FP8 (E4M3, δ = 1): an FP8 payload in the accountants; for the MLP it
+ * selects forward GEMMs on per-tensor scaled E4M3 operands (bf16 storage). */
+typedef enum { TP_F32 = 0, TP_BF16 = 1, TP_FP8 = 2 } tp_dtype;  /* δ = 4, 2, 1 */
 typedef enum { TP_GELU = 0, TP_SWIGLU = 1 } tp_act;
 typedef enum { TP_REDUCE_FUSED = 0, TP_REDUCE_MATERIALISED = 1 } tp_reduce_mode;
 typedef enum { TP_SCOPE_MLP = 0, TP_SCOPE_ATTN = 1, TP_SCOPE_LAYER = 2 } tp_scope;

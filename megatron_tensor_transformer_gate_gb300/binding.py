@@ -13,7 +13,7 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libtp.so")
 
-F32, BF16 = 0, 1
+F32, BF16, FP8 = 0, 1, 2
 GELU, SWIGLU = 0, 1
 FUSED, MATERIALISED = 0, 1
 SCOPE_MLP, SCOPE_ATTN, SCOPE_LAYER = 0, 1, 2

@@ -5,7 +5,8 @@
 //    in backward (f on the input gradient) per MLP or attention block; four
 //    per layer ([Grasp-TP] §5 list; [adu-TP] 张量并行的通信开销);
 //  * each reduction's logical payload P = T·h·δ bytes ([Grasp-TP] §5,
-//    δ from [Troverld] §O.I: FP32 4, BF16 2);
+//    δ from [Troverld] §O.I: FP32 4, BF16 2; FP8 1 for the FP8 buffers of
+//    [Grasp-TP] §6);
 //  * a ring all-reduce moves 2(n−1)·P/n per rank ([Grasp-TP] §5), returned
 //    as an exact reduced fraction; [Troverld] §II.II counts 2·P.
 // Megatron-SP ([Troverld] §III.III): each all-reduce position splits into a
@@ -41,6 +42,7 @@ extern "C" tp_status tp_comm_bytes(int32_t scope, int64_t T, int64_t h,
   switch (dtype) {
     case TP_F32: delta = 4; break;
     case TP_BF16: delta = 2; break;
+    case TP_FP8: delta = 1; break;
     default: return TP_ERR_DTYPE;
   }
   uint64_t fwd, bwd;
@@ -91,6 +93,7 @@ extern "C" tp_status tp_act_memory(const tp_act_desc* d, tp_act_report* out) {
   switch (d->dtype) {
     case TP_F32: delta = 4; break;
     case TP_BF16: delta = 2; break;
+    case TP_FP8: delta = 1; break;
     default: return TP_ERR_DTYPE;
   }
   if (d->act != TP_GELU && d->act != TP_SWIGLU) return TP_ERR_DTYPE;

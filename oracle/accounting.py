@@ -44,7 +44,7 @@ FLOPs ([hjcheng-TP] MLP / Attention 单卡forward, 单卡backward, TP forward):
 
 from fractions import Fraction
 
-DTYPE_BYTES = {"f32": 4, "bf16": 2}
+DTYPE_BYTES = {"f32": 4, "bf16": 2, "fp8": 1}   # fp8: [Grasp-TP] §6 buffers
 _REDUCTIONS = {"mlp": (1, 1), "attn": (1, 1), "layer": (2, 2)}
 
 

@@ -33,14 +33,15 @@ WORKLOADS = [  # scope, T, h, n, dtype
     ("mlp", 64, 128, 2, "f32"), ("mlp", 4096, 1024, 4, "bf16"),
     ("mlp", 8192, 4096, 8, "bf16"), ("attn", 4096, 4096, 4, "bf16"),
     ("layer", 8192, 8192, 8, "bf16"), ("layer", 3, 40, 5, "f32"),
-    ("mlp", 1, 8, 1, "bf16"),
+    ("mlp", 1, 8, 1, "bf16"), ("layer", 8192, 8192, 8, "fp8"),
+    ("attn", 7, 9, 2, "fp8"),
 ]
 
 
 @pytest.mark.parametrize("scope,T,h,n,dt", WORKLOADS)
 def test_comm_bytes_bit_exact(tp, scope, T, h, n, dt):
     r = tp.comm_bytes({"mlp": 0, "attn": 1, "layer": 2}[scope], T, h, n,
-                      {"f32": tp.F32, "bf16": tp.BF16}[dt])
+                      {"f32": tp.F32, "bf16": tp.BF16, "fp8": tp.FP8}[dt])
     o = oracle.comm_report(scope, T, h, n, dt)
     assert r["reductions_fwd"] == o["reductions_fwd"]
     assert r["reductions_bwd"] == o["reductions_bwd"]

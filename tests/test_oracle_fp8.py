@@ -1,0 +1,89 @@
+"""Pins of the FP8 oracle (oracle/fp8.py): the E4M3 format from its
+definition, round-to-nearest-even with saturation, and the per-tensor scaled
+quantization and GEMM."""
+
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import fp8
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "e4m3_values.txt")
+
+
+def golden():
+    out = []
+    for line in open(GOLDEN):
+        line = line.split("#")[0].strip()
+        if line:
+            c, v = line.split()
+            out.append((int(c, 16), float(v)))
+    return out
+
+
+def test_decode_matches_the_format_table():
+    for code, value in golden():
+        got = fp8.e4m3_value(code)
+        if math.isnan(value):
+            assert math.isnan(got)
+        else:
+            assert got == value and math.copysign(1, got) == math.copysign(1, value)
+
+
+def test_finite_codes_are_monotone_and_round_trip():
+    pos = [fp8.e4m3_value(c) for c in range(0x7F)]
+    assert all(b > a for a, b in zip(pos, pos[1:]))
+    assert pos[-1] == 448.0 and pos[1] == 2.0 ** -9
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F])
+    vals = fp8.e4m3_decode(codes)
+    back = fp8.e4m3_encode(vals)
+    # -0 encodes to +0; every other finite code is its own encoding
+    ok = (back == codes) | ((codes == 0x80) & (back == 0x00))
+    assert ok.all()
+
+
+def test_round_to_nearest_even_and_saturation():
+    # halfway between 1.0 (0x38, even) and 1.125 (0x39): the even code
+    assert fp8.e4m3_encode([1.0625])[0] == 0x38
+    # halfway between 1.125 (0x39) and 1.25 (0x3a): 0x3a
+    assert fp8.e4m3_encode([1.1875])[0] == 0x3A
+    # just above a halfway point rounds up; just below rounds down
+    assert fp8.e4m3_encode([1.0626])[0] == 0x39
+    assert fp8.e4m3_encode([1.0624])[0] == 0x38
+    # subnormal range: 2^-10 is halfway between 0 and 2^-9 → 0 (even)
+    assert fp8.e4m3_encode([2.0 ** -10])[0] == 0x00
+    assert fp8.e4m3_encode([3 * 2.0 ** -10])[0] == 0x02
+    # beyond the largest finite value: saturate to ±448
+    assert fp8.e4m3_encode([1000.0])[0] == 0x7E
+    assert fp8.e4m3_encode([-465.0])[0] == 0xFE
+    assert fp8.e4m3_encode([-1.0])[0] == 0xB8
+
+
+def test_quantize_scale_and_codes():
+    x = np.array([[0.5, -2.0], [1.0, 0.25]], dtype=np.float32)
+    q, s, amax = fp8.quantize(x)
+    assert amax == np.float32(2.0)
+    assert s == np.float32(224.0)                 # 448 / 2
+    # 0.5·224 = 112 = 1.75·2^6 → 0x6e; −2·224 = −448 → 0xfe;
+    # 224 = 1.75·2^7 → 0x76; 0.25·224 = 56 = 1.75·2^5 → 0x66
+    assert q.tolist() == [[0x6E, 0xFE], [0x76, 0x66]]
+    q0, s0, a0 = fp8.quantize(np.zeros((2, 3), dtype=np.float32))
+    assert a0 == 0 and s0 == 1 and (q0 == 0).all()
+
+
+def test_gemm_of_quantized_operands():
+    # exactly representable operands: the quantized GEMM is the plain GEMM
+    rng = np.random.default_rng(3)
+    A = rng.integers(-7, 8, size=(5, 16)).astype(np.float32) / 4
+    B = rng.integers(-7, 8, size=(3, 16)).astype(np.float32) / 4
+    qa, sa, _ = fp8.quantize(A)
+    qb, sb, _ = fp8.quantize(B)
+    C = fp8.gemm(qa, sa, qb, sb)
+    err = np.abs(C - A.astype(np.float64) @ B.T.astype(np.float64)).max()
+    # each operand is within one E4M3 rounding (≤ 2^-4 relative) of its value
+    assert err <= 0.15 * np.abs(A).max() * np.abs(B).max() * 16
+    # and dequantize(quantize(x)) stays within half an E4M3 step of x
+    d = fp8.dequantize(qa, sa)
+    assert (np.abs(d - A) <= np.abs(A) * 2.0 ** -4 + 2.0 ** -10).all()
