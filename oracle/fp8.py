@@ -20,8 +20,9 @@ The plainest reading, taken here:
 
 Pins (tests/test_oracle_fp8.py): decoding all 254 finite codes gives the
 format's values (the table written from the definition above, and
-monotone); every finite value encodes to its own code; halfway points go to
-the even code; saturation; scale and amax on small hand-worked tensors.
+monotone); every finite value (−0 included) encodes to its own code; halfway
+points go to the even code; tiny negatives keep their sign; saturation;
+scale and amax on small hand-worked tensors.
 """
 
 import numpy as np
@@ -58,7 +59,8 @@ def e4m3_decode(codes):
 
 def e4m3_encode(x):
     """Round-to-nearest-even E4M3 codes (uint8) of float values, saturating
-    finite values beyond ±448 to ±448.  Input must be finite."""
+    finite values beyond ±448 to ±448; negative values that round to zero
+    give −0 (0x80).  Input must be finite."""
     x = np.asarray(x, dtype=np.float64)
     a = np.minimum(np.abs(x), E4M3_MAX)
     # the neighbours below and above |x| among the non-negative values
@@ -72,7 +74,9 @@ def e4m3_encode(x):
     pick_hi = (dhi < dlo) | ((dhi == dlo) & ((_POS_CODES[hi] & 1) == 0))
     mag = np.where(exact, _POS_CODES[hi],
                    np.where(pick_hi, _POS_CODES[hi], _POS_CODES[lo]))
-    sign = np.where(np.signbit(x) & (mag != 0), 0x80, 0)
+    # the sign is kept when the magnitude rounds to 0: S.0000.000 with S = 1
+    # is −0, as rounding keeps the sign of the value rounded
+    sign = np.where(np.signbit(x), 0x80, 0)
     return (mag | sign).astype(np.uint8)
 
 
@@ -97,3 +101,33 @@ def gemm(qa, sa, qb, sb):
     """C = (decode(qa)·decode(qb)ᵀ) / (sa·sb) in float64; qa [M, K], qb [N, K]."""
     return (e4m3_decode(qa) @ e4m3_decode(qb).T) / (np.float64(sa) *
                                                    np.float64(sb))
+
+
+def round_bf16(x):
+    """x rounded to fp32, then to bf16 (the top 16 bits of the fp32 pattern,
+    round to nearest even), returned as float64; finite inputs."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def mlp_forward(X, W1, W2, *, act="swiglu", b1=None, b2=None, R=None, p=0.0,
+                seed=0):
+    """The MLP forward on the FP8 path: the first projection on quantized X
+    and W1 (W1 as one tensor, gate and up rows together), bias and
+    activation in fp64, A stored in bf16 then quantized, the second
+    projection on quantized A and W2, bias, dropout, residual.  Returns the
+    dict of ``oracle.mlp_forward`` (saved G/U/A or H/A in fp64, Z, Out) plus
+    the four scales."""
+    from .mlp import _activation, _output
+    qx, sx, _ = quantize(X)
+    qw1, sw1, _ = quantize(W1)
+    saved = _activation(dequantize(qx, sx), dequantize(qw1, sw1), b1, act)
+    qa, sa, _ = quantize(round_bf16(saved["A"]))
+    qw2, sw2, _ = quantize(W2)
+    Z = dequantize(qa, sa) @ dequantize(qw2, sw2).T
+    out = dict(saved)
+    out["Z"] = Z
+    out["Out"] = _output(Z, b2, R, p, seed)
+    out["scales"] = (sx, sw1, sa, sw2)
+    return out

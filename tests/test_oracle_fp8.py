@@ -39,9 +39,7 @@ def test_finite_codes_are_monotone_and_round_trip():
     codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F])
     vals = fp8.e4m3_decode(codes)
     back = fp8.e4m3_encode(vals)
-    # -0 encodes to +0; every other finite code is its own encoding
-    ok = (back == codes) | ((codes == 0x80) & (back == 0x00))
-    assert ok.all()
+    assert (back == codes).all()      # −0 included: it keeps its sign
 
 
 def test_round_to_nearest_even_and_saturation():
@@ -59,6 +57,9 @@ def test_round_to_nearest_even_and_saturation():
     assert fp8.e4m3_encode([1000.0])[0] == 0x7E
     assert fp8.e4m3_encode([-465.0])[0] == 0xFE
     assert fp8.e4m3_encode([-1.0])[0] == 0xB8
+    # a negative value that rounds to zero keeps its sign: −0
+    assert fp8.e4m3_encode([-1e-9])[0] == 0x80
+    assert fp8.e4m3_encode([1e-9])[0] == 0x00
 
 
 def test_quantize_scale_and_codes():
@@ -87,3 +88,32 @@ def test_gemm_of_quantized_operands():
     # and dequantize(quantize(x)) stays within half an E4M3 step of x
     d = fp8.dequantize(qa, sa)
     assert (np.abs(d - A) <= np.abs(A) * 2.0 ** -4 + 2.0 ** -10).all()
+
+
+def test_round_bf16_is_round_to_nearest_even():
+    # 1 + 2^-8 is halfway between bf16 neighbours 1 and 1 + 2^-7: even → 1
+    assert fp8.round_bf16([1.0 + 2.0 ** -8])[0] == 1.0
+    assert fp8.round_bf16([1.0 + 3 * 2.0 ** -8])[0] == 1.0 + 2.0 ** -6
+    assert fp8.round_bf16([1.0 + 2.0 ** -8 + 2.0 ** -20])[0] == 1.0 + 2.0 ** -7
+    assert fp8.round_bf16([-3.0])[0] == -3.0
+
+
+def test_fp8_mlp_forward_is_the_mlp_on_dequantized_operands():
+    # with operands already exact in E4M3 (after scaling) and a bf16-exact A,
+    # the FP8 path equals the plain MLP on the dequantized tensors
+    import oracle
+    rng = np.random.default_rng(5)
+    X = rng.integers(-8, 9, size=(6, 32)) / 8.0
+    W1 = rng.integers(-8, 9, size=(2 * 16, 32)) / 64.0
+    W2 = rng.integers(-8, 9, size=(32, 16)) / 64.0
+    o = fp8.mlp_forward(X, W1, W2, act="swiglu")
+    sx, sw1, sa, sw2 = o["scales"]
+    ref = oracle.mlp_forward(fp8.dequantize(fp8.quantize(X)[0], sx),
+                             fp8.dequantize(fp8.quantize(W1)[0], sw1), W2,
+                             act="swiglu")
+    assert np.allclose(o["G"], ref["G"], rtol=0, atol=1e-12)
+    assert np.allclose(o["U"], ref["U"], rtol=0, atol=1e-12)
+    # the second projection uses A rounded to bf16, then quantized: within
+    # one E4M3 step of A (relative 2^-4) per element
+    d = np.abs(o["Z"] - ref["Z"]).max()
+    assert d <= 2.0 ** -3 * np.abs(ref["A"]).sum(axis=1).max() * np.abs(W2).max()
