@@ -92,17 +92,24 @@ typedef struct {
   int64_t h;          /* hidden size */
   int64_t h_ffn;      /* MLP intermediate size f */
   int32_t n;          /* TP degree: number of logical shards (n | h_ffn) */
-  int32_t dtype;      /* tp_dtype */
+  int32_t dtype;      /* tp_dtype (TP_FP8: see below) */
   int32_t act;        /* tp_act */
   int32_t mode;       /* tp_reduce_mode for the g and f reductions */
   float dropout_p;    /* in [0, 1) */
   uint64_t seed;      /* dropout stream seed */
 } tp_mlp_desc;
+/* dtype TP_FP8: tensors are stored in bf16 as for TP_BF16, and the two
+ * forward GEMMs run the FP8 fused kernel (tp_quantize_fp8 of X, W1, A, W2;
+ * E4M3 GEMMs dequantized in the epilogue, whose bias, activation, dropout
+ * and residual steps are unchanged); the backward is the bf16 backward on
+ * the saved bf16 activations.  Needs h and h_ffn/n multiples of 16. */
 
 /* Bytes of `ws` for tp_mlp_fwd/tp_mlp_bwd: saved activations (H and A for
  * GeLU; G, U and A for SwiGLU; each [T, h_ffn] in dtype) followed by the
- * forward scratch (n partial [T, h] tensors in materialised mode).  Every
- * region starts at the next 256-byte boundary, in the order listed. */
+ * forward scratch (n partial [T, h] tensors in materialised mode; for
+ * TP_FP8 also the E4M3 copies of X [T, h], W1, A [T, h_ffn] and W2 and 16
+ * bytes of scales).  Every region starts at the next 256-byte boundary, in
+ * the order listed. */
 size_t tp_mlp_workspace_bytes(const tp_mlp_desc* d);
 /* Bytes of `scratch` for tp_mlp_bwd: dZ [T, h] (when p > 0), the
  * activation-input gradient ([T, h_ffn] or [T, 2·h_ffn]), partial input
@@ -298,6 +305,28 @@ tp_status tp_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K,
                   int64_t ldc, tp_stream stream);
 
 
+/* ------------------------------------------------------------------ FP8 --
+ * The quantize and compute steps of the FP8 fused kernel ([Troverld]
+ * §II.III: quantize + compute + dequantize), per-tensor scaled E4M3:
+ *   amax = max |x|, scale = 448 / amax in fp32 (1 when amax = 0),
+ *   q = E4M3 code of fp32(x·scale), round to nearest even, saturating at ±448.
+ * tp_quantize_fp8: x is n bf16 values (16-byte aligned, n a multiple of 8);
+ * writes q (n bytes, 16-byte aligned) and *scale_out (one device float);
+ * amax_work is one device word of scratch.  All pointers device memory
+ * owned by the caller.  TP_ERR_NULL, TP_ERR_ARG (alignment), TP_ERR_SHAPE.
+ * tp_gemm_fp8: C[M, N] (bf16, row-major, ldc) =
+ *   Σ_k qa[m, k]·qb[n, k] / (scale_a·scale_b) on the tensor cores
+ * (kind::f8f6f4, fp32 accumulate); qa [M, K] and qb [N, K] row-major E4M3
+ * codes (lda, ldb ≥ K, multiples of 16 bytes); scale_a, scale_b device
+ * floats as written by tp_quantize_fp8.  TP_ERR_SHAPE / TP_ERR_ARG on bad
+ * sizes or alignment, before any launch. */
+tp_status tp_quantize_fp8(int64_t n, const void* x, void* q, float* scale_out,
+                          void* amax_work, tp_stream stream);
+tp_status tp_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* qa,
+                      int64_t lda, const float* scale_a, const void* qb,
+                      int64_t ldb, const float* scale_b, void* C, int64_t ldc,
+                      tp_stream stream);
+
 /* ------------------------------------------------------------ profiling --
  * Per-kernel-family device time for roofline reporting.  While enabled,
  * every kernel the library launches is bracketed by two CUDA events recorded
@@ -309,7 +338,8 @@ tp_status tp_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K,
  * family, the number of recorded launches, their summed duration and their
  * summed algorithmic FLOPs and bytes.  Families: 0 tcgen05 GEMM, 1 fp32
  * GEMM, 2 attention forward, 3 attention backward dK/dV, 4 attention
- * backward dQ, 5 shard-partial reduce, 6 other elementwise, 7 RMSNorm. */
+ * backward dQ, 5 shard-partial reduce, 6 other elementwise, 7 RMSNorm,
+ * 8 tcgen05 GEMM on E4M3 operands, 9 FP8 amax / quantize. */
 typedef struct {
   uint64_t launches;
   double ms;

@@ -76,7 +76,8 @@ class ProfileEntry(ctypes.Structure):
 
 
 KERNEL_FAMILIES = ["gemm_tc", "gemm_simt", "attn_fwd", "attn_bwd_dkdv",
-                   "attn_bwd_dq", "reduce", "elementwise", "rmsnorm"]
+                   "attn_bwd_dq", "reduce", "elementwise", "rmsnorm",
+                   "gemm_tc_fp8", "quantize_fp8"]
 
 _P = ctypes.c_void_p
 _I64, _I32, _F, _SZ, _U64 = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
@@ -107,6 +108,9 @@ SIGNATURES = {
                              ctypes.POINTER(CommReport)]),
     "tp_act_memory": (_I32, [ctypes.POINTER(ActDesc),
                              ctypes.POINTER(ActReport)]),
+    "tp_quantize_fp8": (_I32, [_I64, _P, _P, _P, _P, _P]),
+    "tp_gemm_fp8": (_I32, [_I64, _I64, _I64, _P, _I64, _P, _P, _I64, _P, _P,
+                           _I64, _P]),
     "tp_mlp_flops": (_I32, [_MP, _U64P, _U64P]),
     "tp_attn_flops": (_I32, [_AP, _U64P, _U64P]),
     "tp_gemm": (_I32, [_I32, _I64, _I64, _I64, _P, _I64, _I32, _P, _I64, _I32,
@@ -173,6 +177,24 @@ def comm_bytes(scope, T, h, n, dtype):
     check(lib().tp_comm_bytes(scope, T, h, n, dtype, ctypes.byref(r)),
           "tp_comm_bytes")
     return {k: getattr(r, k) for k, _ in CommReport._fields_}
+
+
+def quantize_fp8(x, q, scale, amax_work, stream=None):
+    """E4M3 codes of the bf16 tensor x into q (uint8, same numel); the
+    per-tensor scale into the one-element fp32 tensor ``scale``."""
+    check(lib().tp_quantize_fp8(x.numel(), ptr(x), ptr(q), ptr(scale),
+                                ptr(amax_work), stream_handle(stream)),
+          "tp_quantize_fp8")
+
+
+def gemm_fp8(qa, scale_a, qb, scale_b, C, stream=None):
+    """C[M, N] = qa·qbᵀ / (scale_a·scale_b) on E4M3 codes (K-major both)."""
+    M, N = C.shape
+    K = qa.shape[1]
+    check(lib().tp_gemm_fp8(M, N, K, ptr(qa), qa.stride(0), ptr(scale_a),
+                            ptr(qb), qb.stride(0), ptr(scale_b), ptr(C),
+                            C.stride(0), stream_handle(stream)),
+          "tp_gemm_fp8")
 
 
 def act_memory(b, s, h, h_ffn, n_q, n_kv, d, n, dtype=BF16, act=SWIGLU,

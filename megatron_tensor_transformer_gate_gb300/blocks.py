@@ -13,7 +13,8 @@ import torch
 
 from . import binding as B
 
-_TD = {B.F32: torch.float32, B.BF16: torch.bfloat16}
+_TD = {B.F32: torch.float32, B.BF16: torch.bfloat16,
+       B.FP8: torch.bfloat16}   # FP8 mode stores bf16 tensors
 
 
 def _buf(nbytes, device):

@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtp.so")
 
 SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "elementwise.cu",
-           "attn_fwd_tc.cu", "attn_bwd_tc.cu", "account.cpp"]
+           "attn_fwd_tc.cu", "attn_bwd_tc.cu", "fp8.cu", "account.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                 "-Xcompiler", "-O3", "-I", INCLUDE]

@@ -141,9 +141,13 @@ DropoutSpec make_dropout(float p, uint64_t seed) {
 }
 
 int run_gemm(const GemmProblem& g, tp_stream s) {
-  if (g.dtype == TP_BF16) return launch_gemm_tc(g, s, device_status_ptr());
+  if (g.dtype == TP_BF16 || g.dtype == TP_FP8)
+    return launch_gemm_tc(g, s, device_status_ptr());
   return launch_gemm_simt(g, s);
 }
+
+// The dtype tensors are stored in: FP8 mode keeps bf16 storage.
+int32_t storage(int32_t dtype) { return dtype == TP_FP8 ? TP_BF16 : dtype; }
 
 template <typename F>
 tp_status guarded(F&& f) {
@@ -157,7 +161,8 @@ tp_status guarded(F&& f) {
 // ------------------------------------------------------------------- MLP --
 tp_status check_mlp(const tp_mlp_desc* d) {
   if (d == nullptr) return TP_ERR_NULL;
-  if (d->dtype != TP_F32 && d->dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (d->dtype != TP_F32 && d->dtype != TP_BF16 && d->dtype != TP_FP8)
+    return TP_ERR_DTYPE;
   if (d->act != TP_GELU && d->act != TP_SWIGLU) return TP_ERR_DTYPE;
   if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED)
     return TP_ERR_DTYPE;
@@ -165,12 +170,18 @@ tp_status check_mlp(const tp_mlp_desc* d) {
   if (d->T > (1 << 30) || d->h > (1 << 20) || d->h_ffn > (1 << 24))
     return TP_ERR_SHAPE;
   if (d->h % 8 || d->h_ffn % d->n || (d->h_ffn / d->n) % 8) return TP_ERR_SHAPE;
+  if (d->dtype == TP_FP8 && (d->h % 16 || (d->h_ffn / d->n) % 16))
+    return TP_ERR_SHAPE;   // E4M3 rows: multiples of 16 bytes
   if (!(d->dropout_p >= 0.0f && d->dropout_p < 1.0f)) return TP_ERR_ARG;
   return TP_OK;
 }
 
 struct MlpFwdLayout {
   void *h_or_g = nullptr, *u = nullptr, *a = nullptr, *partials = nullptr;
+  // FP8 mode: E4M3 copies, scales (X, W1, A, W2) and amax scratch words
+  void *xq = nullptr, *w1q = nullptr, *aq = nullptr, *w2q = nullptr;
+  float* scales = nullptr;
+  unsigned* amax = nullptr;
   size_t bytes = 0;
 };
 
@@ -184,6 +195,15 @@ MlpFwdLayout mlp_fwd_layout(const tp_mlp_desc* d, void* ws) {
   L.a = c.take(tf);
   if (d->mode == TP_REDUCE_MATERIALISED)
     L.partials = c.take((size_t)d->n * (size_t)d->T * (size_t)d->h * es);
+  if (d->dtype == TP_FP8) {
+    const size_t w1rows = d->act == TP_SWIGLU ? 2 * d->h_ffn : d->h_ffn;
+    L.xq = c.take((size_t)d->T * (size_t)d->h);
+    L.w1q = c.take(w1rows * (size_t)d->h);
+    L.aq = c.take((size_t)d->T * (size_t)d->h_ffn);
+    L.w2q = c.take((size_t)d->h * (size_t)d->h_ffn);
+    L.scales = static_cast<float*>(c.take(4 * sizeof(float)));
+    L.amax = static_cast<unsigned*>(c.take(4 * sizeof(unsigned)));
+  }
   L.bytes = c.off;
   return L;
 }
@@ -268,22 +288,38 @@ extern "C" tp_status tp_mlp_fwd(const tp_mlp_desc* d, const void* X,
     const size_t es = elem_size(d->dtype);
     const DropoutSpec dr = make_dropout(d->dropout_p, d->seed);
 
+    const bool f8 = d->dtype == TP_FP8;
+    int err = 0;
+    if (f8) {   // quantize the first projection's operands
+      const int64_t w1rows = d->act == TP_SWIGLU ? 2 * f : f;
+      err = quantize_fp8(X, T * h, L.xq, L.scales + 0, L.amax + 0, stream);
+      if (!err)
+        err = quantize_fp8(W1, w1rows * h, L.w1q, L.scales + 1, L.amax + 1,
+                           stream);
+      if (err) return cuda_status(err);
+    }
+
     // column-parallel first projection + activation (shard-local)
     GemmProblem g1;
     g1.dtype = d->dtype;
     g1.M = T;
     g1.N = f;
-    g1.parts[0].a = op(X, h, 0, T);
-    g1.parts[0].b = op(W1, h, 0, f);
+    g1.parts[0].a = op(f8 ? L.xq : X, h, 0, T);
+    g1.parts[0].b = op(f8 ? L.w1q : W1, h, 0, f);
     g1.parts[0].kseg = h;
+    if (f8) {
+      g1.epi.scale_a = L.scales + 0;
+      g1.epi.scale_b = L.scales + 1;
+    }
     if (d->act == TP_GELU) {
       g1.epi.kind = EPI_GELU;
       g1.epi.out = L.h_or_g;
       g1.epi.out2 = L.a;
       g1.epi.bias = b1;
     } else {
-      g1.parts[0].b2 = op(static_cast<const char*>(W1) + (size_t)f * h * es, h,
-                          0, f);
+      g1.parts[0].b2 =
+          f8 ? op(static_cast<const char*>(L.w1q) + (size_t)f * h, h, 0, f)
+             : op(static_cast<const char*>(W1) + (size_t)f * h * es, h, 0, f);
       g1.epi.kind = EPI_SWIGLU;
       g1.epi.out = L.h_or_g;
       g1.epi.out2 = L.u;
@@ -291,16 +327,26 @@ extern "C" tp_status tp_mlp_fwd(const tp_mlp_desc* d, const void* X,
     }
     g1.epi.ldo = f;
     g1.epi.ldo2 = f;
-    int err = run_gemm(g1, stream);
+    err = run_gemm(g1, stream);
     if (err) return cuda_status(err);
+    if (f8) {   // quantize the second projection's operands
+      err = quantize_fp8(L.a, T * f, L.aq, L.scales + 2, L.amax + 2, stream);
+      if (!err)
+        err = quantize_fp8(W2, h * f, L.w2q, L.scales + 3, L.amax + 3, stream);
+      if (err) return cuda_status(err);
+    }
 
     // row-parallel second projection + g reduction + bias/dropout/residual
     GemmProblem g2;
     g2.dtype = d->dtype;
     g2.M = T;
     g2.N = h;
-    g2.parts[0].a = op(L.a, f, 0, T);
-    g2.parts[0].b = op(W2, f, 0, h);
+    g2.parts[0].a = op(f8 ? L.aq : L.a, f, 0, T);
+    g2.parts[0].b = op(f8 ? L.w2q : W2, f, 0, h);
+    if (f8) {
+      g2.epi.scale_a = L.scales + 2;
+      g2.epi.scale_b = L.scales + 3;
+    }
     if (d->mode == TP_REDUCE_FUSED) {
       g2.parts[0].kseg = f;
       g2.epi.kind = EPI_STORE;
@@ -325,8 +371,8 @@ extern "C" tp_status tp_mlp_fwd(const tp_mlp_desc* d, const void* X,
     g2.epi.out_z_stride = T * h;
     err = run_gemm(g2, stream);
     if (err) return cuda_status(err);
-    return cuda_status(reduce_t<int>(d->dtype, L.partials, n, T, h, b2, R, Out,
-                                     dr, stream));
+    return cuda_status(reduce_t<int>(storage(d->dtype), L.partials, n, T, h,
+                                     b2, R, Out, dr, stream));
   });
 }
 
@@ -339,6 +385,7 @@ extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
   return guarded([&]() -> tp_status {
     tp_status st = check_mlp(d);
     if (st != TP_OK) return st;
+    const int32_t sdt = storage(d->dtype);   // FP8 mode: bf16 backward
     if (!dOut || !X || !W1 || !W2 || !ws || !dX || !dW1 || !dW2 || !scratch)
       return TP_ERR_NULL;
     if (!aligned16(dOut) || !aligned16(X) || !aligned16(W1) ||
@@ -353,26 +400,26 @@ extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
     const int n = d->n;
     const bool swiglu = d->act == TP_SWIGLU;
     const int64_t fp = swiglu ? 2 * f : f;
-    const size_t es = elem_size(d->dtype);
+    const size_t es = elem_size(sdt);
     const DropoutSpec dr = make_dropout(d->dropout_p, d->seed);
     int err = 0;
 
     // dZ = dOut ⊙ mask/(1−p)
     const void* dZ = dOut;
     if (dr.enabled) {
-      err = d->dtype == TP_F32
+      err = sdt == TP_F32
                 ? dropout_bwd<float>(dOut, T * h, L.dz, dr, stream)
                 : dropout_bwd<__nv_bfloat16>(dOut, T * h, L.dz, dr, stream);
       if (err) return cuda_status(err);
       dZ = L.dz;
     }
     if (db2) {
-      err = colsum_d(d->dtype, dZ, T, h, db2, L.colsum, stream);
+      err = colsum_d(sdt, dZ, T, h, db2, L.colsum, stream);
       if (err) return cuda_status(err);
     }
     // dA = dZ·W2 (shard-local columns), through the activation
     GemmProblem ga;
-    ga.dtype = d->dtype;
+    ga.dtype = sdt;
     ga.M = T;
     ga.N = f;
     ga.parts[0].a = op(dZ, h, 0, T);
@@ -396,12 +443,12 @@ extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
     err = run_gemm(ga, stream);
     if (err) return cuda_status(err);
     if (db1) {
-      err = colsum_d(d->dtype, L.dh1, T, fp, db1, L.colsum, stream);
+      err = colsum_d(sdt, L.dh1, T, fp, db1, L.colsum, stream);
       if (err) return cuda_status(err);
     }
     // dW2 = dZᵀ·A  [h, f]
     GemmProblem gw2;
-    gw2.dtype = d->dtype;
+    gw2.dtype = sdt;
     gw2.M = h;
     gw2.N = f;
     gw2.parts[0].a = op(dZ, h, 1, h);
@@ -414,7 +461,7 @@ extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
     if (err) return cuda_status(err);
     // dW1 = dH1ᵀ·X  [fp, h]
     GemmProblem gw1;
-    gw1.dtype = d->dtype;
+    gw1.dtype = sdt;
     gw1.M = fp;
     gw1.N = h;
     gw1.parts[0].a = op(L.dh1, fp, 1, fp);
@@ -427,7 +474,7 @@ extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
     if (err) return cuda_status(err);
     // f: dX = Σ_i dH1_i·W1_i (+ dres)
     GemmProblem gx;
-    gx.dtype = d->dtype;
+    gx.dtype = sdt;
     gx.M = T;
     gx.N = h;
     gx.parts[0].a = op(L.dh1, fp, 0, T);
@@ -452,7 +499,7 @@ extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
     gx.epi.out_z_stride = T * h;
     err = run_gemm(gx, stream);
     if (err) return cuda_status(err);
-    return cuda_status(reduce_t<int>(d->dtype, L.partials, n, T, h, nullptr,
+    return cuda_status(reduce_t<int>(sdt, L.partials, n, T, h, nullptr,
                                      dres, dX, DropoutSpec(), stream));
   });
 }
@@ -808,6 +855,50 @@ extern "C" tp_status tp_gemm(int32_t dtype, int64_t M, int64_t N, int64_t K,
   });
 }
 
+extern "C" tp_status tp_quantize_fp8(int64_t n, const void* x, void* q,
+                                     float* scale_out, void* amax_work,
+                                     tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    if (!x || !q || !scale_out || !amax_work) return TP_ERR_NULL;
+    if (n < 1 || n % 8) return TP_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(q) ||
+        (reinterpret_cast<uintptr_t>(scale_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(amax_work) & 3u))
+      return TP_ERR_ARG;
+    return cuda_status(quantize_fp8(x, n, q, scale_out,
+                                    static_cast<unsigned*>(amax_work),
+                                    stream));
+  });
+}
+
+extern "C" tp_status tp_gemm_fp8(int64_t M, int64_t N, int64_t K,
+                                 const void* qa, int64_t lda,
+                                 const float* scale_a, const void* qb,
+                                 int64_t ldb, const float* scale_b, void* C,
+                                 int64_t ldc, tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    if (!qa || !qb || !C || !scale_a || !scale_b) return TP_ERR_NULL;
+    if (M < 1 || N < 1 || K < 1 || M > (1 << 30) || N > (1 << 30))
+      return TP_ERR_SHAPE;
+    if (lda % 16 || ldb % 16 || K % 16 || ldc % 8 || lda < K || ldb < K ||
+        ldc < N)
+      return TP_ERR_SHAPE;
+    if (!aligned16(qa) || !aligned16(qb) || !aligned16(C)) return TP_ERR_ARG;
+    GemmProblem g;
+    g.dtype = TP_FP8;
+    g.M = M;
+    g.N = N;
+    g.parts[0].a = op(qa, lda, 0, M);
+    g.parts[0].b = op(qb, ldb, 0, N);
+    g.parts[0].kseg = K;
+    g.epi.kind = EPI_STORE;
+    g.epi.out = C;
+    g.epi.ldo = ldc;
+    g.epi.scale_a = scale_a;
+    g.epi.scale_b = scale_b;
+    return cuda_status(run_gemm(g, stream));
+  });
+}
 
 // ------------------------------------------------------------- profiling --
 extern "C" tp_status tp_profile_enable(int32_t max_launches) {

@@ -45,4 +45,10 @@ int rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* gamma,
                         const float* rstd, const void* dres, void* dx,
                         void* dgamma, int64_t rows, int64_t h, void* stream);
 
+// Per-tensor scaled E4M3 codes of n bf16 values (n a multiple of 8): writes
+// q (n bytes) and the scale (one device float); amax_work is one device word
+// of scratch.  fp8.cu.
+int quantize_fp8(const void* x, int64_t n, void* q, float* scale,
+                 unsigned* amax_work, void* stream);
+
 }  // namespace tp

@@ -64,10 +64,17 @@ struct GemmEpilogue {
   // EPI_STORE only: write fp16 instead of bf16 (the attention-core operands);
   // a value beyond the fp16 range records a range error in the status word
   int out_f16 = 0;
+  // FP8 operands (GemmProblem::dtype 2): device pointers to the per-tensor
+  // quantization scales of A and B; the accumulator is multiplied by
+  // 1 / (scale_a·scale_b) before the rest of the epilogue
+  const float* scale_a = nullptr;
+  const float* scale_b = nullptr;
 };
 
 struct GemmProblem {
-  int dtype = 1;  // tp_dtype: 0 fp32 (CUDA cores), 1 bf16 (tensor cores)
+  // tp_dtype: 0 fp32 (CUDA cores), 1 bf16 (tensor cores), 2 E4M3 operands
+  // (tensor cores, K-major only, bf16 outputs, scales in the epilogue)
+  int dtype = 1;
   int64_t M = 0, N = 0;
   int nparts = 1;
   GemmPart parts[3];

@@ -145,7 +145,7 @@ __device__ __forceinline__ void store32_f16(__half* dst, const float* v,
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p,
                                               uint32_t taddr, int z, int m,
-                                              int n0) {
+                                              int n0, float dq) {
   const GemmEpilogue& e = p.epi;
   const bool row_ok = m < p.M;
   if constexpr (EPI == EPI_SWIGLU) {
@@ -163,8 +163,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p,
         float g[32], u[32], a[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          g[i] = __uint_as_float(rg[i]);
-          u[i] = __uint_as_float(ru[i]);
+          g[i] = __uint_as_float(rg[i]) * dq;
+          u[i] = __uint_as_float(ru[i]) * dq;
           a[i] = g[i] * sigmoid_f(g[i]) * u[i];
         }
         const int64_t off = (int64_t)m * e.ldo + n;
@@ -186,7 +186,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p,
       const int valid = min(32, p.N - n);
       float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * dq;
       if constexpr (EPI == EPI_STORE) {
         if (e.bias != nullptr) {
           float b[32];
@@ -259,9 +259,12 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p,
 }
 
 // ------------------------------------------------------------------ kernel --
-template <int A_MN, int B_MN, int EPI>
+// F8 = 1: E4M3 operands; a K block is 128 elements (the same 128 bytes per
+// row as 64 bf16 elements), one kind::f8f6f4 instruction per 32 of them.
+template <int A_MN, int B_MN, int EPI, int F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ TcParams p) {
+  constexpr int BKE = F8 ? 2 * BK : BK;   // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -339,7 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               const uint32_t fb = full0 + stage * 8;
               uint8_t* sa = smA + stage * A_BYTES;
               uint8_t* sb = smB + stage * B_BYTES;
-              const int k0 = kb * BK;
+              const int k0 = kb * BKE;
               if (A_MN) {
                 tma_load_3d_pair(sa, &p.ma[pi], fb, m0, k0, seg);
                 tma_load_3d_pair(sa + 8192, &p.ma[pi], fb, m0 + 64, k0, seg);
@@ -390,7 +393,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (leader && lane == 0) {
       // -------------------------------------------------------- MMA issue --
-      constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+      constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(2 * BM, BN)
+                                    : idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int it = 0;
@@ -423,7 +427,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const uint64_t bd =
                     B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
                          : smem_desc_sw128(b0 + kk * 32, 16, 1024);
-                tc_mma_f16_pair(d_tmem, ad, bd, IDESC, acc);
+                if (F8)
+                  tc_mma_f8_pair(d_tmem, ad, bd, IDESC, acc);
+                else
+                  tc_mma_f16_pair(d_tmem, ad, bd, IDESC, acc);
                 acc = 1;
               }
               tc_commit_pair(&empty[stage], 3);
@@ -447,6 +454,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3;   // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
     const uint32_t tempty0 = cluster_addr(tempty, 0);   // the leader's
+    const float dq = (F8 && p.epi.scale_a != nullptr)
+                         ? 1.0f / (*p.epi.scale_a * *p.epi.scale_b)
+                         : 1.0f;
     int it = 0;
     for (int t = cid; t < p.total_tiles; t += ncl, ++it) {
       int z, mt, nt;
@@ -458,7 +468,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN;
       epilogue_tile<EPI>(p, taddr, z, mt * 2 * BM + (int)rank * BM + row,
-                         nt * BN_LOG);
+                         nt * BN_LOG, dq);
       tc_fence_before();
       mbar_arrive_cluster(tempty0 + buf * 8);
     }
@@ -490,13 +500,13 @@ bool get_encode() {
 
 bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
                uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0,
-               uint32_t b1, uint32_t b2) {
+               uint32_t b1, uint32_t b2,
+               CUtensorMapDataType ty = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {s1, s2};
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                  const_cast<void*>(base), dims, strides, box, es,
+  return g_encode(m, ty, 3, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -505,7 +515,11 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
 // K-major operand (rows × K, row stride ld): dims {kseg, nseg, rows}.
 // MN-major operand (K × rows, row stride ld): dims {rows, kseg, nseg}.
 bool encode_operand(CUtensorMap* m, const GemmOperand& o, int64_t kseg,
-                    int nseg, uint32_t box_rows) {
+                    int nseg, uint32_t box_rows, bool f8 = false) {
+  if (f8)   // E4M3, K-major: 128-element (128-byte) K boxes
+    return !o.mn_major &&
+           encode_3d(m, o.ptr, kseg, nseg, o.rows, kseg, o.ld, 2 * BK, 1,
+                     box_rows, CU_TENSOR_MAP_DATA_TYPE_UINT8);
   if (o.mn_major)
     return encode_3d(m, o.ptr, o.rows, kseg, nseg, o.ld * 2,
                      (uint64_t)kseg * o.ld * 2, 64, BK, 1);
@@ -515,14 +529,14 @@ bool encode_operand(CUtensorMap* m, const GemmOperand& o, int64_t kseg,
 
 // One CTA pair per two SMs: the grid is as many pairs as can be resident
 // at once (clusters need both CTAs on SMs of one GPC), capped by the tiles.
-template <int A_MN, int B_MN, int EPI>
+template <int A_MN, int B_MN, int EPI, int F8 = 0>
 int launch_inst(const TcParams& prm, cudaStream_t s, double flops,
                 double bytes) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int clusters = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<A_MN, B_MN, EPI>,
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<A_MN, B_MN, EPI, F8>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     SMEM_BYTES);
     if (attr_err != cudaSuccess) return;
@@ -532,14 +546,14 @@ int launch_inst(const TcParams& prm, cudaStream_t s, double flops,
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     attr_err = cudaOccupancyMaxActiveClusters(
-        &clusters, gemm_tc_kernel<A_MN, B_MN, EPI>, &cfg);
+        &clusters, gemm_tc_kernel<A_MN, B_MN, EPI, F8>, &cfg);
     if (attr_err == cudaSuccess && clusters < 1) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int grid = 2 * std::min(prm.total_tiles, clusters);
   {
-    ProfScope ps(s, KF_GEMM_TC, flops, bytes);
-    gemm_tc_kernel<A_MN, B_MN, EPI><<<grid, THREADS, SMEM_BYTES, s>>>(prm);
+    ProfScope ps(s, F8 ? KF_GEMM_TC_FP8 : KF_GEMM_TC, flops, bytes);
+    gemm_tc_kernel<A_MN, B_MN, EPI, F8><<<grid, THREADS, SMEM_BYTES, s>>>(prm);
   }
   count_launch();
   return cudaGetLastError();
@@ -571,21 +585,27 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
       return cudaErrorInvalidValue;
   if (e.kind == EPI_SWIGLU && (b_mn || a_mn || pr.nparts != 1))
     return cudaErrorInvalidValue;
+  const bool f8 = pr.dtype == 2;
+  if (f8 && (a_mn || b_mn || e.out_f16 ||
+             (e.kind != EPI_STORE && e.kind != EPI_GELU &&
+              e.kind != EPI_SWIGLU)))
+    return cudaErrorInvalidValue;
+  const int bke = f8 ? 2 * BK : BK;   // K elements per stage
 
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
   prm.nparts = pr.nparts;
   for (int i = 0; i < pr.nparts; ++i) {
     const GemmPart& pt = pr.parts[i];
-    if (!encode_operand(&prm.ma[i], pt.a, pt.kseg, pt.nseg, BM))
+    if (!encode_operand(&prm.ma[i], pt.a, pt.kseg, pt.nseg, BM, f8))
       return cudaErrorInvalidValue;
     const uint32_t brows = BNH;   // each CTA of the pair loads half of B
-    if (!encode_operand(&prm.mb[i], pt.b, pt.kseg, pt.nseg, brows))
+    if (!encode_operand(&prm.mb[i], pt.b, pt.kseg, pt.nseg, brows, f8))
       return cudaErrorInvalidValue;
     if (e.kind == EPI_SWIGLU &&
-        !encode_operand(&prm.mb2, pt.b2, pt.kseg, pt.nseg, brows))
+        !encode_operand(&prm.mb2, pt.b2, pt.kseg, pt.nseg, brows, f8))
       return cudaErrorInvalidValue;
-    prm.part[i].kblocks = (int)((pt.kseg + BK - 1) / BK);
+    prm.part[i].kblocks = (int)((pt.kseg + bke - 1) / bke);
     prm.part[i].nsub = pt.nsub;
     prm.part[i].seg_z_stride = pt.seg_z_stride;
     prm.part[i].seg_sub_stride = pt.seg_sub_stride;
@@ -611,9 +631,17 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
   const double flops = 2.0 * (double)pr.M * ntot * ktile * pr.nz;
   const int outs = e.kind == EPI_SWIGLU ? 3
                    : (e.kind == EPI_GELU || e.kind == EPI_DSWIGLU) ? 2 : 1;
-  const double bytes = 2.0 * (((double)pr.M + ntot) * ktile * pr.nz +
-                              (double)pr.M * pr.N * pr.nz * outs);
+  const double bytes = (f8 ? 1.0 : 2.0) * ((double)pr.M + ntot) * ktile * pr.nz +
+                       2.0 * (double)pr.M * pr.N * pr.nz * outs;
 
+  if (f8) {
+    switch (e.kind) {
+      case EPI_STORE: return launch_inst<0, 0, EPI_STORE, 1>(prm, s, flops, bytes);
+      case EPI_GELU: return launch_inst<0, 0, EPI_GELU, 1>(prm, s, flops, bytes);
+      case EPI_SWIGLU: return launch_inst<0, 0, EPI_SWIGLU, 1>(prm, s, flops, bytes);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (e.kind) {
     case EPI_STORE:
       if (!a_mn && !b_mn) return launch_inst<0, 0, EPI_STORE>(prm, s, flops, bytes);

@@ -19,7 +19,9 @@ enum KernelFamily : int {
   KF_REDUCE = 5,
   KF_ELEMENTWISE = 6,
   KF_NORM = 7,
-  KF_COUNT = 8
+  KF_GEMM_TC_FP8 = 8,
+  KF_QUANT = 9,
+  KF_COUNT = 10
 };
 
 // RAII bracket around one kernel launch.
