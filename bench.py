@@ -47,7 +47,7 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="layer_bf16",
                     choices=["layer_bf16", "mlp_swiglu_bf16", "mlp_gelu_bf16",
-                             "attn_gqa_bf16"])
+                             "attn_gqa_bf16", "mlp_swiglu_fp8"])
     ap.add_argument("--mode", default="fused",
                     choices=["fused", "materialised"])
     ap.add_argument("--seq", type=int, default=0,
@@ -198,8 +198,9 @@ class Runner:
         elif self.kind == "mlp":
             self.x = I.mlp_inputs(cfg, seed, device)
             act = B.SWIGLU if cfg["act"] == "swiglu" else B.GELU
-            self.blk = TPMLP(T, h, cfg["h_ffn"], cfg["n"], act=act, mode=md,
-                             dropout_p=cfg.get("p", 0.0), seed=seed,
+            dt = B.FP8 if cfg.get("gemm_dtype") == "fp8" else B.BF16
+            self.blk = TPMLP(T, h, cfg["h_ffn"], cfg["n"], dtype=dt, act=act,
+                             mode=md, dropout_p=cfg.get("p", 0.0), seed=seed,
                              device=device)
             self.grads = self.blk.alloc_grads(
                 self.x["W1"], self.x["W2"], self.x["b1"] is not None,
@@ -261,8 +262,12 @@ def run_oracle_step(scfg, xs):
         oracle.layer_backward(xs["dOut"], xs["X"], xs, f, **shp)
     elif k == "mlp":
         p = scfg.get("p", 0.0)
-        f = oracle.mlp_forward(xs["X"], xs["W1"], xs["W2"], act=scfg["act"],
-                               b1=xs["b1"], b2=xs["b2"], R=xs["R"], p=p)
+        fwd = oracle.mlp_forward
+        if scfg.get("gemm_dtype") == "fp8":
+            from oracle import fp8
+            fwd = fp8.mlp_forward
+        f = fwd(xs["X"], xs["W1"], xs["W2"], act=scfg["act"], b1=xs["b1"],
+                b2=xs["b2"], R=xs["R"], p=p)
         oracle.mlp_backward(xs["dOut"], xs["X"], xs["W1"], xs["W2"], f,
                             act=scfg["act"], p=p)
     else:
@@ -406,17 +411,23 @@ def roofline(prof, steps, peaks, peaks_src, workload=None):
     dom = max(fams, key=lambda k: fams[k]["ms"])
     v = fams[dom]
     per_ms = v["ms"] / v["launches"]
-    if dom in ("gemm_tc", "attn_fwd", "attn_bwd_dkdv", "attn_bwd_dq"):
+    if dom in ("gemm_tc", "gemm_tc_fp8", "attn_fwd", "attn_bwd_dkdv",
+               "attn_bwd_dq"):
         peak = float(peaks.get("bf16_tflops_sustained",
                                peaks.get("bf16_tflops")))
+        if dom == "gemm_tc_fp8":   # E4M3: the bf16 figure × the 2x nominal ratio
+            peak *= 2.0
         ach = (v["flops"] / v["launches"]) / (per_ms / 1e3) / 1e12
         traffic, tsrc = committed_traffic(dom, workload)
-        burst = float(peaks.get("bf16_tflops", peak))
+        burst = float(peaks.get("bf16_tflops", peak)) * (
+            2.0 if dom == "gemm_tc_fp8" else 1.0)
         return {"bound": "tensor", "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
                 "traffic_source": tsrc, "kernel": dom,
                 "peak_burst": burst, "frac_burst": ach / burst,
-                "peak_source": f"{peaks_src} bf16_tflops_sustained",
+                "peak_source": f"{peaks_src} bf16_tflops_sustained" + (
+                    " x 2 (nominal e4m3 / bf16 ratio)"
+                    if dom == "gemm_tc_fp8" else ""),
                 "flops_per_launch": v["flops"] / v["launches"],
                 "ms_per_launch": per_ms}, kernels
     peak = float(peaks["hbm_gbs"])
@@ -549,7 +560,10 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": warmup,
             "ms_per_step": ms, "step_ms": step_stats,
             "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None,
+            "dtype": ("fp8 forward GEMMs (e4m3), bf16 backward"
+                      if cfg.get("gemm_dtype") == "fp8" else "bf16"),
+            "data": "synthetic",
             "config": conf,
             "pct_of_bf16_peak": 100.0 * value / world / burst,
             "pct_of_bf16_peak_sustained": 100.0 * value / world / sust,

@@ -40,6 +40,12 @@ WORKLOADS = {
     "mlp_swiglu_bf16": dict(kind="mlp", dtype="bf16", b=2, s=4096, h=4096,
                             h_ffn=11008, n=8, act="swiglu", w_std="fan_in",
                             b1=False, b2=False, residual=None, p=0.0),
+    # the SwiGLU workload with its forward GEMMs on per-tensor scaled E4M3
+    # (bf16 storage, bf16 backward)
+    "mlp_swiglu_fp8": dict(kind="mlp", dtype="bf16", gemm_dtype="fp8", b=2,
+                           s=4096, h=4096, h_ffn=11008, n=8, act="swiglu",
+                           w_std="fan_in", b1=False, b2=False, residual=None,
+                           p=0.0),
     "attn_gqa_bf16": dict(kind="attn", dtype="bf16", b=2, s=2048, h=4096,
                           n_q=32, n_kv=8, d=128, n=4, causal=True,
                           w_std=0.02, bo=False, residual=None),
