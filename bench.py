@@ -49,7 +49,7 @@ def parse_args():
                     choices=["layer_bf16", "mlp_swiglu_bf16", "mlp_gelu_bf16",
                              "attn_gqa_bf16", "mlp_swiglu_fp8"])
     ap.add_argument("--mode", default="fused",
-                    choices=["fused", "materialised"])
+                    choices=["fused", "materialised", "overlap"])
     ap.add_argument("--seq", type=int, default=0,
                     help="override s (smaller cases for profiler captures)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -184,7 +184,8 @@ class Runner:
             TPAttention, TPLayer, TPMLP)
         self.cfg = cfg
         self.kind = cfg["kind"]
-        md = B.FUSED if mode == "fused" else B.MATERIALISED
+        md = {"fused": B.FUSED, "materialised": B.MATERIALISED,
+              "overlap": B.OVERLAP}[mode]
         b, s, h = cfg["b"], cfg["s"], cfg["h"]
         T = b * s
         if self.kind == "layer":

@@ -67,7 +67,14 @@ typedef enum {
  * selects forward GEMMs on per-tensor scaled E4M3 operands (bf16 storage). */
 typedef enum { TP_F32 = 0, TP_BF16 = 1, TP_FP8 = 2 } tp_dtype;  /* δ = 4, 2, 1 */
 typedef enum { TP_GELU = 0, TP_SWIGLU = 1 } tp_act;
-typedef enum { TP_REDUCE_FUSED = 0, TP_REDUCE_MATERIALISED = 1 } tp_reduce_mode;
+/* TP_REDUCE_OVERLAP: materialised partials, summed band by band (row bands
+ * of the GEMM, up to 4) on a second stream while the GEMM computes the next
+ * band ([Troverld] §II.II tile-wise overlap of the reduction with the GEMM);
+ * the result equals TP_REDUCE_MATERIALISED bit for bit.  The library creates
+ * that stream (one per device) and orders it against the caller's stream
+ * with events; the call returns with all work ordered on `stream`. */
+typedef enum { TP_REDUCE_FUSED = 0, TP_REDUCE_MATERIALISED = 1,
+               TP_REDUCE_OVERLAP = 2 } tp_reduce_mode;
 typedef enum { TP_SCOPE_MLP = 0, TP_SCOPE_ATTN = 1, TP_SCOPE_LAYER = 2 } tp_scope;
 
 typedef void* tp_stream; /* cudaStream_t */

@@ -164,7 +164,8 @@ tp_status check_mlp(const tp_mlp_desc* d) {
   if (d->dtype != TP_F32 && d->dtype != TP_BF16 && d->dtype != TP_FP8)
     return TP_ERR_DTYPE;
   if (d->act != TP_GELU && d->act != TP_SWIGLU) return TP_ERR_DTYPE;
-  if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED)
+  if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED &&
+      d->mode != TP_REDUCE_OVERLAP)
     return TP_ERR_DTYPE;
   if (d->T < 1 || d->h < 8 || d->h_ffn < 8 || d->n < 1) return TP_ERR_SHAPE;
   if (d->T > (1 << 30) || d->h > (1 << 20) || d->h_ffn > (1 << 24))
@@ -193,7 +194,7 @@ MlpFwdLayout mlp_fwd_layout(const tp_mlp_desc* d, void* ws) {
   L.h_or_g = c.take(tf);
   if (d->act == TP_SWIGLU) L.u = c.take(tf);
   L.a = c.take(tf);
-  if (d->mode == TP_REDUCE_MATERIALISED)
+  if (d->mode != TP_REDUCE_FUSED)
     L.partials = c.take((size_t)d->n * (size_t)d->T * (size_t)d->h * es);
   if (d->dtype == TP_FP8) {
     const size_t w1rows = d->act == TP_SWIGLU ? 2 * d->h_ffn : d->h_ffn;
@@ -221,7 +222,7 @@ MlpBwdLayout mlp_bwd_layout(const tp_mlp_desc* d, void* scratch) {
   const int64_t fp = d->act == TP_SWIGLU ? 2 * d->h_ffn : d->h_ffn;
   if (d->dropout_p > 0.0f) L.dz = c.take((size_t)d->T * (size_t)d->h * es);
   L.dh1 = c.take((size_t)d->T * (size_t)fp * es);
-  if (d->mode == TP_REDUCE_MATERIALISED)
+  if (d->mode != TP_REDUCE_FUSED)
     L.partials = c.take((size_t)d->n * (size_t)d->T * (size_t)d->h * es);
   L.colsum = static_cast<float*>(c.take(std::max(
       colsum_scratch_bytes(d->T, fp), colsum_scratch_bytes(d->T, d->h))));
@@ -229,15 +230,96 @@ MlpBwdLayout mlp_bwd_layout(const tp_mlp_desc* d, void* scratch) {
   return L;
 }
 
-template <typename T>
-int reduce_t(int32_t dtype, const void* P, int n, int64_t rows, int64_t h,
-             const void* bias, const void* resid, void* out,
-             const DropoutSpec& dr, tp_stream s) {
-  (void)sizeof(T);
+int reduce_d(int32_t dtype, const void* P, int n, int64_t rows, int64_t h,
+             int64_t zstride, int64_t row0, const void* bias,
+             const void* resid, void* out, const DropoutSpec& dr,
+             tp_stream s) {
   return dtype == TP_F32
-             ? reduce_partials<float>(P, n, rows, h, bias, resid, out, dr, s)
-             : reduce_partials<__nv_bfloat16>(P, n, rows, h, bias, resid, out,
-                                              dr, s);
+             ? reduce_partials<float>(P, n, rows, h, zstride, row0, bias,
+                                      resid, out, dr, s)
+             : reduce_partials<__nv_bfloat16>(P, n, rows, h, zstride, row0,
+                                              bias, resid, out, dr, s);
+}
+
+// A second stream per device for the overlapped reductions, with a few
+// events; one caller at a time enqueues through it.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t ev[8] = {};
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+int side_stream(SideStream** out) {
+  int dev = 0;
+  int err = cudaGetDevice(&dev);
+  if (err) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  SideStream& ss = g_side[dev];
+  if (ss.s == nullptr) {
+    err = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking);
+    for (int i = 0; !err && i < 8; ++i)
+      err = cudaEventCreateWithFlags(&ss.ev[i], cudaEventDisableTiming);
+    if (err) return err;
+  }
+  *out = &ss;
+  return 0;
+}
+
+// A row-parallel projection (or input gradient) whose GEMM writes the n
+// shard partials [n][T, h] (batch z = shard z), followed by their sum
+// (+ bias, dropout, residual).  TP_REDUCE_MATERIALISED: the GEMM, then the
+// reduce.  TP_REDUCE_OVERLAP: the rows are cut into bands ([Troverld]
+// §II.II: the reduction of a tile can start as soon as the tile is
+// computed); band b's GEMM runs on `stream`, then its reduce on a second
+// stream after an event, while band b+1's GEMM runs; `stream` waits for the
+// last reduce.  The arithmetic of every element is the same in both modes.
+// The A operands of g are K-major [T, K] row blocks.
+int gemm_and_reduce(const GemmProblem& g, int32_t sdt, void* partials, int n,
+                    int64_t T, int64_t h, const void* bias, const void* resid,
+                    void* out, const DropoutSpec& dr, int32_t mode,
+                    tp_stream stream) {
+  const size_t eo = elem_size(sdt);
+  if (mode != TP_REDUCE_OVERLAP || T < 2048) {
+    int err = run_gemm(g, stream);
+    if (err) return err;
+    return reduce_d(sdt, partials, n, T, h, T * h, 0, bias, resid, out, dr,
+                    stream);
+  }
+  const size_t ea = g.dtype == TP_FP8 ? 1 : eo;
+  const int nb = (int)std::min<int64_t>(4, T / 1024);
+  // bands of whole 256-row pair tiles
+  const int64_t band = (T / nb + 255) / 256 * 256;
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStream* ss = nullptr;
+  int err = side_stream(&ss);
+  if (err) return err;
+  cudaStream_t main_s = static_cast<cudaStream_t>(stream);
+  int b = 0;
+  for (int64_t r0 = 0; r0 < T; r0 += band, ++b) {
+    const int64_t rows = std::min(band, T - r0);
+    GemmProblem gb = g;
+    gb.M = rows;
+    for (int p = 0; p < g.nparts; ++p) {
+      gb.parts[p].a.ptr = static_cast<const char*>(g.parts[p].a.ptr) +
+                          (size_t)r0 * (size_t)g.parts[p].a.ld * ea;
+      gb.parts[p].a.rows = rows;
+    }
+    gb.epi.out = static_cast<char*>(partials) + (size_t)r0 * (size_t)h * eo;
+    err = run_gemm(gb, stream);
+    if (!err) err = cudaEventRecord(ss->ev[b], main_s);
+    if (!err) err = cudaStreamWaitEvent(ss->s, ss->ev[b], 0);
+    if (!err)
+      err = reduce_d(sdt, static_cast<char*>(partials) + (size_t)r0 * h * eo,
+                     n, rows, h, T * h, r0, bias,
+                     resid ? static_cast<const char*>(resid) + r0 * h * eo
+                           : nullptr,
+                     static_cast<char*>(out) + (size_t)r0 * h * eo, dr, ss->s);
+    if (err) return err;
+  }
+  err = cudaEventRecord(ss->ev[b], ss->s);
+  if (!err) err = cudaStreamWaitEvent(main_s, ss->ev[b], 0);
+  return err;
 }
 
 int colsum_d(int32_t dtype, const void* X, int64_t rows, int64_t cols,
@@ -369,10 +451,8 @@ extern "C" tp_status tp_mlp_fwd(const tp_mlp_desc* d, const void* X,
     g2.epi.out = L.partials;
     g2.epi.ldo = h;
     g2.epi.out_z_stride = T * h;
-    err = run_gemm(g2, stream);
-    if (err) return cuda_status(err);
-    return cuda_status(reduce_t<int>(storage(d->dtype), L.partials, n, T, h,
-                                     b2, R, Out, dr, stream));
+    return cuda_status(gemm_and_reduce(g2, storage(d->dtype), L.partials, n,
+                                       T, h, b2, R, Out, dr, d->mode, stream));
   });
 }
 
@@ -497,10 +577,9 @@ extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
     gx.nz = n;
     gx.epi.out = L.partials;
     gx.epi.out_z_stride = T * h;
-    err = run_gemm(gx, stream);
-    if (err) return cuda_status(err);
-    return cuda_status(reduce_t<int>(sdt, L.partials, n, T, h, nullptr,
-                                     dres, dX, DropoutSpec(), stream));
+    return cuda_status(gemm_and_reduce(gx, sdt, L.partials, n, T, h, nullptr,
+                                       dres, dX, DropoutSpec(), d->mode,
+                                       stream));
   });
 }
 
@@ -510,7 +589,8 @@ namespace {
 tp_status check_attn(const tp_attn_desc* d) {
   if (d == nullptr) return TP_ERR_NULL;
   if (d->dtype != TP_F32 && d->dtype != TP_BF16) return TP_ERR_DTYPE;
-  if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED)
+  if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED &&
+      d->mode != TP_REDUCE_OVERLAP)
     return TP_ERR_DTYPE;
   if (d->b < 1 || d->s < 1 || d->h < 8 || d->n_q < 1 || d->n_kv < 1 ||
       d->d < 1 || d->n < 1)
@@ -540,7 +620,7 @@ AttnFwdLayout attn_fwd_layout(const tp_attn_desc* d, void* ws) {
   L.v = c.take(T * kd * 2);
   L.o = c.take(T * qd * 2);
   L.lse = static_cast<float*>(c.take((size_t)d->b * d->n_q * d->s * 4));
-  if (d->mode == TP_REDUCE_MATERIALISED)
+  if (d->mode != TP_REDUCE_FUSED)
     L.partials = c.take((size_t)d->n * T * (size_t)d->h * 2);
   L.bytes = c.off;
   return L;
@@ -566,7 +646,7 @@ AttnBwdLayout attn_bwd_layout(const tp_attn_desc* d, void* scratch) {
   const size_t stats = (size_t)d->b * d->n_q * attn_stats_pad(d->s) * 4;
   L.D = static_cast<float*>(c.take(stats));
   L.L2 = static_cast<float*>(c.take(stats));
-  if (d->mode == TP_REDUCE_MATERIALISED)
+  if (d->mode != TP_REDUCE_FUSED)
     L.partials = c.take((size_t)d->n * T * (size_t)d->h * 2);
   L.colsum = static_cast<float*>(c.take(colsum_scratch_bytes(T, d->h)));
   L.bytes = c.off;
@@ -657,10 +737,8 @@ extern "C" tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X,
     g.nz = n;
     g.epi.out = L.partials;
     g.epi.out_z_stride = T * h;
-    err = run_gemm(g, stream);
-    if (err) return cuda_status(err);
-    return cuda_status(reduce_partials<__nv_bfloat16>(
-        L.partials, n, T, h, bo, R, Out, DropoutSpec(), stream));
+    return cuda_status(gemm_and_reduce(g, TP_BF16, L.partials, n, T, h, bo, R,
+                                       Out, DropoutSpec(), d->mode, stream));
   });
 }
 
@@ -742,10 +820,9 @@ extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
     g.nz = n;
     g.epi.out = L.partials;
     g.epi.out_z_stride = T * h;
-    err = run_gemm(g, stream);
-    if (err) return cuda_status(err);
-    return cuda_status(reduce_partials<__nv_bfloat16>(
-        L.partials, n, T, h, nullptr, dres, dX, DropoutSpec(), stream));
+    return cuda_status(gemm_and_reduce(g, TP_BF16, L.partials, n, T, h,
+                                       nullptr, dres, dX, DropoutSpec(),
+                                       d->mode, stream));
   });
 }
 

@@ -93,7 +93,8 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
 template <typename T>
 __global__ void __launch_bounds__(256)
     reduce_partials_kernel(const T* __restrict__ P, int n, int64_t count,
-                           int64_t h, const T* __restrict__ bias,
+                           int64_t zstride, int64_t e0, int64_t h,
+                           const T* __restrict__ bias,
                            const T* __restrict__ resid, T* __restrict__ out,
                            int dropout, uint32_t thr, float scale,
                            uint64_t seed) {
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(256)
     float acc[V], v[V];
     Vec<T>::load(P + i, acc);
     for (int s = 1; s < n; ++s) {
-      Vec<T>::load(P + (int64_t)s * count + i, v);
+      Vec<T>::load(P + (int64_t)s * zstride + i, v);
 #pragma unroll
       for (int q = 0; q < V; ++q) acc[q] += v[q];
     }
@@ -117,8 +118,9 @@ __global__ void __launch_bounds__(256)
     if (dropout) {
 #pragma unroll
       for (int q = 0; q < V; ++q)
-        acc[q] = dropout_keep(seed, (uint64_t)(i + q), thr) ? acc[q] * scale
-                                                            : 0.0f;
+        acc[q] = dropout_keep(seed, (uint64_t)(e0 + i + q), thr)
+                     ? acc[q] * scale
+                     : 0.0f;
     }
     if (resid != nullptr) {
       Vec<T>::load(resid + i, v);
@@ -368,8 +370,9 @@ int grid_for(int64_t work_items, int per_block) {
 // ------------------------------------------------------------------- host --
 template <typename T>
 int reduce_partials(const void* P, int n, int64_t rows, int64_t h,
-                    const void* bias, const void* resid, void* out,
-                    const DropoutSpec& d, void* stream) {
+                    int64_t zstride, int64_t row0, const void* bias,
+                    const void* resid, void* out, const DropoutSpec& d,
+                    void* stream) {
   const int64_t count = rows * h;
   if (count == 0) return cudaSuccess;
   const int grid = grid_for(count / Vec<T>::N, 256);
@@ -377,7 +380,8 @@ int reduce_partials(const void* P, int n, int64_t rows, int64_t h,
                (double)sizeof(T) * count *
                    (n + 1 + (resid != nullptr ? 1 : 0)));
   reduce_partials_kernel<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const T*>(P), n, count, h, static_cast<const T*>(bias),
+      static_cast<const T*>(P), n, count, zstride, row0 * h, h,
+      static_cast<const T*>(bias),
       static_cast<const T*>(resid), static_cast<T*>(out), d.enabled, d.thr,
       d.scale, d.seed);
   count_launch();
@@ -484,8 +488,8 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
 
 #define TP_INST(T)                                                            \
   template int reduce_partials<T>(const void*, int, int64_t, int64_t,         \
-                                  const void*, const void*, void*,            \
-                                  const DropoutSpec&, void*);                 \
+                                  int64_t, int64_t, const void*, const void*, \
+                                  void*, const DropoutSpec&, void*);          \
   template int dropout_bwd<T>(const void*, int64_t, void*, const DropoutSpec&, \
                               void*);                                         \
   template int colsum<T>(const void*, int64_t, int64_t, int64_t, void*,       \

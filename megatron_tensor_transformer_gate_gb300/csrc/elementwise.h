@@ -13,11 +13,14 @@ struct DropoutSpec {
   uint64_t seed = 0;
 };
 
-// out = resid + Dropout(Σ_{i<n} P[i] + bias); P is n × [rows, h] contiguous.
+// out = resid + Dropout(Σ_{i<n} P[i] + bias) over rows [rows, h]; partial i
+// starts zstride elements after partial i−1; row0 is the first row's index
+// in the whole [T, h] tensor (the dropout draw of element (t, j) is t·h + j).
 template <typename T>
 int reduce_partials(const void* P, int n, int64_t rows, int64_t h,
-                    const void* bias, const void* resid, void* out,
-                    const DropoutSpec& d, void* stream);
+                    int64_t zstride, int64_t row0, const void* bias,
+                    const void* resid, void* out, const DropoutSpec& d,
+                    void* stream);
 // dz = dout ⊙ mask · scale over `count` elements of a [*, h] tensor.
 template <typename T>
 int dropout_bwd(const void* dout, int64_t count, void* dz,

@@ -79,3 +79,22 @@ def test_gqa_layer_widths(tp):
     cfg = I.workload("attn_gqa_bf16", b=1, s=512, h=8192, n_q=64, n_kv=8,
                      n=8)
     run_case(tp, cfg, 0, 20260005)
+
+
+def test_overlapped_reduction_attention_workload(tp):
+    # the attention workload (T 4096) with the out-projection g and the input
+    # gradient f reduced band by band: against the oracle, and bit-identical
+    # to the materialised mode
+    cfg = I.workload("attn_gqa_bf16")
+    run_case(tp, cfg, tp.OVERLAP, 20260004)
+    x = I.attn_inputs(cfg, 20260004, "cuda")
+    res = []
+    for mode in (tp.MATERIALISED, tp.OVERLAP):
+        a = TPAttention(cfg["b"], cfg["s"], cfg["h"], cfg["n_q"], cfg["n_kv"],
+                        cfg["d"], cfg["n"], mode=mode)
+        out = a.forward(x["X"], x["Wq"], x["Wk"], x["Wv"], x["Wo"])
+        g = a.backward(x["dOut"], x["X"], x["Wq"], x["Wk"], x["Wv"], x["Wo"])
+        tp.device_status()
+        res.append([out.clone(), g["dX"].clone()])
+    for u, v in zip(*res):
+        assert u.equal(v)

@@ -142,3 +142,24 @@ def test_bf16_swiglu_layer_widths(tp):
     cfg = I.workload("mlp_swiglu_bf16", b=1, s=512, h=8192, h_ffn=28672,
                      n=8, w_std=0.02, residual="X")
     run_case(tp, cfg, 0, 20260005)
+
+
+def test_overlapped_reduction_equals_materialised(tp):
+    # TP_REDUCE_OVERLAP sums the same partials band by band on a second
+    # stream: bit-identical to the materialised mode, bias, dropout (the mask
+    # draw index must follow the band's rows) and residual included
+    cfg = I.workload("mlp_gelu_bf16")           # T 4096: four bands
+    T = cfg["b"] * cfg["s"]
+    x = I.mlp_inputs(cfg, 20260002, "cuda")
+    res = {}
+    for mode in (tp.MATERIALISED, tp.OVERLAP):
+        m = TPMLP(T, cfg["h"], cfg["h_ffn"], cfg["n"], act=tp.GELU, mode=mode,
+                  dropout_p=cfg["p"], seed=20260002)
+        out = m.forward(x["X"], x["W1"], x["W2"], b2=x["b2"], R=x["X"])
+        g = m.backward(x["dOut"], x["X"], x["W1"], x["W2"], dres=x["dOut"],
+                       want_db2=True)
+        tp.device_status()
+        res[mode] = [out.clone()] + [g[k].clone() for k in ("dX", "dW1",
+                                                             "dW2", "db2")]
+    for a, b in zip(res[tp.MATERIALISED], res[tp.OVERLAP]):
+        assert torch.equal(a, b)
