@@ -14,7 +14,8 @@ job: FLOPs per step (the pages' closed forms, causal pairs only) × ranks ÷ the
 slowest rank's mean step time.  `roofline` covers the dominant kernel family,
 timed live with CUDA events recorded on its launch stream.  `e2e` repeats the
 measurement through the same public API with the step's activations copied
-from pinned host memory and the results read back inside the timed region.
+from pinned host memory and the results read back inside the timed region;
+a copy stream overlaps those transfers with the neighbouring steps' compute.
 `cpu_baseline` times the fp64 oracle on a bounded sample of the same
 workload.  `--impl reference` times that oracle alone (the reference arm).
 """
@@ -221,25 +222,27 @@ class Runner:
                 n += v.numel() * v.element_size()
         return n
 
-    def step(self, X=None, dOut=None):
+    def step(self, X=None, dOut=None, out=None, grads=None):
         x = self.x
         X = x["X"] if X is None else X
         dOut = x["dOut"] if dOut is None else dOut
+        out = self.out if out is None else out
+        grads = self.grads if grads is None else grads
         if self.kind == "layer":
-            self.blk.forward(X, self.P, out=self.out)
-            self.blk.backward(dOut, X, self.P, grads=self.grads)
+            self.blk.forward(X, self.P, out=out)
+            self.blk.backward(dOut, X, self.P, grads=grads)
         elif self.kind == "mlp":
             R = X if self.cfg.get("residual") == "X" else x["R"]
             self.blk.forward(X, x["W1"], x["W2"], b1=x["b1"], b2=x["b2"],
-                             R=R, out=self.out)
+                             R=R, out=out)
             dres = dOut if self.cfg.get("residual") == "X" else None
             self.blk.backward(dOut, X, x["W1"], x["W2"], dres=dres,
-                              grads=self.grads)
+                              grads=grads)
         else:
             self.blk.forward(X, x["Wq"], x["Wk"], x["Wv"], x["Wo"],
-                             bo=x["bo"], R=x["R"], out=self.out)
+                             bo=x["bo"], R=x["R"], out=out)
             self.blk.backward(dOut, X, x["Wq"], x["Wk"], x["Wv"], x["Wo"],
-                              grads=self.grads)
+                              grads=grads)
 
 
 # ------------------------------------------------------------ CPU baseline --
@@ -506,32 +509,63 @@ def main():
         ms = float(t.item())
     value = fl * world / (ms / 1e3) / 1e12
 
-    # ---- end to end: pinned host activations in, results out, every step
+    # ---- end to end: every step's activations come from pinned host memory
+    # and its output and input gradient go back to pinned host memory.  A
+    # copy stream feeds step k+1's inputs and drains step k's results while
+    # step k+1 computes (inputs and the two read-back results are double-
+    # buffered; events order every reuse), so the step pays only the part
+    # of the transfers that the compute does not cover.
     e2e = None
     if not args.no_e2e:
         hX = run.x["X"].to("cpu").pin_memory()
         hdO = run.x["dOut"].to("cpu").pin_memory()
-        dX_res = run.grads["dX"]
-        hOut = torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
-        hdX = torch.empty(dX_res.shape, dtype=dX_res.dtype).pin_memory()
-        dXin = torch.empty_like(run.x["X"])
-        ddO = torch.empty_like(run.x["dOut"])
+        xin = [torch.empty_like(run.x["X"]) for _ in range(2)]
+        din = [torch.empty_like(run.x["dOut"]) for _ in range(2)]
+        outs = [run.out, torch.empty_like(run.out)]
+        gsets = [run.grads, dict(run.grads)]
+        gsets[1]["dX"] = torch.empty_like(run.grads["dX"])
+        hOut = [torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory()
+                for _ in range(2)]
+        hdX = [torch.empty(run.grads["dX"].shape,
+                           dtype=run.grads["dX"].dtype).pin_memory()
+               for _ in range(2)]
         h2d = hX.numel() * hX.element_size() + hdO.numel() * hdO.element_size()
-        d2h = (hOut.numel() * hOut.element_size()
-               + hdX.numel() * hdX.element_size())
+        d2h = (hOut[0].numel() * hOut[0].element_size()
+               + hdX[0].numel() * hdX[0].element_size())
+        cs = torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()
+        in_ready, done, drained = ([ev() for _ in range(2)] for _ in range(3))
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(args.steps):
-            dXin.copy_(hX, non_blocking=True)
-            ddO.copy_(hdO, non_blocking=True)
-            run.step(dXin, ddO)
-            hOut.copy_(run.out, non_blocking=True)
-            hdX.copy_(dX_res, non_blocking=True)
-        t1.record(stream)
+        t0.record(cs)
+        with torch.cuda.stream(cs):
+            xin[0].copy_(hX, non_blocking=True)
+            din[0].copy_(hdO, non_blocking=True)
+            in_ready[0].record(cs)
+        for k in range(args.steps):
+            b = k % 2
+            stream.wait_event(in_ready[b])
+            if k >= 2:
+                stream.wait_event(drained[b])   # outs[b] read back
+            run.step(xin[b], din[b], out=outs[b], grads=gsets[b])
+            done[b].record(stream)
+            with torch.cuda.stream(cs):
+                if k + 1 < args.steps:
+                    nb = 1 - b
+                    if k >= 1:
+                        cs.wait_event(done[nb])  # step k−1 has read them
+                    xin[nb].copy_(hX, non_blocking=True)
+                    din[nb].copy_(hdO, non_blocking=True)
+                    in_ready[nb].record(cs)
+                cs.wait_event(done[b])
+                hOut[b].copy_(outs[b], non_blocking=True)
+                hdX[b].copy_(gsets[b]["dX"], non_blocking=True)
+                drained[b].record(cs)
+        cs.wait_stream(stream)
+        t1.record(cs)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -542,7 +576,9 @@ def main():
             ems = float(t.item())
         e2e = {"value": fl * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": ems, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+               "d2h_bytes_per_step": d2h,
+               "pipeline": "copy stream: inputs of step k+1 in and results "
+                           "of step k out while step k+1 computes"}
 
     roof, kernels = roofline(prof, args.steps, peaks, peaks_src, args.workload)
     cpu = None
