@@ -171,8 +171,9 @@ typedef struct {
  * TP_ERR_RANGE. */
 size_t tp_attn_workspace_bytes(const tp_attn_desc* d);
 /* scratch: dO (fp16), dQ, dK, dV (bf16), D = rowsum(dO∘O) and LSE·log2e
- * (fp32, [b, n_q, s rounded up to 128]), partials and
- * column-sum partials. */
+ * (fp32, [b, n_q, s rounded up to 128]), the score gradient dS in fp16
+ * 128×128 tiles (b·n_q·B(B+1)/2 tiles causal, b·n_q·B² full, B = ⌈s/128⌉;
+ * 32 KB each), partials and column-sum partials. */
 size_t tp_attn_bwd_scratch_bytes(const tp_attn_desc* d);
 
 tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X, const void* Wq,

@@ -628,11 +628,14 @@ AttnFwdLayout attn_fwd_layout(const tp_attn_desc* d, void* ws) {
 
 struct AttnBwdLayout {
   void *dO = nullptr, *dQ = nullptr, *dK = nullptr, *dV = nullptr;
+  void* dS = nullptr;
   float *D = nullptr, *L2 = nullptr;
   void* partials = nullptr;
   float* colsum = nullptr;
   size_t bytes = 0;
 };
+
+AttnShape attn_shape(const tp_attn_desc* d);
 
 AttnBwdLayout attn_bwd_layout(const tp_attn_desc* d, void* scratch) {
   AttnBwdLayout L;
@@ -646,6 +649,7 @@ AttnBwdLayout attn_bwd_layout(const tp_attn_desc* d, void* scratch) {
   const size_t stats = (size_t)d->b * d->n_q * attn_stats_pad(d->s) * 4;
   L.D = static_cast<float*>(c.take(stats));
   L.L2 = static_cast<float*>(c.take(stats));
+  L.dS = c.take((size_t)attn_ds_bytes(attn_shape(d)));
   if (d->mode != TP_REDUCE_FUSED)
     L.partials = c.take((size_t)d->n * T * (size_t)d->h * 2);
   L.colsum = static_cast<float*>(c.take(colsum_scratch_bytes(T, d->h)));
@@ -783,7 +787,7 @@ extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
                      stream);
     if (err) return cuda_status(err);
     err = flash_bwd(attn_shape(d), F.q, F.k, F.v, F.o, L.dO, F.lse, L.D, L.L2,
-                    L.dQ, L.dK, L.dV, device_status_ptr(), stream);
+                    L.dS, L.dQ, L.dK, L.dV, device_status_ptr(), stream);
     if (err) return cuda_status(err);
     err = run_gemm(proj(qd, h, op(L.dQ, qd, 1, qd), op(X, h, 1, h), T, dWq, h),
                    stream);

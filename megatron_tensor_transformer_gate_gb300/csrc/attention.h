@@ -20,11 +20,14 @@ int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
               void* O, float* LSE, unsigned* status, void* stream);
 // Backward on tcgen05 (attn_bwd_tc.cu): dQ, dK, dV (bf16, GQA groups summed).
 // Dp and L2p are fp32 scratch of b·nq·attn_stats_pad(s) elements each
-// (D = rowsum(dO∘O) and LSE·log2e, zero-padded); dO is fp16.
+// (D = rowsum(dO∘O) and LSE·log2e, zero-padded); dO is fp16.  dS is
+// attn_ds_bytes(sh) bytes of scratch (16-byte aligned) for the fp16 score
+// gradient tiles that the dK/dV kernel writes and the dQ kernel reads.
 int64_t attn_stats_pad(int64_t s);
+int64_t attn_ds_bytes(const AttnShape& sh);
 int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
               const void* O, const void* dO, const float* LSE, float* Dp,
-              float* L2p, void* dQ, void* dK, void* dV, unsigned* status,
-              void* stream);
+              float* L2p, void* dS, void* dQ, void* dK, void* dV,
+              unsigned* status, void* stream);
 
 }  // namespace tp

@@ -7,34 +7,42 @@
 //
 //   pre-pass  D = rowsum(dO ∘ O) and LSE·log2e per (batch, head, position),
 //             padded with zeros to a multiple of 128 positions.
-//   dQ        CTA = 128 queries of one (batch, q head); per block of 128 keys
-//               S = Q·Kᵀ, dP = dO·Vᵀ            (M=128, N=128, K=128) → TMEM
-//               dS = P ⊙ (dP − D), P = exp2(S·c − LSE·log2e)   (elementwise)
-//               dQ += dS·K                       (M=128, N=128, K=128) → TMEM
-//             Q and dO sit in TMEM as the A operands of S and dP.
 //   dK, dV    CTA = 128 keys of one (batch, kv head); per q head of the GQA
 //             group and block of 128 queries at or after the keys
 //               Sᵀ = K·Qᵀ, then dPᵀ = V·dOᵀ      (M=128, N=128, K=128) → TMEM
+//               Pᵀ = exp2(Sᵀ·c − LSE·log2e), dSᵀ = Pᵀ ⊙ (dPᵀ − D)
 //               dV += Pᵀ·dO,  dK += dSᵀ·Q        (M=128, N=128, K=128) → TMEM
 //             K and V sit in TMEM as the A operands; Sᵀ and dPᵀ of a block
 //             take turns in one 128-column TMEM buffer, which leaves room
-//             for both accumulators.
-// Both: warp 0 TMA, warp 1 TMEM allocation + single-thread MMA issue, warps
-// 2–9 elementwise (two threads per TMEM lane, half of the columns each).
-// The score MMAs of the next block are issued as soon as the elementwise
-// warps have copied the current scores to registers, ahead of the gradient
-// MMAs, so the tensor cores work while the elementwise warps do.  The
-// elementwise loops are unrolled but branch-free (masks come from padding
-// and a fix-up of the causal diagonal on packed words): a per-block body
-// that outgrows the instruction cache runs several times slower.  K and V
-// (dQ) or Q and dO (dK, dV) stream through rings of their own, each tile
-// freed by the last MMA that reads it.  A tcgen05.mma of M=128 costs about
-// the same for N=64 as for N=128, so the wider blocks do twice the work per
-// instruction.  No atomics: reruns are bit-identical, and the GQA sums of
-// dK, dV stay inside one CTA.
+//             for both accumulators.  Each dSᵀ tile (fp16, 32 KB) also goes
+//             out to global memory with one bulk copy, in the swizzled
+//             layout the tensor cores read.
+//   dQ        a persistent streaming GEMM over those tiles: per (batch, q
+//             head, block of 128 queries) dQ = Σ_kb dS_kb·K_kb over the key
+//             blocks at or before it (M=128, N=128, K=128 per tile; dSᵀ is
+//             the M-major A operand, K the N-major B), two TMEM accumulators
+//             so the epilogue of one block overlaps the next.
+// Computing dQ from the stored dS instead of recomputing S and dP per query
+// block moves 2·32 KB of HBM traffic per 128×128 block pair (the tile out,
+// then back in) in place of two of the seven products of the backward; the
+// dQ kernel is bound by reading the tiles.
+// dK/dV: warp 0 TMA (+ one thread for the dSᵀ copies), warp 1 TMEM
+// allocation + single-thread MMA issue, warps 2–9 elementwise (two threads
+// per TMEM lane, half of the columns each).  The score MMAs of the next
+// block are issued as soon as the elementwise warps have copied the current
+// scores to registers, ahead of the gradient MMAs, so the tensor cores work
+// while the elementwise warps do.  The elementwise loops are unrolled but
+// branch-free (masks come from padding and a fix-up of the causal diagonal
+// on packed words): a per-block body that outgrows the instruction cache
+// runs several times slower.  Q and dO stream through rings of their own,
+// each tile freed by the last MMA that reads it.  A tcgen05.mma of M=128
+// costs about the same for N=64 as for N=128, so the wider blocks do twice
+// the work per instruction.  No atomics: reruns are bit-identical, and the
+// GQA sums of dK, dV stay inside one CTA.
 // Operands fp16, accumulation fp32; dQ, dK, dV are written in bf16.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "attention.h"
@@ -58,6 +66,23 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src,
       "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Shared → global bulk copy (async proxy), tracked by this thread's bulk
+// groups: commit, then wait until the source may be overwritten (read) or
+// until the writes are done.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src,
+                                           uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(dst), "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // K-major operand with K = 128 in two 64-column halves `atom` bytes apart.
@@ -124,21 +149,6 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// ----------------------------------------------------------------------- dQ --
-namespace dq {
-constexpr int NK = 3, NV = 2;                 // K ring and V ring depths
-constexpr int TILE = 2 * A128;                // one 128-key tile, 32 KB
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + NK * TILE;
-constexpr int OFF_DS = OFF_V + NV * TILE;     // 2 buffers of 32 KB
-constexpr int OFF_BAR = OFF_DS + 2 * TILE;
-constexpr int SMEM = OFF_BAR + 256 + 1024;
-// Q and dO live in TMEM as the A operands of S and dP (fp16 pairs, 64
-// columns each); S, dP (128 keys each) and the dQ accumulator fill the rest.
-constexpr uint32_t COL_Q = 0, COL_DO = 64, COL_S = 128, COL_DP = 256,
-                   COL_DQ = 384;
-}  // namespace dq
-
 struct BwdTcArgs {
   CUtensorMap mq, mk, mv, mdo;
   const __half* q;       // [b, s, nq·d] as the tensor maps
@@ -149,10 +159,25 @@ struct BwdTcArgs {
   const float* L2p;
   __nv_bfloat16* out0;   // dQ, or dK
   __nv_bfloat16* out1;   // dV
+  uint8_t* ds;           // dSᵀ tiles, 32 KB each (see ds_tile)
+  int hk0, hkn;          // this pass: (batch, kv head) pairs [hk0, hk0+hkn)
   int s, s_pad, nq, nkv, causal;
   float scale, scale_log2;
   unsigned* status;
 };
+
+// Index of the dSᵀ tile of (q head lh of this pass, query block qb, key
+// block kb), lh = (pair − hk0)·group + head within the group: per head the
+// query blocks in order, each with its key blocks in order (causal: kb ≤ qb
+// only), so one query block's tiles are contiguous.
+__device__ __forceinline__ int64_t ds_tile(const BwdTcArgs& a, int lh, int qb,
+                                           int kb, int nblk) {
+  const int64_t per_head =
+      a.causal ? (int64_t)nblk * (nblk + 1) / 2 : (int64_t)nblk * nblk;
+  const int64_t first =
+      a.causal ? (int64_t)qb * (qb + 1) / 2 : (int64_t)qb * nblk;
+  return (int64_t)lh * per_head + first + kb;
+}
 
 // Row r of a 128-row K-major swizzled half tile (128-byte rows): its eight
 // 16-byte chunks from 32 packed words.
@@ -164,173 +189,155 @@ __device__ __forceinline__ void st_row8(uint8_t* tile, int r,
         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
-// dS for 32 keys of one query row: P = exp2(S·c − L2), dS = P·(dP − D),
-// packed in fp16 pairs (element 2j in the low half of word j).
-__device__ __forceinline__ void ds_chunk(const uint32_t (&sv)[32],
-                                         const uint32_t (&pv)[32], float c,
-                                         float l2, float dd, uint32_t* pk) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), c, -l2));
-    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), c, -l2));
-    pk[i >> 1] = pack_f16x2(p0 * (__uint_as_float(pv[i]) - dd),
-                            p1 * (__uint_as_float(pv[i + 1]) - dd));
-  }
-}
-
-// Causal masks of a diagonal block on 64 fp16 values in 32 packed words:
-// keep elements [0, t] (keep_upto) or [t, 64) (keep_from), zero the rest.
-// Applied to packed words so the unrolled hot loops stay branch-free.
-__device__ __forceinline__ void keep_upto(uint32_t (&w)[32], int t) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    w[j] &= (2 * j > t) ? 0u : (2 * j + 1 > t ? 0x0000ffffu : 0xffffffffu);
-}
+// Causal mask of a diagonal block on 64 fp16 values in 32 packed words:
+// keep elements [t, 64), zero the rest.  Applied to packed words so the
+// unrolled hot loop stays branch-free.
 __device__ __forceinline__ void keep_from(uint32_t (&w)[32], int t) {
 #pragma unroll
   for (int j = 0; j < 32; ++j)
     w[j] &= (2 * j + 1 < t) ? 0u : (2 * j < t ? 0xffff0000u : 0xffffffffu);
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+// ----------------------------------------------------------------------- dQ --
+namespace dq {
+constexpr int NS = 3;                          // stages of (dSᵀ, K) tiles
+constexpr int TILE = 2 * A128;                 // 128 × 128 fp16, 32 KB
+constexpr int OFF_DS = 0;
+constexpr int OFF_K = NS * TILE;
+constexpr int OFF_BAR = 2 * NS * TILE;
+constexpr int SMEM = OFF_BAR + 256 + 1024;
+constexpr int NTHREADS = 192;                  // TMA, MMA, 4 epilogue warps
+constexpr uint32_t NCOLS = 256;                // two 128-column accumulators
+}  // namespace dq
+
+__global__ void __launch_bounds__(dq::NTHREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ BwdTcArgs a) {
   using namespace dq;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint64_t* q_full = bar;              // Q and dO written to TMEM
-  uint64_t* k_full = bar + 1;          // [NK]
-  uint64_t* k_empty = k_full + NK;     // [NK]
-  uint64_t* v_full = k_empty + NK;     // [NV]
-  uint64_t* v_empty = v_full + NV;     // [NV]
-  uint64_t* sdp_full = v_empty + NV;   // S and dP of the current block
-  uint64_t* sdp_free = sdp_full + 1;   // S, dP copied to registers
-  uint64_t* ds_full = sdp_free + 1;    // [2]
-  uint64_t* ds_free = ds_full + 2;     // [2]
-  uint64_t* dq_done = ds_free + 2;
-  uint64_t* drain = dq_done + 1;
+  uint64_t* full = bar;              // [NS] dSᵀ and K tiles landed
+  uint64_t* empty = full + NS;       // [NS] their MMAs done
+  uint64_t* tfull = empty + NS;      // [2] accumulator complete
+  uint64_t* tempty = tfull + 2;      // [2] accumulator read out
+  uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // 1-D grid, block rank slowest: the heaviest query blocks first
+  // work items in heavy-first order (query block rank slowest), dealt out
+  // round-robin to the persistent CTAs
   const int nblk = (a.s + 127) / 128;
-  const int per = gridDim.x / nblk;   // n_q · batch
-  const int rank = blockIdx.x / per, rem = blockIdx.x % per;
-  const int b = rem / a.nq, j = rem % a.nq;
-  const int q0 = (nblk - 1 - rank) * 128;
-  const int kvh = j / (a.nq / a.nkv);
-  const int kv_end = a.causal ? min(a.s, q0 + 128) : a.s;
-  const int nkb = (kv_end + 127) / 128;
+  const int group = a.nq / a.nkv;
+  const int per = a.hkn * group;   // q heads of this pass
+  const int items = nblk * per;
+  auto decode = [&](int t, int& bb, int& jq, int& lh, int& qb, int& nkb) {
+    const int rank = t / per;
+    lh = t % per;
+    const int pair = a.hk0 + lh / group;
+    bb = pair / a.nkv;
+    jq = (pair % a.nkv) * group + lh % group;
+    qb = nblk - 1 - rank;
+    nkb = a.causal ? qb + 1 : nblk;
+  };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 256);
-    for (int i = 0; i < NK; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < NV; ++i) {
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
-    }
-    mbar_init(sdp_full, 1);
-    mbar_init(sdp_free, 256);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ds_full[i], 256);
-      mbar_init(&ds_free[i], 1);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
     }
-    mbar_init(dq_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 1) tmem_alloc(tmem_slot, NCOLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane < 2) {
-      // lane 0: the K ring (K_j is freed after dQ += dS_j·K_j);
-      // lane 1: the V ring (V_j is freed as soon as dP_j is done)
-      const bool is_k = lane == 0;
-      const CUtensorMap* map = is_k ? &a.mk : &a.mv;
-      uint64_t* full = is_k ? k_full : v_full;
-      uint64_t* empty = is_k ? k_empty : v_empty;
-      uint8_t* ring = sm + (is_k ? OFF_K : OFF_V);
-      const int depth = is_k ? NK : NV;
-      tma_prefetch_desc(map);
-      uint32_t armed = 0, armed_par = 0;
-      for (int jb = 0; jb < nkb; ++jb) {
-        const int st = jb % depth;
-        const uint32_t ph = (jb / depth) & 1;
-        if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, a.status, 31)) break;
-        mbar_arrive_expect_tx(&full[st], TILE);
-        armed |= 1u << st;
-        armed_par = (armed_par & ~(1u << st)) | (ph << st);
-        for (int hh = 0; hh < 2; ++hh)
-          tma_load_3d(ring + st * TILE + hh * A128, map, &full[st],
-                      kvh * HD + hh * 64, jb * 128, b);
+    if (lane == 0) {
+      // ------------------------------------------------------------- TMA --
+      tma_prefetch_desc(&a.mk);
+      uint32_t st = 0, ph = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < items; t += gridDim.x) {
+        int bb, jq, lh, qb, nkb;
+        decode(t, bb, jq, lh, qb, nkb);
+        const int kvh = jq / group;
+        const uint8_t* src = a.ds + ds_tile(a, lh, qb, 0, nblk) * TILE;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, a.status, 31)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], 2 * TILE);
+          armed |= 1u << st;
+          armed_par = (armed_par & ~(1u << st)) | (ph << st);
+          bulk_load(sm + OFF_DS + st * TILE, src + (int64_t)kb * TILE, TILE,
+                    &full[st]);
+          for (int hh = 0; hh < 2; ++hh)
+            tma_load_3d(sm + OFF_K + st * TILE + hh * A128, &a.mk, &full[st],
+                        kvh * HD + hh * 64, kb * 128, bb);
+          if (++st == NS) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
-        for (int st = 0; st < depth; ++st)
-          if (armed & (1u << st))
-            mbar_wait(&full[st], (armed_par >> st) & 1u, &no_abort, nullptr, 0);
+        for (int i = 0; i < NS; ++i)
+          if (armed & (1u << i))
+            mbar_wait(&full[i], (armed_par >> i) & 1u, &no_abort, nullptr, 0);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_f16_f32(128, 128, 0, 0);
-      constexpr uint32_t IDESC_Q = idesc_f16_f32(128, 128, 0, 1);
-      bool ok = mbar_wait(q_full, 0, abort_flag, a.status, 32);
-      tc_fence_after();
-      auto sdp_mma = [&](int jb) -> bool {
-        if (!mbar_wait(&k_full[jb % NK], (jb / NK) & 1, abort_flag, a.status,
-                       34) ||
-            !mbar_wait(&v_full[jb % NV], (jb / NV) & 1, abort_flag, a.status,
-                       39))
-          return false;
-        tc_fence_after();
-        const uint32_t sK = smem_u32(sm + OFF_K + (jb % NK) * TILE);
-        const uint32_t sV = smem_u32(sm + OFF_V + (jb % NV) * TILE);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          tc_mma_f16_ts(tmem + COL_S, tmem + COL_Q + kk * 8,
-                        dk128(sK, kk, A128), IDESC_S, kk > 0 ? 1u : 0u);
-          tc_mma_f16_ts(tmem + COL_DP, tmem + COL_DO + kk * 8,
-                        dk128(sV, kk, A128), IDESC_S, kk > 0 ? 1u : 0u);
+      // ------------------------------------------------------------- MMA --
+      // D[q][d] += Σ_key dSᵀ[key][q] · K[key][d]: both operands have the
+      // key (the reduction) as their row, so A is M-major and B N-major
+      constexpr uint32_t IDESC = idesc_f16_f32(128, 128, 1, 1);
+      uint32_t st = 0, ph = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = blockIdx.x; ok && t < items; t += gridDim.x, ++it) {
+        int bb, jq, lh, qb, nkb;
+        decode(t, bb, jq, lh, qb, nkb);
+        const int buf = it & 1;
+        if (!mbar_wait(&tempty[buf], ((it >> 1) & 1) ^ 1, abort_flag,
+                       a.status, 32)) {
+          ok = false;
+          break;
         }
-        tc_commit(sdp_full);
-        tc_commit(&v_empty[jb % NV]);
-        return true;
-      };
-      auto dq_mma = [&](int i) -> bool {
-        const int bb = i & 1;
-        if (!mbar_wait(&ds_full[bb], (i >> 1) & 1, abort_flag, a.status, 33))
-          return false;
         tc_fence_after();
-        const uint32_t sK = smem_u32(sm + OFF_K + (i % NK) * TILE);
-        const uint32_t sdS = smem_u32(sm + OFF_DS + bb * TILE);
+        const uint32_t d_tmem = tmem + buf * 128;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full[st], ph, abort_flag, a.status, 33)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sdS = smem_u32(sm + OFF_DS + st * TILE);
+          const uint32_t sK = smem_u32(sm + OFF_K + st * TILE);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem + COL_DQ, dk128(sdS, kk, A128), dmn(sK, kk, A128),
-                     IDESC_Q, (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&ds_free[bb]);
-        tc_commit(&k_empty[i % NK]);
-        return true;
-      };
-      // S_{j+1}, dP_{j+1} go in as soon as S_j, dP_j are in registers, ahead
-      // of dQ += dS_j·K_j, so the elementwise warps never wait on dQ.
-      if (ok) ok = sdp_mma(0);
-      for (int jb = 0; ok && jb < nkb; ++jb) {
-        ok = mbar_wait(sdp_free, jb & 1, abort_flag, a.status, 35);
-        if (ok && jb + 1 < nkb) ok = sdp_mma(jb + 1);
-        if (ok) ok = dq_mma(jb);
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_f16(d_tmem, dmn(sdS, kk, A128), dmn(sK, kk, A128), IDESC,
+                       (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[st]);
+          if (++st == NS) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (ok) tc_commit(&tfull[buf]);
       }
-      if (ok) tc_commit(dq_done);
       if (*abort_flag) {
         volatile int no_abort = 0;
         tc_commit(drain);
@@ -338,93 +345,43 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else {
-    // ------------------------------------------------------ elementwise --
-    // thread: query row r (TMEM lane), keys [64·half, 64·half + 64) of each
-    // block
-    const int half = (warp - 2) >> 2;
+    // -------------------------------------------------------- epilogue --
+    // thread: query row of the block (TMEM lane), all 128 columns of dQ
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const int qi = q0 + r;
-    const uint32_t lanes = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int64_t srow = ((int64_t)b * a.nq + j) * a.s_pad + qi;
-    const float l2 = a.L2p[srow], dd = a.Dp[srow];
-    const float c = a.scale_log2;
-    {
-      // this thread's half row of Q and of dO into TMEM (zeros past the end)
-      const int64_t off =
-          ((int64_t)b * a.s + qi) * (int64_t)(a.nq * HD) + j * HD + half * 64;
-      uint32_t qv[32];
-      const __half* const srcs[2] = {a.q, a.dout};
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const uint4* src = reinterpret_cast<const uint4*>(srcs[t] + off);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 u = qi < a.s ? src[i] : make_uint4(0u, 0u, 0u, 0u);
-          qv[4 * i] = u.x;
-          qv[4 * i + 1] = u.y;
-          qv[4 * i + 2] = u.z;
-          qv[4 * i + 3] = u.w;
-        }
-        tmem_st32(lanes + (t == 0 ? COL_Q : COL_DO) + half * 32, qv);
+    const int row = quarter * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < items; t += gridDim.x, ++it) {
+      int bb, jq, lh, qb, nkb;
+      decode(t, bb, jq, lh, qb, nkb);
+      const int buf = it & 1;
+      if (!mbar_wait_warp(&tfull[buf], (it >> 1) & 1, abort_flag, a.status,
+                          38))
+        break;
+      tc_fence_after();
+      const int qi = qb * 128 + row;
+      const uint32_t lanes = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             buf * 128;
+      __nv_bfloat16* dst = a.out0 +
+                           ((int64_t)bb * a.s + qi) * (int64_t)(a.nq * HD) +
+                           jq * HD;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(lanes + hh * 64, o0);
+        tmem_ld32(lanes + hh * 64 + 32, o1);
+        tmem_ld_wait(o0);
+        reg_fence32(o1);
+        if (qi < a.s) store_bf16_row64(dst + hh * 64, o0, o1, a.scale);
       }
       tc_fence_before();
-      mbar_arrive(q_full);
-    }
-    bool ok = true;
-    for (int jb = 0; jb < nkb; ++jb) {
-      const int bb = jb & 1;
-      if (!mbar_wait_warp(sdp_full, jb & 1, abort_flag, a.status, 36)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t s0[32], s1[32], p0[32], p1[32];
-      tmem_ld32(lanes + COL_S + half * 64, s0);
-      tmem_ld32(lanes + COL_S + half * 64 + 32, s1);
-      tmem_ld32(lanes + COL_DP + half * 64, p0);
-      tmem_ld32(lanes + COL_DP + half * 64 + 32, p1);
-      tmem_ld_wait(s0);
-      reg_fence32(s1);
-      reg_fence32(p0);
-      reg_fence32(p1);
-      tc_fence_before();
-      mbar_arrive(sdp_free);
-      // keys past the end need no mask: their K rows are zero, so they add
-      // nothing to dS·K; on the causal diagonal keep keys ≤ the query
-      uint32_t pk[32];
-      ds_chunk(s0, p0, c, l2, dd, pk);
-      ds_chunk(s1, p1, c, l2, dd, pk + 16);
-      if (a.causal && jb * 128 == q0) keep_upto(pk, r - half * 64);
-      // the dS buffer is free once dQ += dS_{j-2}·K_{j-2} has completed
-      if (jb >= 2 && !mbar_wait_warp(&ds_free[bb], ((jb - 2) >> 1) & 1,
-                                     abort_flag, a.status, 37)) {
-        ok = false;
-        break;
-      }
-      st_row8(sm + OFF_DS + bb * TILE + half * A128, r, pk);
-      fence_proxy_async_smem();
-      mbar_arrive(&ds_full[bb]);
-    }
-    if (__all_sync(0xffffffffu, ok) &&
-        mbar_wait_warp(dq_done, 0, abort_flag, a.status, 38)) {
-      tc_fence_after();
-      uint32_t o0[32], o1[32];
-      tmem_ld32(lanes + COL_DQ + half * 64, o0);
-      tmem_ld32(lanes + COL_DQ + half * 64 + 32, o1);
-      tmem_ld_wait(o0);
-      reg_fence32(o1);
-      if (qi < a.s)
-        store_bf16_row64(a.out0 + ((int64_t)b * a.s + qi) * (int64_t)(a.nq * HD) +
-                             j * HD + half * 64,
-                         o0, o1, a.scale);
+      mbar_arrive(&tempty[buf]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem, NCOLS);
 }
 
 // ------------------------------------------------------------------ dK, dV --
@@ -467,7 +424,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* p_full = x_free + 1;       // Pᵀ written
   uint64_t* p_free = p_full + 1;       // dV += Pᵀ·dO done with it
   uint64_t* ds_full = p_free + 1;      // dSᵀ written
-  uint64_t* ds_free = ds_full + 1;     // dK += dSᵀ·Q done with it
+  uint64_t* ds_free = ds_full + 1;     // dK += dSᵀ·Q and its copy out done
   uint64_t* done = ds_free + 1;
   uint64_t* drain = done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -478,9 +435,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   // mask) key blocks of every kv head start first; in (kv head, key block)
   // order the last heads' heavy blocks would start late and set the tail
   const int nblk = (a.s + 127) / 128;
-  const int per = gridDim.x / nblk;   // n_kv · batch
+  const int per = a.hkn;              // (batch, kv head) pairs of this pass
   const int rank = blockIdx.x / per, rem = blockIdx.x % per;
-  const int b = rem / a.nkv, kvh = rem % a.nkv;
+  const int b = (a.hk0 + rem) / a.nkv, kvh = (a.hk0 + rem) % a.nkv;
   const int k0 = rank * 128;
   const int group = a.nq / a.nkv;
   const int nqb = (a.s + 127) / 128;
@@ -503,7 +460,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(p_full, 256);
     mbar_init(p_free, 1);
     mbar_init(ds_full, 256);
-    mbar_init(ds_free, 1);
+    mbar_init(ds_free, 2);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -550,6 +507,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (armed & (1u << st))
             mbar_wait(&full[st], (armed_par >> st) & 1u, &no_abort, nullptr, 0);
       }
+    } else if (lane == 2) {
+      // each dSᵀ tile out to global memory for the dQ kernel; the buffer is
+      // released (second arrival on ds_free) once the copy has read it
+      for (int it = 0; it < iters; ++it) {
+        if (!mbar_wait(ds_full, it & 1, abort_flag, a.status, 54)) break;
+        const int qb = qb_first + it % per_head;
+        bulk_store(a.ds + ds_tile(a, rem * group + it / per_head, qb, rank,
+                                  nblk) *
+                              TILE,
+                   sm + OFF_DS, TILE);
+        bulk_wait_read();
+        mbar_arrive(ds_free);
+      }
+      bulk_wait_all();
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -657,9 +628,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int it = 0; it < iters; ++it) {
       const int qb = qb_first + it % per_head;
-      // queries past the end have L2 = +∞ (P = 0); keys past the end feed
-      // only dK, dV rows that are never stored; the causal diagonal block
-      // keeps queries ≥ the key
+      // queries past the end have L2 = +∞ (P = 0); keys past the end get
+      // P = 0 (their dSᵀ rows go to the dQ kernel); the causal diagonal
+      // block keeps queries ≥ the key
       const bool diag = a.causal && qb * 128 == k0;
       // Sᵀ → P, kept in fp16
       if (!mbar_wait_warp(x_full, 0, abort_flag, a.status, 46)) {
@@ -695,6 +666,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (diag) keep_from(pp, r - half * 64);
+      const uint32_t kmask = key < a.s ? 0xffffffffu : 0u;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pp[i] &= kmask;
       // Pᵀ(it) out now: the tile is free once dV of it−1 has completed
       if (it >= 1 &&
           !mbar_wait_warp(p_free, (it - 1) & 1, abort_flag, a.status, 47)) {
@@ -773,10 +747,30 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 int64_t attn_stats_pad(int64_t s) { return (s + 127) / 128 * 128; }
 
+namespace {
+// dSᵀ tiles of one (batch, kv head) pair: its GQA group's q heads
+int64_t ds_pair_bytes(const AttnShape& sh) {
+  const int64_t nblk = (sh.s + 127) / 128;
+  const int64_t per_head = sh.causal ? nblk * (nblk + 1) / 2 : nblk * nblk;
+  return (int64_t)(sh.nq / sh.nkv) * per_head * (int64_t)dq::TILE;
+}
+// (batch, kv head) pairs per pass: as many as fit in kDsBudget bytes of
+// tiles (at least one), so the scratch stays bounded for long sequences
+constexpr int64_t kDsBudget = int64_t(8) << 30;
+int64_t ds_pairs_per_pass(const AttnShape& sh) {
+  return std::max<int64_t>(
+      1, std::min<int64_t>(sh.b * sh.nkv, kDsBudget / ds_pair_bytes(sh)));
+}
+}  // namespace
+
+int64_t attn_ds_bytes(const AttnShape& sh) {
+  return ds_pairs_per_pass(sh) * ds_pair_bytes(sh);
+}
+
 int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
               const void* O, const void* dO, const float* LSE, float* Dp,
-              float* L2p, void* dQ, void* dK, void* dV, unsigned* status,
-              void* stream) {
+              float* L2p, void* dS, void* dQ, void* dK, void* dV,
+              unsigned* status, void* stream) {
   if (sh.d != HD) return cudaErrorInvalidValue;
   static cudaError_t e1 = cudaFuncSetAttribute(
       attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -786,12 +780,15 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
       dkv::SMEM);
   if (e1 != cudaSuccess) return e1;
   if (e2 != cudaSuccess) return e2;
+  if (reinterpret_cast<uintptr_t>(dS) & 15u) return cudaErrorInvalidValue;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t s_pad = attn_stats_pad(sh.s);
   const double sd = (double)sh.s;
   const double pairs = sh.causal ? sd * (sd + 1.0) / 2.0 : sd * sd;
   const double core = 4.0 * sh.b * sh.nq * HD * pairs;
   const double io = 2.0 * sh.b * sh.s * HD;
+  const double ds_bytes_all =
+      (double)ds_pair_bytes(sh) * (double)(sh.b * sh.nkv);
   {
     const int64_t warps = sh.b * sh.nq * s_pad;
     ProfScope ps(stream, KF_ELEMENTWISE, 2.0 * sh.b * sh.s * sh.nq * HD,
@@ -822,6 +819,7 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   a.v = static_cast<const __half*>(V);
   a.Dp = Dp;
   a.L2p = L2p;
+  a.ds = static_cast<uint8_t*>(dS);
   a.s = (int)sh.s;
   a.s_pad = (int)s_pad;
   a.nq = sh.nq;
@@ -830,22 +828,39 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   a.scale = sh.scale;
   a.scale_log2 = sh.scale * LOG2E_F;
   a.status = status;
-  a.out0 = static_cast<__nv_bfloat16*>(dQ);
-  {
-    const unsigned grid = (unsigned)(((sh.s + 127) / 128) * sh.nq * sh.b);
-    ProfScope ps(stream, KF_ATTN_BWD_DQ, 0.5 * core,
-                 io * (3.0 * sh.nq + 2.0 * sh.nkv));
-    attn_bwd_dq_tc_kernel<<<grid, THREADS, dq::SMEM, s>>>(a);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  sms = std::max(sms, 1);
+  const int64_t pairs_all = sh.b * sh.nkv;
+  const int64_t chunk = ds_pairs_per_pass(sh);
+  const int64_t nblk = (sh.s + 127) / 128;
+  const int group = sh.nq / sh.nkv;
+  int passes = 0;
+  for (int64_t hk0 = 0; hk0 < pairs_all; hk0 += chunk, ++passes) {
+    const int64_t hkn = std::min(chunk, pairs_all - hk0);
+    const double frac = (double)hkn / (double)pairs_all;
+    a.hk0 = (int)hk0;
+    a.hkn = (int)hkn;
+    a.out0 = static_cast<__nv_bfloat16*>(dK);
+    a.out1 = static_cast<__nv_bfloat16*>(dV);
+    {
+      ProfScope ps(stream, KF_ATTN_BWD_DKDV, 1.5 * core * frac,
+                   (io * (2.0 * sh.nq + 4.0 * sh.nkv) + ds_bytes_all) * frac);
+      attn_bwd_dkdv_tc_kernel<<<(unsigned)(nblk * hkn), THREADS, dkv::SMEM,
+                                s>>>(a);
+    }
+    a.out0 = static_cast<__nv_bfloat16*>(dQ);
+    a.out1 = nullptr;
+    {
+      const int64_t items = nblk * hkn * group;
+      ProfScope ps(stream, KF_ATTN_BWD_DQ, 0.5 * core * frac,
+                   (ds_bytes_all + io * sh.nq) * frac);
+      attn_bwd_dq_tc_kernel<<<(unsigned)std::min<int64_t>(items, sms),
+                              dq::NTHREADS, dq::SMEM, s>>>(a);
+    }
   }
-  a.out0 = static_cast<__nv_bfloat16*>(dK);
-  a.out1 = static_cast<__nv_bfloat16*>(dV);
-  {
-    const unsigned grid = (unsigned)(((sh.s + 127) / 128) * sh.nkv * sh.b);
-    ProfScope ps(stream, KF_ATTN_BWD_DKDV, 1.5 * core,
-                 io * (2.0 * sh.nq + 4.0 * sh.nkv));
-    attn_bwd_dkdv_tc_kernel<<<grid, THREADS, dkv::SMEM, s>>>(a);
-  }
-  count_launch(3);
+  count_launch(1 + 2 * passes);
   return cudaGetLastError();
 }
 
