@@ -175,6 +175,13 @@ size_t tp_attn_workspace_bytes(const tp_attn_desc* d);
  * 128×128 tiles (b·n_q·B(B+1)/2 tiles causal, b·n_q·B² full, B = ⌈s/128⌉;
  * 32 KB each), partials and column-sum partials. */
 size_t tp_attn_bwd_scratch_bytes(const tp_attn_desc* d);
+/* Upper bound, in bytes, on the dS tiles held at once: the backward runs in
+ * passes over (batch, kv head) pairs, as many per pass as fit (at least
+ * one), so the scratch stays bounded for long sequences.  bytes = 0 restores
+ * the default (8 GiB).  Returns the previous bound.  Host only; it changes
+ * what tp_attn_bwd_scratch_bytes returns, so query the scratch size after
+ * setting it.  Results do not depend on it (each pair's work is the same). */
+size_t tp_attn_set_ds_budget(size_t bytes);
 
 tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X, const void* Wq,
                       const void* Wk, const void* Wv, const void* Wo,

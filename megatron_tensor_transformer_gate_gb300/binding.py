@@ -95,6 +95,7 @@ SIGNATURES = {
                           _P, _SZ, _P]),
     "tp_attn_workspace_bytes": (_SZ, [_AP]),
     "tp_attn_bwd_scratch_bytes": (_SZ, [_AP]),
+    "tp_attn_set_ds_budget": (_SZ, [_SZ]),
     "tp_attn_fwd": (_I32, [_AP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "tp_attn_bwd": (_I32, [_AP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                            _P, _P, _P, _P, _SZ, _P]),
@@ -274,6 +275,12 @@ def attn_workspace_bytes(desc):
 
 def attn_bwd_scratch_bytes(desc):
     return lib().tp_attn_bwd_scratch_bytes(ctypes.byref(desc))
+
+
+def attn_set_ds_budget(nbytes):
+    """Bound on the attention backward's dS tile bytes per pass (0 = the
+    default); returns the previous bound."""
+    return lib().tp_attn_set_ds_budget(nbytes)
 
 
 def attn_fwd(desc, X, Wq, Wk, Wv, Wo, Out, ws, bo=None, R=None, stream=None):

@@ -1067,6 +1067,11 @@ extern "C" const char* tp_status_string(tp_status s) {
 
 extern "C" uint64_t tp_launch_count(void) { return g_launches.load(); }
 
+extern "C" size_t tp_attn_set_ds_budget(size_t bytes) {
+  return (size_t)attn_set_ds_budget(
+      bytes > (size_t)INT64_MAX ? INT64_MAX : (int64_t)bytes);
+}
+
 extern "C" int32_t tp_num_sms(void) {
   int n = 0;
   if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) return 0;

@@ -25,6 +25,9 @@ int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
 // gradient tiles that the dK/dV kernel writes and the dQ kernel reads.
 int64_t attn_stats_pad(int64_t s);
 int64_t attn_ds_bytes(const AttnShape& sh);
+// Bound on the dS tile bytes per pass (0 = the default 8 GiB); returns the
+// previous bound.
+int64_t attn_set_ds_budget(int64_t bytes);
 int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
               const void* O, const void* dO, const float* LSE, float* Dp,
               float* L2p, void* dS, void* dQ, void* dK, void* dV,

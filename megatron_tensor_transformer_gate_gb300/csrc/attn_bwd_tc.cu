@@ -43,6 +43,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "attention.h"
@@ -754,14 +755,20 @@ int64_t ds_pair_bytes(const AttnShape& sh) {
   const int64_t per_head = sh.causal ? nblk * (nblk + 1) / 2 : nblk * nblk;
   return (int64_t)(sh.nq / sh.nkv) * per_head * (int64_t)dq::TILE;
 }
-// (batch, kv head) pairs per pass: as many as fit in kDsBudget bytes of
-// tiles (at least one), so the scratch stays bounded for long sequences
-constexpr int64_t kDsBudget = int64_t(8) << 30;
+// (batch, kv head) pairs per pass: as many as fit in the budget of tile
+// bytes (at least one), so the scratch stays bounded for long sequences
+constexpr int64_t kDsBudgetDefault = int64_t(8) << 30;
+std::atomic<int64_t> g_ds_budget{kDsBudgetDefault};
 int64_t ds_pairs_per_pass(const AttnShape& sh) {
   return std::max<int64_t>(
-      1, std::min<int64_t>(sh.b * sh.nkv, kDsBudget / ds_pair_bytes(sh)));
+      1, std::min<int64_t>(sh.b * sh.nkv,
+                           g_ds_budget.load() / ds_pair_bytes(sh)));
 }
 }  // namespace
+
+int64_t attn_set_ds_budget(int64_t bytes) {
+  return g_ds_budget.exchange(bytes > 0 ? bytes : kDsBudgetDefault);
+}
 
 int64_t attn_ds_bytes(const AttnShape& sh) {
   return ds_pairs_per_pass(sh) * ds_pair_bytes(sh);

@@ -190,3 +190,22 @@ def test_act_memory_rejects(tp):
     with pytest.raises(tp.TPError) as e:
         tp.act_memory(1, 64, 128, 512, 2, 2, 64, 2, dtype=7)
     assert e.value.code == 3
+
+
+@pytest.mark.parametrize("causal,tiles", [(True, 3), (False, 4)])
+def test_ds_budget_sets_the_tile_scratch(tp, causal, tiles):
+    # b=2, n_kv=2: four (batch, kv head) pairs, each with its group of 4 q
+    # heads × (causal 3 | full 4) tiles of 128×128 fp16 (s=200: 2 blocks)
+    d = tp.attn_desc(2, 200, 512, 8, 2, 128, 2, causal=causal)
+    pair = 4 * tiles * 128 * 128 * 2
+    prev = tp.attn_set_ds_budget(0)
+    try:
+        whole = tp.attn_bwd_scratch_bytes(d)
+        assert tp.attn_set_ds_budget(1) == 8 << 30
+        one = tp.attn_bwd_scratch_bytes(d)
+        tp.attn_set_ds_budget(2 * pair)
+        two = tp.attn_bwd_scratch_bytes(d)
+    finally:
+        tp.attn_set_ds_budget(prev)
+    assert whole - one == 3 * pair
+    assert whole - two == 2 * pair

@@ -98,3 +98,30 @@ def test_overlapped_reduction_attention_workload(tp):
         res.append([out.clone(), g["dX"].clone()])
     for u, v in zip(*res):
         assert u.equal(v)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_in_passes_is_bit_identical(tp, causal):
+    # a dS budget below one (batch, kv head) pair's tiles runs the backward
+    # in one pass per pair (4 here): smaller scratch, identical results
+    cfg = I.workload("attn_gqa_bf16", b=2, s=200, h=512, n_q=8, n_kv=2, n=2,
+                     causal=causal, w_std="fan_in")
+    x = I.attn_inputs(cfg, 34, "cuda")
+    res, scratch = [], []
+    for budget in (0, 1):
+        prev = tp.attn_set_ds_budget(budget)
+        try:
+            a = TPAttention(cfg["b"], cfg["s"], cfg["h"], cfg["n_q"],
+                            cfg["n_kv"], cfg["d"], cfg["n"], causal=causal)
+            scratch.append(tp.attn_bwd_scratch_bytes(a.desc))
+            out = a.forward(x["X"], x["Wq"], x["Wk"], x["Wv"], x["Wo"])
+            g = a.backward(x["dOut"], x["X"], x["Wq"], x["Wk"], x["Wv"],
+                           x["Wo"])
+            tp.device_status()
+            res.append([out.clone()] + [g[k].clone() for k in
+                                        ("dX", "dWq", "dWk", "dWv", "dWo")])
+        finally:
+            tp.attn_set_ds_budget(prev)
+    assert scratch[1] < scratch[0]
+    for u, v in zip(*res):
+        assert u.equal(v)
