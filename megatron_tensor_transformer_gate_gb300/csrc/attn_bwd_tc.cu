@@ -28,10 +28,11 @@
 // dQ kernel is bound by reading the tiles.
 // dK/dV: warp 0 TMA (+ one thread for the dSᵀ copies), warp 1 TMEM
 // allocation + single-thread MMA issue, warps 2–9 elementwise (two threads
-// per TMEM lane, half of the columns each).  The score MMAs of the next
-// block are issued as soon as the elementwise warps have copied the current
-// scores to registers, ahead of the gradient MMAs, so the tensor cores work
-// while the elementwise warps do.  The elementwise loops are unrolled but
+// per TMEM lane, half of the columns each).  The MMAs go in the order
+// Sᵀ(i), dK(i−1), dPᵀ(i), dV(i): the score products of a block are issued as
+// soon as the elementwise warps have copied the previous contents of X to
+// registers, and dK(i−1) keeps the tensor cores busy while they copy Sᵀ(i)
+// out, so the tensor cores work while the elementwise warps do.  The elementwise loops are unrolled but
 // branch-free (masks come from padding and a fix-up of the causal diagonal
 // on packed words): a per-block body that outgrows the instruction cache
 // runs several times slower.  Q and dO stream through rings of their own,
@@ -557,9 +558,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_commit(&q_empty[i % NQ]);
         return true;
       };
-      // per block: Sᵀ(it); dPᵀ(it) as soon as Sᵀ(it) is in registers; dK of
-      // it−1 (its dSᵀ was written while Sᵀ(it) ran); dV of it (Pᵀ(it) is
-      // written while dPᵀ(it) and dK(it−1) run)
+      // per block: Sᵀ(it); dK of it−1 (its dSᵀ was written while Sᵀ(it)
+      // ran), which keeps the tensor cores busy while the elementwise warps
+      // copy Sᵀ(it) out of the shared X buffer; dPᵀ(it) into X once they
+      // have; dV of it (Pᵀ(it) is written while dK(it−1) and dPᵀ(it) run)
       for (int it = 0; ok && it < iters; ++it) {
         ok = mbar_wait(&q_full[it % NQ], (it / NQ) & 1, abort_flag, a.status,
                        44) &&
@@ -572,6 +574,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_mma_f16_ts(tmem + COL_X, tmem + COL_K + kk * 8,
                         dk128(sQ, kk, A128), IDESC_S, kk > 0 ? 1u : 0u);
         tc_commit(x_full);
+        if (it > 0 && !(ok = dk_mma(it - 1))) break;
         ok = mbar_wait(&o_full[it % NO], (it / NO) & 1, abort_flag, a.status,
                        49) &&
              mbar_wait(x_free, 0, abort_flag, a.status, 50);
@@ -583,7 +586,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_mma_f16_ts(tmem + COL_X, tmem + COL_V + kk * 8,
                         dk128(sdO, kk, A128), IDESC_S, kk > 0 ? 1u : 0u);
         tc_commit(x_full);
-        if (it > 0 && !(ok = dk_mma(it - 1))) break;
         if (!(ok = dv_mma(it))) break;
       }
       if (ok && iters > 0) ok = dk_mma(iters - 1);
