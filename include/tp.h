@@ -372,6 +372,9 @@ tp_status tp_profile_read(int32_t family, tp_profile_entry* out);
  * stream failed. */
 tp_status tp_device_status(tp_stream stream);
 const char* tp_status_string(tp_status s);
+/* The CUDA runtime error code behind the latest TP_ERR_CUDA (0 if none
+ * yet) and, when name is not NULL, its name (a static string). */
+int32_t tp_last_cuda_error(const char** name);
 /* Number of kernels this library has launched since load (host counter). */
 uint64_t tp_launch_count(void);
 /* SM count of the current device (0 if none); cached per device. */

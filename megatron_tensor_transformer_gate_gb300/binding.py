@@ -24,9 +24,9 @@ STATUS = {0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_DTYPE",
 
 
 class TPError(RuntimeError):
-    def __init__(self, code, where):
+    def __init__(self, code, where, detail=""):
         self.code = code
-        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        super().__init__(f"{where}: {STATUS.get(code, code)}{detail}")
 
 
 class MlpDesc(ctypes.Structure):
@@ -122,6 +122,7 @@ SIGNATURES = {
     "tp_device_status": (_I32, [_P]),
     "tp_status_string": (ctypes.c_char_p, [_I32]),
     "tp_launch_count": (_U64, []),
+    "tp_last_cuda_error": (_I32, [ctypes.POINTER(ctypes.c_char_p)]),
     "tp_num_sms": (_I32, []),
 }
 
@@ -147,7 +148,12 @@ def lib():
 
 def check(code, where):
     if code != 0:
-        raise TPError(code, where)
+        detail = ""
+        if code == 6:   # TP_ERR_CUDA: name the CUDA error behind it
+            name = ctypes.c_char_p()
+            err = lib().tp_last_cuda_error(ctypes.byref(name))
+            detail = f" ({err}: {(name.value or b'').decode()})"
+        raise TPError(code, where, detail)
 
 
 def ptr(t):

@@ -124,8 +124,12 @@ bool opt_aligned(const void* p) { return p == nullptr || aligned16(p); }
 
 size_t elem_size(int32_t dtype) { return dtype == TP_F32 ? 4 : 2; }
 
+std::atomic<int> g_last_cuda_error{0};
+
 tp_status cuda_status(int err) {
-  return err == 0 ? TP_OK : TP_ERR_CUDA;
+  if (err == 0) return TP_OK;
+  g_last_cuda_error.store(err);
+  return TP_ERR_CUDA;
 }
 
 DropoutSpec make_dropout(float p, uint64_t seed) {
@@ -1066,6 +1070,13 @@ extern "C" const char* tp_status_string(tp_status s) {
 }
 
 extern "C" uint64_t tp_launch_count(void) { return g_launches.load(); }
+
+extern "C" int32_t tp_last_cuda_error(const char** name) {
+  const int e = g_last_cuda_error.load();
+  if (name != nullptr)
+    *name = cudaGetErrorName(static_cast<cudaError_t>(e));
+  return e;
+}
 
 extern "C" size_t tp_attn_set_ds_budget(size_t bytes) {
   return (size_t)attn_set_ds_budget(
