@@ -56,7 +56,7 @@ def test_quantize_all_zero_tensor(tp):
 
 @pytest.mark.parametrize("M,N,K", [(8, 16, 16), (256, 256, 128),
                                    (300, 520, 208), (1000, 1000, 1024),
-                                   (513, 384, 4096)])
+                                   (513, 384, 4096), (2500, 2000, 256)])
 def test_gemm_fp8_parity(tp, M, N, K):
     A, Bm = seeded((M, K), 11), seeded((N, K), 12, 0.05)
     qa, sa = gpu_quantize(tp, A)

@@ -79,3 +79,23 @@ def test_gemm_rejects_unaligned_leading_dim(tp):
     with pytest.raises(tp.TPError) as e:
         tp.gemm(A, Bm, C, a_mn_major=True)
     assert e.value.code == 2
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("M,N,K", [(2560, 2048, 192), (2504, 2000, 200)])
+def test_gemm_partial_last_wave(tp, a_mn, b_mn, M, N, K):
+    # 10 × 8 = 80 pair tiles: one full wave of the ≤ 76 resident pairs and a
+    # last wave of a few tiles (the second shape also ragged in M, N and K)
+    g = torch.Generator().manual_seed(M + N + K + 2 * a_mn + b_mn)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    Bm = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    ref = f64(A) @ f64(Bm).T
+    dA = (A.t().contiguous() if a_mn else A).cuda()
+    dB = (Bm.t().contiguous() if b_mn else Bm).cuda()
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tp.gemm(dA, dB, C, a_mn_major=bool(a_mn), b_mn_major=bool(b_mn))
+    tp.device_status()
+    got = f64(C)
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= 8e-3 * np.abs(ref).max() + 1e-3, err

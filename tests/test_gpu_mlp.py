@@ -163,3 +163,13 @@ def test_overlapped_reduction_equals_materialised(tp):
                                                              "dW2", "db2")]
     for a, b in zip(res[tp.MATERIALISED], res[tp.OVERLAP]):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_partial_last_wave_in_the_mlp(tp, act):
+    # T 2560 × h_ffn 2048: the first projection (GeLU: 80 pair tiles;
+    # SwiGLU: 160) and the gradient GEMM with the activation backward in
+    # its epilogue (80) end in a partly filled wave
+    cfg = I.workload("mlp_gelu_bf16", b=1, s=2560, h=512, h_ffn=2048, n=2,
+                     act=act, b1=(act == "gelu"), p=0.0, w_std="fan_in")
+    run_case(tp, cfg, 0, 9)
