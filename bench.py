@@ -40,7 +40,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
 L2_BYTES = 129 * 1024 * 1024
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -55,7 +55,7 @@ def parse_args():
                     help="override s (smaller cases for profiler captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def load_peaks():
@@ -334,6 +334,23 @@ def dist_setup(args):
     return world, rank, local
 
 
+def slowest_rank_ms(ms, world, device):
+    """The largest of the ranks' step times; every rank receives it."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step, world, ms):
+    """Whole-job TFLOP/s: each of `world` replicas did flops_per_step in
+    the slowest rank's `ms` per step."""
+    return flops_per_step * world / (ms / 1e3) / 1e12
+
+
 def reference_arm(args, cfg, world, rank):
     """The oracle, as it stands, on the host cores (rank 0 only)."""
     if rank != 0:
@@ -503,11 +520,8 @@ def main():
                   "p95": step_times[min(len(step_times) - 1,
                                         int(0.95 * len(step_times)))],
                   "min": step_times[0], "max": step_times[-1]}
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = fl * world / (ms / 1e3) / 1e12
+    ms = slowest_rank_ms(ms, world, dev)
+    value = job_tflops(fl, world, ms)
 
     # ---- end to end: every step's activations come from pinned host memory
     # and its output and input gradient go back to pinned host memory.  A
@@ -569,12 +583,8 @@ def main():
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        ems = t0.elapsed_time(t1) / args.steps
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": fl * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+        ems = slowest_rank_ms(t0.elapsed_time(t1) / args.steps, world, dev)
+        e2e = {"value": job_tflops(fl, world, ems), "unit": "TFLOP/s",
                "ms_per_step": ems, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
                "pipeline": "copy stream: inputs of step k+1 in and results "
