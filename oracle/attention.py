@@ -53,14 +53,11 @@ def _check_heads(n_q, n_kv):
         raise ValueError("n_kv must divide n_q")
 
 
-def attention_forward(X, Wq, Wk, Wv, Wo, *, b, s, n_q, n_kv, d, causal=True,
-                      bo=None, R=None):
-    """Unsharded attention forward.  Returns Out, Q, K, V, O, LSE."""
+def attention_core(Q, K, V, *, b, s, n_q, n_kv, d, causal=True):
+    """softmax(mask(Q·Kᵀ/√d))·V per (batch, q head) with kv head
+    ⌊j·n_kv/n_q⌋; Q [T, n_q·d], K, V [T, n_kv·d].  Returns O [T, n_q·d] and
+    LSE [b, n_q, s]."""
     _check_heads(n_q, n_kv)
-    X = np.asarray(X, np.float64)
-    Q = X @ np.asarray(Wq, np.float64).T
-    K = X @ np.asarray(Wk, np.float64).T
-    V = X @ np.asarray(Wv, np.float64).T
     Qh, Kh, Vh = (_heads(Q, b, s, n_q, d), _heads(K, b, s, n_kv, d),
                   _heads(V, b, s, n_kv, d))
     group = n_q // n_kv
@@ -73,7 +70,19 @@ def attention_forward(X, Wq, Wk, Wv, Wo, *, b, s, n_q, n_kv, d, causal=True,
             P, lse = _probs(Qh[bi, :, j], Kh[bi, :, kv], scale, causal)
             O[bi, :, j] = P @ Vh[bi, :, kv]
             LSE[bi, j] = lse
-    Of = O.reshape(b * s, n_q * d)
+    return O.reshape(b * s, n_q * d), LSE
+
+
+def attention_forward(X, Wq, Wk, Wv, Wo, *, b, s, n_q, n_kv, d, causal=True,
+                      bo=None, R=None):
+    """Unsharded attention forward.  Returns Out, Q, K, V, O, LSE."""
+    _check_heads(n_q, n_kv)
+    X = np.asarray(X, np.float64)
+    Q = X @ np.asarray(Wq, np.float64).T
+    K = X @ np.asarray(Wk, np.float64).T
+    V = X @ np.asarray(Wv, np.float64).T
+    Of, LSE = attention_core(Q, K, V, b=b, s=s, n_q=n_q, n_kv=n_kv, d=d,
+                             causal=causal)
     Z = Of @ np.asarray(Wo, np.float64).T
     Out = Z if bo is None else Z + bo
     if R is not None:

@@ -131,3 +131,32 @@ def mlp_forward(X, W1, W2, *, act="swiglu", b1=None, b2=None, R=None, p=0.0,
     out["Out"] = _output(Z, b2, R, p, seed)
     out["scales"] = (sx, sw1, sa, sw2)
     return out
+
+
+def attention_forward(X, Wq, Wk, Wv, Wo, *, b, s, n_q, n_kv, d, causal=True,
+                      bo=None, R=None):
+    """The attention block's forward on the FP8 path: the Q, K, V
+    projections on quantized X and Wq, Wk, Wv (one scale per tensor), the
+    attention core in fp64 on those products, O stored in bf16 then
+    quantized, the output projection on quantized O and Wo, bias, residual.
+    Returns the dict of ``oracle.attention_forward`` (Q, K, V, O, LSE, Z,
+    Out) plus the six scales."""
+    from .attention import attention_core
+    qx, sx, _ = quantize(X)
+    xd = dequantize(qx, sx)
+    proj, scales = [], [sx]
+    for W in (Wq, Wk, Wv):
+        qw, sw, _ = quantize(W)
+        proj.append(xd @ dequantize(qw, sw).T)
+        scales.append(sw)
+    Q, K, V = proj
+    O, LSE = attention_core(Q, K, V, b=b, s=s, n_q=n_q, n_kv=n_kv, d=d,
+                            causal=causal)
+    qo, so, _ = quantize(round_bf16(O))
+    qwo, swo, _ = quantize(Wo)
+    Z = dequantize(qo, so) @ dequantize(qwo, swo).T
+    Out = Z if bo is None else Z + np.asarray(bo, np.float64)
+    if R is not None:
+        Out = Out + np.asarray(R, np.float64)
+    return {"Out": Out, "Q": Q, "K": K, "V": V, "O": O, "LSE": LSE, "Z": Z,
+            "scales": tuple(scales) + (so, swo)}

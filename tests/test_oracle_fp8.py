@@ -117,3 +117,43 @@ def test_fp8_mlp_forward_is_the_mlp_on_dequantized_operands():
     # one E4M3 step of A (relative 2^-4) per element
     d = np.abs(o["Z"] - ref["Z"]).max()
     assert d <= 2.0 ** -3 * np.abs(ref["A"]).sum(axis=1).max() * np.abs(W2).max()
+
+
+def test_fp8_attention_forward_is_attention_on_dequantized_operands():
+    # X and the weights take values ±2^-k·amax (exact in E4M3 after the
+    # per-tensor scale), so the projections and the attention core equal the
+    # plain oracle's exactly; the output projection quantizes O (bf16-rounded)
+    # and is within one E4M3 step of it per element
+    import oracle
+    rng = np.random.default_rng(6)
+    b, s, n_q, n_kv, d, h = 2, 5, 4, 2, 8, 16
+    pick = lambda shape, unit: (rng.choice([-1.0, -0.5, -0.25, 0.0, 0.25, 0.5,
+                                            1.0], size=shape) * unit)
+    X = pick((b * s, h), 1.0)
+    X[0, 0] = 1.0                                  # amax exactly 1
+    Wq, Wk, Wv = (pick((n * d, h), 1 / 16) for n in (n_q, n_kv, n_kv))
+    Wo = pick((h, n_q * d), 1 / 16)
+    for W in (Wq, Wk, Wv, Wo):
+        W[0, 0] = 1 / 16
+    kw = dict(b=b, s=s, n_q=n_q, n_kv=n_kv, d=d, causal=True)
+    o = fp8.attention_forward(X, Wq, Wk, Wv, Wo, **kw)
+    ref = oracle.attention_forward(X, Wq, Wk, Wv, Wo, **kw)
+    for k in ("Q", "K", "V", "O", "LSE"):
+        assert np.array_equal(o[k], ref[k]), k
+    assert o["scales"][0] == np.float32(448.0)
+    bound = 2.0 ** -3 * np.abs(ref["O"]).sum(axis=1).max() * np.abs(Wo).max()
+    assert np.abs(o["Z"] - ref["Z"]).max() <= bound
+    assert np.abs(o["Z"] - ref["Z"]).max() > 0     # O is not exact in E4M3
+
+
+def test_fp8_attention_forward_bias_and_residual():
+    rng = np.random.default_rng(7)
+    b, s, n_q, n_kv, d, h = 1, 4, 2, 1, 8, 8
+    X = rng.standard_normal((b * s, h))
+    Wq, Wk, Wv = (rng.standard_normal((n * d, h)) * 0.1 for n in (n_q, n_kv, n_kv))
+    Wo = rng.standard_normal((h, n_q * d)) * 0.1
+    bo, R = rng.standard_normal(h), rng.standard_normal((b * s, h))
+    kw = dict(b=b, s=s, n_q=n_q, n_kv=n_kv, d=d)
+    plain = fp8.attention_forward(X, Wq, Wk, Wv, Wo, **kw)
+    full = fp8.attention_forward(X, Wq, Wk, Wv, Wo, bo=bo, R=R, **kw)
+    assert np.array_equal(full["Out"], plain["Z"] + bo + R)
