@@ -21,14 +21,25 @@ from .norm import rmsnorm_forward, rmsnorm_backward
 
 
 def layer_forward(x, P, *, b, s, n_q, n_kv, d, eps=1e-5, act="swiglu",
-                  causal=True):
-    """``P`` holds g1, Wq, Wk, Wv, Wo, g2, W1, W2 (unsharded, fp64-convertible)."""
-    n1 = rmsnorm_forward(x, P["g1"], eps)
-    at = attention_forward(n1["y"], P["Wq"], P["Wk"], P["Wv"], P["Wo"], b=b,
-                           s=s, n_q=n_q, n_kv=n_kv, d=d, causal=causal, R=x)
+                  causal=True, fp8=False):
+    """``P`` holds g1, Wq, Wk, Wv, Wo, g2, W1, W2 (unsharded, fp64-convertible).
+    fp8=True: both blocks' forward projections on E4M3 operands
+    (``oracle.fp8.attention_forward`` and ``oracle.fp8.mlp_forward``), each
+    block quantizing its input as stored (the RMSNorm outputs rounded to
+    bf16); the backward then follows the saved values of that forward."""
+    attn_f, mlp_f = attention_forward, mlp_forward
+    stored = lambda n: n
+    if fp8:
+        # a block quantizes its input as stored: the norm outputs in bf16
+        from . import fp8 as f8
+        attn_f, mlp_f = f8.attention_forward, f8.mlp_forward
+        stored = lambda n: dict(n, y=f8.round_bf16(n["y"]))
+    n1 = stored(rmsnorm_forward(x, P["g1"], eps))
+    at = attn_f(n1["y"], P["Wq"], P["Wk"], P["Wv"], P["Wo"], b=b, s=s,
+                n_q=n_q, n_kv=n_kv, d=d, causal=causal, R=x)
     x1 = at["Out"]
-    n2 = rmsnorm_forward(x1, P["g2"], eps)
-    ml = mlp_forward(n2["y"], P["W1"], P["W2"], act=act, R=x1)
+    n2 = stored(rmsnorm_forward(x1, P["g2"], eps))
+    ml = mlp_f(n2["y"], P["W1"], P["W2"], act=act, R=x1)
     return {"Out": ml["Out"], "x1": x1, "n1": n1, "n2": n2, "attn": at,
             "mlp": ml}
 
