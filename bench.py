@@ -48,7 +48,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="layer_bf16",
                     choices=["layer_bf16", "mlp_swiglu_bf16", "mlp_gelu_bf16",
-                             "attn_gqa_bf16", "mlp_swiglu_fp8"])
+                             "attn_gqa_bf16", "mlp_swiglu_fp8", "layer_fp8"])
     ap.add_argument("--mode", default="fused",
                     choices=["fused", "materialised", "overlap"])
     ap.add_argument("--seq", type=int, default=0,
@@ -189,18 +189,18 @@ class Runner:
               "overlap": B.OVERLAP}[mode]
         b, s, h = cfg["b"], cfg["s"], cfg["h"]
         T = b * s
+        dt = B.FP8 if cfg.get("gemm_dtype") == "fp8" else B.BF16
         if self.kind == "layer":
             self.x = I.layer_inputs(cfg, seed, device)
             self.blk = TPLayer(b, s, h, cfg["h_ffn"], cfg["n_q"], cfg["n_kv"],
                                cfg["d"], cfg["n"], eps=cfg["eps"], mode=md,
-                               device=device)
+                               dtype=dt, device=device)
             self.P = {k: self.x[k] for k in ("g1", "Wq", "Wk", "Wv", "Wo",
                                              "g2", "W1", "W2")}
             self.grads = self.blk.alloc_grads(self.P)
         elif self.kind == "mlp":
             self.x = I.mlp_inputs(cfg, seed, device)
             act = B.SWIGLU if cfg["act"] == "swiglu" else B.GELU
-            dt = B.FP8 if cfg.get("gemm_dtype") == "fp8" else B.BF16
             self.blk = TPMLP(T, h, cfg["h_ffn"], cfg["n"], dtype=dt, act=act,
                              mode=md, dropout_p=cfg.get("p", 0.0), seed=seed,
                              device=device)
@@ -262,7 +262,8 @@ def run_oracle_step(scfg, xs):
     if k == "layer":
         shp = dict(kw, n_q=scfg["n_q"], n_kv=scfg["n_kv"], d=scfg["d"],
                    eps=scfg["eps"])
-        f = oracle.layer_forward(xs["X"], xs, **shp)
+        f = oracle.layer_forward(xs["X"], xs,
+                                 fp8=scfg.get("gemm_dtype") == "fp8", **shp)
         oracle.layer_backward(xs["dOut"], xs["X"], xs, f, **shp)
     elif k == "mlp":
         p = scfg.get("p", 0.0)

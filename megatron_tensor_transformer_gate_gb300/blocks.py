@@ -84,9 +84,12 @@ class TPMLP:
 
 
 class TPAttention:
+    """dtype B.BF16, or B.FP8: the projections of the forward on E4M3
+    operands (bf16 storage and backward)."""
+
     def __init__(self, b, s, h, n_q, n_kv, d, n, *, causal=True, mode=B.FUSED,
-                 device="cuda"):
-        self.desc = B.attn_desc(b, s, h, n_q, n_kv, d, n, B.BF16, causal,
+                 dtype=B.BF16, device="cuda"):
+        self.desc = B.attn_desc(b, s, h, n_q, n_kv, d, n, dtype, causal,
                                 mode)
         self.T, self.h = b * s, h
         self.shape = (b, s, n_q, n_kv, d)
@@ -134,16 +137,17 @@ class TPAttention:
 
 
 class TPLayer:
-    """Pre-norm layer: RMSNorm → attention (+x) → RMSNorm → SwiGLU MLP (+x1)."""
+    """Pre-norm layer: RMSNorm → attention (+x) → RMSNorm → SwiGLU MLP (+x1).
+    dtype B.FP8 runs every projection of the forward on E4M3 operands."""
 
     def __init__(self, b, s, h, h_ffn, n_q, n_kv, d, n, *, eps=1e-5,
-                 act=B.SWIGLU, mode=B.FUSED, device="cuda"):
+                 act=B.SWIGLU, mode=B.FUSED, dtype=B.BF16, device="cuda"):
         T = b * s
         self.T, self.h, self.eps = T, h, eps
         self.device = device
         self.attn = TPAttention(b, s, h, n_q, n_kv, d, n, mode=mode,
-                                device=device)
-        self.mlp = TPMLP(T, h, h_ffn, n, dtype=B.BF16, act=act, mode=mode,
+                                dtype=dtype, device=device)
+        self.mlp = TPMLP(T, h, h_ffn, n, dtype=dtype, act=act, mode=mode,
                          device=device)
         kw = dict(dtype=torch.bfloat16, device=device)
         self.xn1 = torch.empty((T, h), **kw)

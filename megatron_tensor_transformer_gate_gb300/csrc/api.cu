@@ -592,7 +592,8 @@ namespace {
 
 tp_status check_attn(const tp_attn_desc* d) {
   if (d == nullptr) return TP_ERR_NULL;
-  if (d->dtype != TP_F32 && d->dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (d->dtype != TP_F32 && d->dtype != TP_BF16 && d->dtype != TP_FP8)
+    return TP_ERR_DTYPE;
   if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED &&
       d->mode != TP_REDUCE_OVERLAP)
     return TP_ERR_DTYPE;
@@ -603,7 +604,9 @@ tp_status check_attn(const tp_attn_desc* d) {
     return TP_ERR_SHAPE;
   // GQA groups and heads must split evenly over the n ranks
   if (d->n_q % d->n_kv || d->n_q % d->n || d->n_kv % d->n) return TP_ERR_SHAPE;
-  if (d->dtype != TP_BF16 || d->d != 128) return TP_ERR_UNSUPPORTED;
+  if (storage(d->dtype) != TP_BF16 || d->d != 128) return TP_ERR_UNSUPPORTED;
+  // FP8 mode: E4M3 rows of X (h bytes) must start on 16-byte boundaries
+  if (d->dtype == TP_FP8 && d->h % 16) return TP_ERR_SHAPE;
   return TP_OK;
 }
 
@@ -611,6 +614,12 @@ struct AttnFwdLayout {
   void *q = nullptr, *k = nullptr, *v = nullptr, *o = nullptr;
   float* lse = nullptr;
   void* partials = nullptr;
+  // FP8 mode: E4M3 copies of X, Wq, Wk, Wv, O, Wo, their scales (same
+  // order) and amax scratch words
+  void *xq = nullptr, *wqq = nullptr, *wkq = nullptr, *wvq = nullptr,
+       *oq = nullptr, *woq = nullptr;
+  float* scales = nullptr;
+  unsigned* amax = nullptr;
   size_t bytes = 0;
 };
 
@@ -626,6 +635,17 @@ AttnFwdLayout attn_fwd_layout(const tp_attn_desc* d, void* ws) {
   L.lse = static_cast<float*>(c.take((size_t)d->b * d->n_q * d->s * 4));
   if (d->mode != TP_REDUCE_FUSED)
     L.partials = c.take((size_t)d->n * T * (size_t)d->h * 2);
+  if (d->dtype == TP_FP8) {
+    const size_t h = (size_t)d->h;
+    L.xq = c.take(T * h);
+    L.wqq = c.take(qd * h);
+    L.wkq = c.take(kd * h);
+    L.wvq = c.take(kd * h);
+    L.oq = c.take(T * qd);
+    L.woq = c.take(h * qd);
+    L.scales = static_cast<float*>(c.take(6 * sizeof(float)));
+    L.amax = static_cast<unsigned*>(c.take(6 * sizeof(unsigned)));
+  }
   L.bytes = c.off;
   return L;
 }
@@ -718,21 +738,57 @@ extern "C" tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X,
     const int64_t T = d->b * d->s, h = d->h;
     const int64_t qd = (int64_t)d->n_q * d->d, kd = (int64_t)d->n_kv * d->d;
     const int n = d->n;
+    const bool f8 = d->dtype == TP_FP8;
+    int err = 0;
+    if (f8) {   // quantize the projections' operands, one scale per tensor
+      const void* src[4] = {X, Wq, Wk, Wv};
+      void* dst[4] = {L.xq, L.wqq, L.wkq, L.wvq};
+      const int64_t cnt[4] = {T * h, qd * h, kd * h, kd * h};
+      for (int i = 0; i < 4 && !err; ++i)
+        err = quantize_fp8(src[i], cnt[i], dst[i], L.scales + i, L.amax + i,
+                           stream);
+      if (err) return cuda_status(err);
+    }
     // column-parallel Q, K, V projections (each rank's heads are a column
     // block, written in fp16 for the attention core)
-    GemmProblem gq = proj(T, qd, op(X, h, 0, T), op(Wq, h, 0, qd), h, L.q, qd);
-    GemmProblem gk = proj(T, kd, op(X, h, 0, T), op(Wk, h, 0, kd), h, L.k, kd);
-    GemmProblem gv = proj(T, kd, op(X, h, 0, T), op(Wv, h, 0, kd), h, L.v, kd);
+    const void* xa = f8 ? L.xq : X;
+    GemmProblem gq = proj(T, qd, op(xa, h, 0, T), op(f8 ? L.wqq : Wq, h, 0, qd),
+                          h, L.q, qd);
+    GemmProblem gk = proj(T, kd, op(xa, h, 0, T), op(f8 ? L.wkq : Wk, h, 0, kd),
+                          h, L.k, kd);
+    GemmProblem gv = proj(T, kd, op(xa, h, 0, T), op(f8 ? L.wvq : Wv, h, 0, kd),
+                          h, L.v, kd);
     gq.epi.out_f16 = gk.epi.out_f16 = gv.epi.out_f16 = 1;
-    int err = run_gemm(gq, stream);
+    if (f8) {
+      GemmProblem* gs[3] = {&gq, &gk, &gv};
+      for (int i = 0; i < 3; ++i) {
+        gs[i]->dtype = TP_FP8;
+        gs[i]->epi.scale_a = L.scales + 0;
+        gs[i]->epi.scale_b = L.scales + 1 + i;
+      }
+    }
+    err = run_gemm(gq, stream);
     if (!err) err = run_gemm(gk, stream);
     if (!err) err = run_gemm(gv, stream);
     if (err) return cuda_status(err);
     err = flash_fwd(attn_shape(d), L.q, L.k, L.v, L.o, L.lse,
                     device_status_ptr(), stream);
     if (err) return cuda_status(err);
+    if (f8) {   // O (bf16) and Wo to E4M3
+      err = quantize_fp8(L.o, T * qd, L.oq, L.scales + 4, L.amax + 4, stream);
+      if (!err)
+        err = quantize_fp8(Wo, h * qd, L.woq, L.scales + 5, L.amax + 5,
+                           stream);
+      if (err) return cuda_status(err);
+    }
     // row-parallel output projection + g reduction + bias + residual
-    GemmProblem g = proj(T, h, op(L.o, qd, 0, T), op(Wo, qd, 0, h), qd, Out, h);
+    GemmProblem g = proj(T, h, op(f8 ? L.oq : L.o, qd, 0, T),
+                         op(f8 ? L.woq : Wo, qd, 0, h), qd, Out, h);
+    if (f8) {
+      g.dtype = TP_FP8;
+      g.epi.scale_a = L.scales + 4;
+      g.epi.scale_b = L.scales + 5;
+    }
     if (d->mode == TP_REDUCE_FUSED) {
       g.epi.bias = bo;
       g.epi.resid = R;

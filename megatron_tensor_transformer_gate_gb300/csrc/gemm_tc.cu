@@ -586,7 +586,7 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
   if (e.kind == EPI_SWIGLU && (b_mn || a_mn || pr.nparts != 1))
     return cudaErrorInvalidValue;
   const bool f8 = pr.dtype == 2;
-  if (f8 && (a_mn || b_mn || e.out_f16 ||
+  if (f8 && (a_mn || b_mn ||
              (e.kind != EPI_STORE && e.kind != EPI_GELU &&
               e.kind != EPI_SWIGLU)))
     return cudaErrorInvalidValue;

@@ -52,6 +52,11 @@ WORKLOADS = {
     "layer_bf16": dict(kind="layer", dtype="bf16", b=1, s=8192, h=8192,
                        h_ffn=28672, n_q=64, n_kv=8, d=128, n=8, act="swiglu",
                        w_std=0.02, eps=1e-5),
+    # the layer with every forward projection on per-tensor scaled E4M3
+    # (bf16 storage, bf16 backward)
+    "layer_fp8": dict(kind="layer", dtype="bf16", gemm_dtype="fp8", b=1,
+                      s=8192, h=8192, h_ffn=28672, n_q=64, n_kv=8, d=128, n=8,
+                      act="swiglu", w_std=0.02, eps=1e-5),
 }
 
 # Fixed sub-seed index of every tensor a workload draws.

@@ -26,6 +26,17 @@ import torch
 BF16_FRO = 1e-2
 BF16_MAXRMS = 3e-2
 F32_MAXREL = 1e-4
+# FP8 forward projections (E4M3, one scale per tensor): an intermediate the
+# path computes on its own before quantizing it (the attention output O)
+# differs from the oracle's in its last bf16 bits, and where that moves a
+# value across an E4M3 rounding boundary its code changes by one step (2^-4
+# relative for normal values; a fraction f of the elements flips, adding
+# about sqrt(f)·2^-4 ≈ 0.6-0.9 % in Frobenius norm for f of 1-2 %).  The
+# blocks keep the bf16 Frobenius bound downstream of O (a row may hold a few
+# flips, so not the row-wise one); the composed layer carries two blocks'
+# flips through the residual stream, the norms and the softmax / SwiGLU
+# backward, and is held to twice the bound.
+FP8_LAYER_FRO = 2e-2
 
 
 def f64(t):
@@ -60,7 +71,7 @@ def check(g, o, name, dtype="bf16"):
     return fro, maxrms, maxrel
 
 
-def check_fro(g, o, name):
+def check_fro(g, o, name, bound=BF16_FRO):
     fro, maxrms, maxrel = errors(g, o)
-    assert fro <= BF16_FRO, f"{name}: fro {fro:.3e}"
+    assert fro <= bound, f"{name}: fro {fro:.3e}"
     return fro, maxrms, maxrel

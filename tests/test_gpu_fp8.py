@@ -1,7 +1,7 @@
 """GPU parity of the FP8 path: E4M3 codes and scales bit-exact against the
-oracle's quantization of the same bf16 values, the E4M3 GEMM and the MLP
-forward in FP8 mode against the oracle, and the bf16 backward that follows
-it."""
+oracle's quantization of the same bf16 values, the E4M3 GEMM, the MLP, the
+attention block and the whole layer with their forward projections in FP8
+mode against the oracle, and the bf16 backward that follows them."""
 
 import numpy as np
 import pytest
@@ -10,8 +10,9 @@ import torch
 import oracle
 from oracle import fp8 as ofp8
 from megatron_tensor_transformer_gate_gb300 import inputs as I
-from megatron_tensor_transformer_gate_gb300.blocks import TPMLP
-from _parity import check
+from megatron_tensor_transformer_gate_gb300.blocks import (TPAttention,
+                                                          TPLayer, TPMLP)
+from _parity import FP8_LAYER_FRO, check, check_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -126,3 +127,78 @@ def test_fp8_mode_rejects_unaligned_widths(tp):
     with pytest.raises(tp.TPError) as e:
         tp.mlp_fwd(desc, X, W1, W2, torch.empty_like(X), ws)
     assert e.value.code == 2
+
+
+def run_attn(tp, cfg, mode, seed):
+    b, s, h = cfg["b"], cfg["s"], cfg["h"]
+    nq, nkv, d, n = cfg["n_q"], cfg["n_kv"], cfg["d"], cfg["n"]
+    causal = cfg.get("causal", True)
+    x = I.attn_inputs(cfg, seed, "cpu")
+    dv = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    a = TPAttention(b, s, h, nq, nkv, d, n, causal=causal, mode=mode,
+                    dtype=tp.FP8)
+    out = a.forward(dv["X"], dv["Wq"], dv["Wk"], dv["Wv"], dv["Wo"],
+                    bo=dv["bo"], R=dv["R"])
+    g = a.backward(dv["dOut"], dv["X"], dv["Wq"], dv["Wk"], dv["Wv"],
+                   dv["Wo"], want_dbo=x["bo"] is not None)
+    tp.device_status()
+    f = {k: I.to_f64(v) for k, v in x.items()}
+    kw = dict(b=b, s=s, n_q=nq, n_kv=nkv, d=d, causal=causal)
+    fo = ofp8.attention_forward(f["X"], f["Wq"], f["Wk"], f["Wv"], f["Wo"],
+                                bo=f["bo"], R=f["R"], **kw)
+    go = oracle.attention_backward(f["dOut"], f["X"], f["Wq"], f["Wk"],
+                                   f["Wv"], f["Wo"], fo, **kw)
+    # Out comes from O re-quantized to E4M3: the GPU's O (fp16 probabilities,
+    # flash accumulation) and the oracle's differ in the last bf16 bits, which
+    # moves some O elements across an E4M3 rounding boundary (a 2^-4 step);
+    # those flips stay inside the Frobenius bound but not the row-wise one
+    check_fro(out, fo["Out"], "Out")
+    for k in ("dX", "dWq", "dWk", "dWv", "dWo"):
+        check(g[k], go[k], k)
+    if "dbo" in g:
+        check(g["dbo"], go["dbo"], "dbo")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_fp8_attention_workload(tp, mode):
+    # the attention workload (b 2, s 2048, h 4096, 32 q / 8 kv heads, n 4)
+    run_attn(tp, I.workload("attn_gqa_bf16"), mode, 20260004)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_fp8_attention_ragged_bias_residual(tp, causal):
+    cfg = I.workload("attn_gqa_bf16", b=2, s=200, h=512, n_q=8, n_kv=2, n=2,
+                     causal=causal, bo=True, residual="random",
+                     w_std="fan_in")
+    run_attn(tp, cfg, 1, 35)
+
+
+def test_fp8_layer(tp):
+    # the pre-norm layer with both blocks' forward projections on E4M3
+    cfg = I.workload("layer_fp8", b=2, s=256, h=1024, h_ffn=2048, n_q=8,
+                     n_kv=2, d=128, n=2)
+    x = I.layer_inputs(cfg, 36, "cpu")
+    names = ("g1", "Wq", "Wk", "Wv", "Wo", "g2", "W1", "W2")
+    P = {k: x[k].cuda() for k in names}
+    L = TPLayer(cfg["b"], cfg["s"], cfg["h"], cfg["h_ffn"], cfg["n_q"],
+                cfg["n_kv"], cfg["d"], cfg["n"], dtype=tp.FP8)
+    X = x["X"].cuda()
+    out = L.forward(X, P)
+    g = L.backward(x["dOut"].cuda(), X, P)
+    tp.device_status()
+    f = {k: I.to_f64(v) for k, v in x.items()}
+    shp = dict(b=cfg["b"], s=cfg["s"], n_q=cfg["n_q"], n_kv=cfg["n_kv"],
+               d=cfg["d"], eps=cfg["eps"])
+    fo = oracle.layer_forward(f["X"], f, fp8=True, **shp)
+    go = oracle.layer_backward(f["dOut"], f["X"], f, fo, **shp)
+    # two quantized blocks' E4M3 code flips carried through the layer: the
+    # FP8 layer's Frobenius bound
+    check_fro(out, fo["Out"], "Out", FP8_LAYER_FRO)
+    for k in ("dX", "dWq", "dWk", "dWv", "dWo", "dW1", "dW2", "dg1", "dg2"):
+        check_fro(g[k], go[k], k, FP8_LAYER_FRO)
+
+
+def test_fp8_attention_rejects_unaligned_width(tp):
+    # h = 264: E4M3 rows of X are not a multiple of 16 bytes
+    desc = tp.attn_desc(1, 64, 264, 2, 1, 128, 1, tp.FP8)
+    assert tp.attn_workspace_bytes(desc) == 0
