@@ -113,6 +113,7 @@ def test_mlp_rejects_before_launch(tp):
     assert _fwd(tp, tp.mlp_desc(64, 124, 512, 2)) == 2      # h % 8
     assert _fwd(tp, tp.mlp_desc(64, 128, 512, 2, dtype=7)) == 3
     assert _fwd(tp, tp.mlp_desc(64, 128, 512, 2, dropout_p=1.0)) == 8
+    assert _fwd(tp, tp.mlp_desc(0, 128, 512, 2)) == 2       # no tokens
     d = tp.mlp_desc(64, 128, 512, 2)
     assert _fwd(tp, d, ws_bytes=16) == 4                    # ws too small
     assert tp.mlp_workspace_bytes(d) >= 2 * 64 * 512 * 2
@@ -136,6 +137,24 @@ def test_attn_rejects_before_launch(tp):
     assert call(tp.attn_desc(1, 64, 512, 8, 2, 128, 2, dtype=tp.F32)) == 5
     assert call(tp.attn_desc(1, 64, 512, 8, 2, 128, 2), ws_bytes=1) == 4
     assert tp.attn_workspace_bytes(tp.attn_desc(1, 64, 512, 8, 2, 128, 2)) > 0
+    assert call(tp.attn_desc(0, 64, 512, 8, 2, 128, 2)) == 2   # no batch
+    assert call(tp.attn_desc(1, 0, 512, 8, 2, 128, 2)) == 2    # no tokens
+    # FP8 mode: E4M3 rows of X need h % 16 == 0
+    assert call(tp.attn_desc(1, 64, 264, 2, 1, 128, 1, dtype=tp.FP8)) == 2
+
+
+def test_attn_fp8_workspace_adds_the_e4m3_copies(tp):
+    # X, Wq, Wk, Wv, O, Wo in E4M3 (one byte each) plus 6 scales and 6 amax
+    # words, each region on a 256-byte boundary
+    b, s, h, nq, nkv, d, n = 2, 200, 512, 8, 2, 128, 2
+    T, qd, kd = b * s, nq * d, nkv * d
+    base = tp.attn_workspace_bytes(tp.attn_desc(b, s, h, nq, nkv, d, n))
+    f8 = tp.attn_workspace_bytes(tp.attn_desc(b, s, h, nq, nkv, d, n,
+                                              dtype=tp.FP8))
+    up = lambda x: (x + 255) // 256 * 256
+    extra = sum(up(x) for x in (T * h, qd * h, kd * h, kd * h, T * qd,
+                                h * qd, 24))
+    assert f8 - up(base) == extra + 24      # the amax words end it
 
 
 def test_status_strings(tp):
