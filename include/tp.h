@@ -156,10 +156,15 @@ tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut, const void* X,
 typedef struct {
   int64_t b, s, h;
   int32_t n_q, n_kv, d, n;
-  int32_t dtype;      /* TP_BF16 only (TP_F32 -> TP_ERR_UNSUPPORTED) */
+  int32_t dtype;      /* TP_BF16 or TP_FP8 (TP_F32 -> TP_ERR_UNSUPPORTED) */
   int32_t causal;     /* 1 = causal mask, 0 = full */
   int32_t mode;       /* tp_reduce_mode */
 } tp_attn_desc;
+/* dtype TP_FP8: storage and backward as for TP_BF16; the Q, K, V and output
+ * projections of the forward run on E4M3 operands (tp_quantize_fp8 of X,
+ * Wq, Wk, Wv, then of O and Wo; dequantized in the epilogue).  Needs h a
+ * multiple of 16.  ws then also holds the E4M3 copies of X, Wq, Wk, Wv, O,
+ * Wo and their six scales (and six amax words) after the regions below. */
 
 /* ws: Q [T, n_q·d], K, V [T, n_kv·d] (fp16), O [T, n_q·d] (bf16) and LSE
  * [b, n_q, s] fp32 saved for backward, then the forward scratch (n partial
@@ -232,6 +237,47 @@ tp_status tp_rmsnorm_bwd_noalloc(int64_t T, int64_t h, float eps,
                                  const void* gamma, const float* rstd,
                                  const void* dres, void* dx, void* dgamma,
                                  tp_stream stream);
+
+/* ---------------------------------------------------------------- layer --
+ * The pre-norm layer of the C5 workload as one call per direction
+ * ([Troverld] §III.III layer with the norm before each block; [Grasp-TP]
+ * §3–§4 blocks):  x1 = x + Attn(RMSNorm₁(x)),  out = x1 + MLP(RMSNorm₂(x1)),
+ * causal GQA attention without bias, SwiGLU MLP without bias or dropout,
+ * four reductions (g after each row-parallel projection, f on each block's
+ * input gradient) taken as the desc's mode says.  Composes tp_rmsnorm_*,
+ * tp_attn_* and tp_mlp_* in this order on one stream; every tensor is bf16
+ * [T, h] (weights as for the blocks, γ₁ and γ₂ [h]).  dtype TP_FP8 runs both
+ * blocks' forward projections on E4M3 operands (see the blocks). */
+typedef struct {
+  int64_t b, s, h, h_ffn;
+  int32_t n_q, n_kv, d, n;
+  int32_t dtype;      /* TP_BF16 or TP_FP8 */
+  int32_t mode;       /* tp_reduce_mode */
+  float eps;          /* RMSNorm ε (> 0) */
+} tp_layer_desc;
+/* ws: saved for backward — RMSNorm₁ output, x1, RMSNorm₂ output (bf16
+ * [T, h]), rstd₁, rstd₂ (fp32 [T]), then the attention block's ws and the
+ * MLP block's ws (tp_attn_workspace_bytes, tp_mlp_workspace_bytes of the
+ * blocks' descs); each region on the next 256-byte boundary. */
+size_t tp_layer_workspace_bytes(const tp_layer_desc* d);
+/* scratch: the two block gradients' [T, h] hand-overs (bf16), the RMSNorm
+ * scratch, then the larger of the attention and MLP backward scratches
+ * (the blocks run one after the other and share it). */
+size_t tp_layer_bwd_scratch_bytes(const tp_layer_desc* d);
+tp_status tp_layer_fwd(const tp_layer_desc* d, const void* x, const void* g1,
+                       const void* Wq, const void* Wk, const void* Wv,
+                       const void* Wo, const void* g2, const void* W1,
+                       const void* W2, void* out, void* ws, size_t ws_bytes,
+                       tp_stream stream);
+/* Gradients of ⟨dout, out⟩ with respect to x and every weight (overwritten);
+ * ws must hold what tp_layer_fwd saved for the same inputs. */
+tp_status tp_layer_bwd(const tp_layer_desc* d, const void* dout, const void* x,
+                       const void* g1, const void* Wq, const void* Wk,
+                       const void* Wv, const void* Wo, const void* g2,
+                       const void* W1, const void* W2, const void* ws,
+                       void* dx, void* dg1, void* dWq, void* dWk, void* dWv,
+                       void* dWo, void* dg2, void* dW1, void* dW2,
+                       void* scratch, size_t scratch_bytes, tp_stream stream);
 
 /* ----------------------------------------------------------- accounting --
  * Host-only, exact integer figures; no GPU needed.

@@ -70,6 +70,15 @@ class ActReport(ctypes.Structure):
         "layer_bytes_flash")]
 
 
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("s", ctypes.c_int64),
+                ("h", ctypes.c_int64), ("h_ffn", ctypes.c_int64),
+                ("n_q", ctypes.c_int32), ("n_kv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("n", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("mode", ctypes.c_int32),
+                ("eps", ctypes.c_float)]
+
+
 class ProfileEntry(ctypes.Structure):
     _fields_ = [("launches", ctypes.c_uint64), ("ms", ctypes.c_double),
                 ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
@@ -84,6 +93,7 @@ _I64, _I32, _F, _SZ, _U64 = (ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
                              ctypes.c_size_t, ctypes.c_uint64)
 _MP = ctypes.POINTER(MlpDesc)
 _AP = ctypes.POINTER(AttnDesc)
+_LP = ctypes.POINTER(LayerDesc)
 _U64P = ctypes.POINTER(ctypes.c_uint64)
 
 # name -> (restype, argtypes); mirrors include/tp.h
@@ -99,6 +109,10 @@ SIGNATURES = {
     "tp_attn_fwd": (_I32, [_AP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "tp_attn_bwd": (_I32, [_AP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                            _P, _P, _P, _P, _SZ, _P]),
+    "tp_layer_workspace_bytes": (_SZ, [_LP]),
+    "tp_layer_bwd_scratch_bytes": (_SZ, [_LP]),
+    "tp_layer_fwd": (_I32, [_LP] + [_P] * 11 + [_SZ, _P]),
+    "tp_layer_bwd": (_I32, [_LP] + [_P] * 21 + [_SZ, _P]),
     "tp_rmsnorm_fwd": (_I32, [_I64, _I64, _F, _I32, _P, _P, _P, _P, _P]),
     "tp_rmsnorm_bwd_scratch_bytes": (_SZ, [_I64, _I64]),
     "tp_rmsnorm_bwd": (_I32, [_I64, _I64, _F, _I32, _P, _P, _P, _P, _P, _P,
@@ -307,6 +321,41 @@ def attn_bwd(desc, dOut, X, Wq, Wk, Wv, Wo, ws, dX, dWq, dWk, dWv, dWo,
 
 
 # --------------------------------------------------------------- RMSNorm --
+# ----------------------------------------------------------------- layer --
+def layer_desc(b, s, h, h_ffn, n_q, n_kv, d, n, dtype=BF16, mode=FUSED,
+               eps=1e-5):
+    return LayerDesc(b, s, h, h_ffn, n_q, n_kv, d, n, dtype, mode, eps)
+
+
+def layer_workspace_bytes(desc):
+    return lib().tp_layer_workspace_bytes(ctypes.byref(desc))
+
+
+def layer_bwd_scratch_bytes(desc):
+    return lib().tp_layer_bwd_scratch_bytes(ctypes.byref(desc))
+
+
+def layer_fwd(desc, x, P, out, ws, stream=None):
+    """out = x1 + MLP(RMSNorm₂(x1)), x1 = x + Attn(RMSNorm₁(x)); P holds g1,
+    Wq, Wk, Wv, Wo, g2, W1, W2."""
+    check(lib().tp_layer_fwd(
+        ctypes.byref(desc), ptr(x), *(ptr(P[k]) for k in
+                                      ("g1", "Wq", "Wk", "Wv", "Wo", "g2",
+                                       "W1", "W2")),
+        ptr(out), ptr(ws), ws.numel() * ws.element_size(),
+        stream_handle(stream)), "tp_layer_fwd")
+
+
+def layer_bwd(desc, dout, x, P, ws, grads, scratch, stream=None):
+    """grads: dX, dg1, dWq, dWk, dWv, dWo, dg2, dW1, dW2 (overwritten)."""
+    names = ("g1", "Wq", "Wk", "Wv", "Wo", "g2", "W1", "W2")
+    check(lib().tp_layer_bwd(
+        ctypes.byref(desc), ptr(dout), ptr(x), *(ptr(P[k]) for k in names),
+        ptr(ws), ptr(grads["dX"]), *(ptr(grads["d" + k]) for k in names),
+        ptr(scratch), scratch.numel() * scratch.element_size(),
+        stream_handle(stream)), "tp_layer_bwd")
+
+
 def rmsnorm_fwd(x, gamma, y, rstd, eps=1e-5, stream=None):
     T, h = x.shape
     check(lib().tp_rmsnorm_fwd(T, h, eps, dtype_code(x), ptr(x), ptr(gamma),

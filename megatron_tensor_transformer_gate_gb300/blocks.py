@@ -137,35 +137,27 @@ class TPAttention:
 
 
 class TPLayer:
-    """Pre-norm layer: RMSNorm → attention (+x) → RMSNorm → SwiGLU MLP (+x1).
-    dtype B.FP8 runs every projection of the forward on E4M3 operands."""
+    """Pre-norm layer: RMSNorm → attention (+x) → RMSNorm → SwiGLU MLP (+x1),
+    one tp_layer_fwd / tp_layer_bwd call per direction.  dtype B.FP8 runs
+    every projection of the forward on E4M3 operands."""
 
     def __init__(self, b, s, h, h_ffn, n_q, n_kv, d, n, *, eps=1e-5,
                  act=B.SWIGLU, mode=B.FUSED, dtype=B.BF16, device="cuda"):
-        T = b * s
-        self.T, self.h, self.eps = T, h, eps
+        if act != B.SWIGLU:
+            raise ValueError("the layer's MLP is SwiGLU")
+        self.T, self.h, self.eps = b * s, h, eps
         self.device = device
-        self.attn = TPAttention(b, s, h, n_q, n_kv, d, n, mode=mode,
-                                dtype=dtype, device=device)
-        self.mlp = TPMLP(T, h, h_ffn, n, dtype=dtype, act=act, mode=mode,
-                         device=device)
-        kw = dict(dtype=torch.bfloat16, device=device)
-        self.xn1 = torch.empty((T, h), **kw)
-        self.x1 = torch.empty((T, h), **kw)
-        self.xn2 = torch.empty((T, h), **kw)
-        self.rstd1 = torch.empty((T,), dtype=torch.float32, device=device)
-        self.rstd2 = torch.empty((T,), dtype=torch.float32, device=device)
-        self.norm_scratch = _buf(B.rmsnorm_bwd_scratch_bytes(T, h), device)
-        self.dxn = torch.empty((T, h), **kw)
-        self.dx1 = torch.empty((T, h), **kw)
+        self.desc = B.layer_desc(b, s, h, h_ffn, n_q, n_kv, d, n, dtype, mode,
+                                 eps)
+        self.ws = _buf(B.layer_workspace_bytes(self.desc), device)
+        self.scratch = _buf(B.layer_bwd_scratch_bytes(self.desc), device)
 
     def forward(self, x, P, out=None, stream=None):
-        B.rmsnorm_fwd(x, P["g1"], self.xn1, self.rstd1, self.eps, stream)
-        self.attn.forward(self.xn1, P["Wq"], P["Wk"], P["Wv"], P["Wo"], R=x,
-                          out=self.x1, stream=stream)
-        B.rmsnorm_fwd(self.x1, P["g2"], self.xn2, self.rstd2, self.eps, stream)
-        return self.mlp.forward(self.xn2, P["W1"], P["W2"], R=self.x1,
-                                out=out, stream=stream)
+        if out is None:
+            out = torch.empty((self.T, self.h), dtype=torch.bfloat16,
+                              device=self.device)
+        B.layer_fwd(self.desc, x, P, out, self.ws, stream)
+        return out
 
     def alloc_grads(self, P):
         g = {k: torch.empty_like(P[k]) for k in ("g1", "Wq", "Wk", "Wv", "Wo",
@@ -177,15 +169,5 @@ class TPLayer:
 
     def backward(self, dout, x, P, grads=None, stream=None):
         g = grads if grads is not None else self.alloc_grads(P)
-        mg = {"dX": self.dxn, "dW1": g["dW1"], "dW2": g["dW2"]}
-        self.mlp.backward(dout, self.xn2, P["W1"], P["W2"], grads=mg,
-                          stream=stream)
-        B.rmsnorm_bwd(self.dxn, self.x1, P["g2"], self.rstd2, self.dx1,
-                      g["dg2"], self.norm_scratch, dres=dout, stream=stream)
-        ag = {"dX": self.dxn, "dWq": g["dWq"], "dWk": g["dWk"],
-              "dWv": g["dWv"], "dWo": g["dWo"]}
-        self.attn.backward(self.dx1, self.xn1, P["Wq"], P["Wk"], P["Wv"],
-                           P["Wo"], grads=ag, stream=stream)
-        B.rmsnorm_bwd(self.dxn, x, P["g1"], self.rstd1, g["dX"], g["dg1"],
-                      self.norm_scratch, dres=self.dx1, stream=stream)
+        B.layer_bwd(self.desc, dout, x, P, self.ws, g, self.scratch, stream)
         return g

@@ -1144,3 +1144,184 @@ extern "C" int32_t tp_num_sms(void) {
   if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) return 0;
   return device_sm_count();
 }
+
+// ----------------------------------------------------------------- layer --
+// The pre-norm layer composed from the block entry points on one stream.
+namespace {
+
+tp_status check_layer(const tp_layer_desc* d) {
+  if (d == nullptr) return TP_ERR_NULL;
+  if (d->dtype != TP_BF16 && d->dtype != TP_FP8) return TP_ERR_UNSUPPORTED;
+  if (!(d->eps > 0.0f)) return TP_ERR_ARG;
+  if (d->h > 16384) return TP_ERR_SHAPE;   // the RMSNorm kernels' limit
+  return TP_OK;
+}
+
+tp_attn_desc layer_attn(const tp_layer_desc* d) {
+  tp_attn_desc a;
+  a.b = d->b;
+  a.s = d->s;
+  a.h = d->h;
+  a.n_q = d->n_q;
+  a.n_kv = d->n_kv;
+  a.d = d->d;
+  a.n = d->n;
+  a.dtype = d->dtype;
+  a.causal = 1;
+  a.mode = d->mode;
+  return a;
+}
+
+tp_mlp_desc layer_mlp(const tp_layer_desc* d) {
+  tp_mlp_desc m;
+  m.T = d->b * d->s;
+  m.h = d->h;
+  m.h_ffn = d->h_ffn;
+  m.n = d->n;
+  m.dtype = d->dtype;
+  m.act = TP_SWIGLU;
+  m.mode = d->mode;
+  m.dropout_p = 0.0f;
+  m.seed = 0;
+  return m;
+}
+
+struct LayerFwdLayout {
+  void *xn1 = nullptr, *x1 = nullptr, *xn2 = nullptr;
+  float *rstd1 = nullptr, *rstd2 = nullptr;
+  void *attn_ws = nullptr, *mlp_ws = nullptr;
+  size_t attn_bytes = 0, mlp_bytes = 0, bytes = 0;
+};
+
+// Zero `bytes` when a block rejects its part of the desc.
+LayerFwdLayout layer_fwd_layout(const tp_layer_desc* d, void* ws) {
+  LayerFwdLayout L;
+  const tp_attn_desc ad = layer_attn(d);
+  const tp_mlp_desc md = layer_mlp(d);
+  L.attn_bytes = tp_attn_workspace_bytes(&ad);
+  L.mlp_bytes = tp_mlp_workspace_bytes(&md);
+  if (L.attn_bytes == 0 || L.mlp_bytes == 0) return L;
+  Carver c(ws);
+  const size_t th = (size_t)(d->b * d->s) * (size_t)d->h * 2;
+  L.xn1 = c.take(th);
+  L.x1 = c.take(th);
+  L.xn2 = c.take(th);
+  L.rstd1 = static_cast<float*>(c.take((size_t)(d->b * d->s) * 4));
+  L.rstd2 = static_cast<float*>(c.take((size_t)(d->b * d->s) * 4));
+  L.attn_ws = c.take(L.attn_bytes);
+  L.mlp_ws = c.take(L.mlp_bytes);
+  L.bytes = c.off;
+  return L;
+}
+
+struct LayerBwdLayout {
+  void *dxn = nullptr, *dx1 = nullptr, *norm = nullptr, *blk = nullptr;
+  size_t norm_bytes = 0, blk_bytes = 0, bytes = 0;
+};
+
+LayerBwdLayout layer_bwd_layout(const tp_layer_desc* d, void* scratch) {
+  LayerBwdLayout L;
+  const tp_attn_desc ad = layer_attn(d);
+  const tp_mlp_desc md = layer_mlp(d);
+  const size_t a = tp_attn_bwd_scratch_bytes(&ad);
+  const size_t m = tp_mlp_bwd_scratch_bytes(&md);
+  L.norm_bytes = tp_rmsnorm_bwd_scratch_bytes(d->b * d->s, d->h);
+  if (a == 0 || m == 0 || L.norm_bytes == 0) return L;
+  L.blk_bytes = std::max(a, m);
+  Carver c(scratch);
+  const size_t th = (size_t)(d->b * d->s) * (size_t)d->h * 2;
+  L.dxn = c.take(th);
+  L.dx1 = c.take(th);
+  L.norm = c.take(L.norm_bytes);
+  L.blk = c.take(L.blk_bytes);
+  L.bytes = c.off;
+  return L;
+}
+
+}  // namespace
+
+extern "C" size_t tp_layer_workspace_bytes(const tp_layer_desc* d) {
+  if (check_layer(d) != TP_OK) return 0;
+  return layer_fwd_layout(d, nullptr).bytes;
+}
+
+extern "C" size_t tp_layer_bwd_scratch_bytes(const tp_layer_desc* d) {
+  if (check_layer(d) != TP_OK) return 0;
+  return layer_bwd_layout(d, nullptr).bytes;
+}
+
+extern "C" tp_status tp_layer_fwd(const tp_layer_desc* d, const void* x,
+                                  const void* g1, const void* Wq,
+                                  const void* Wk, const void* Wv,
+                                  const void* Wo, const void* g2,
+                                  const void* W1, const void* W2, void* out,
+                                  void* ws, size_t ws_bytes,
+                                  tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    tp_status st = check_layer(d);
+    if (st != TP_OK) return st;
+    if (!x || !g1 || !g2 || !out || !ws) return TP_ERR_NULL;
+    const LayerFwdLayout L = layer_fwd_layout(d, ws);
+    if (L.bytes == 0) {   // a block rejects the shape: report its reason
+      const tp_attn_desc ad = layer_attn(d);
+      const tp_mlp_desc md = layer_mlp(d);
+      st = check_attn(&ad);
+      return st != TP_OK ? st : check_mlp(&md);
+    }
+    if (ws_bytes < L.bytes) return TP_ERR_WORKSPACE;
+    const int64_t T = d->b * d->s, h = d->h;
+    const tp_attn_desc ad = layer_attn(d);
+    const tp_mlp_desc md = layer_mlp(d);
+    st = tp_rmsnorm_fwd(T, h, d->eps, TP_BF16, x, g1, L.xn1, L.rstd1, stream);
+    if (st == TP_OK)
+      st = tp_attn_fwd(&ad, L.xn1, Wq, Wk, Wv, Wo, nullptr, x, L.x1,
+                       L.attn_ws, L.attn_bytes, stream);
+    if (st == TP_OK)
+      st = tp_rmsnorm_fwd(T, h, d->eps, TP_BF16, L.x1, g2, L.xn2, L.rstd2,
+                          stream);
+    if (st == TP_OK)
+      st = tp_mlp_fwd(&md, L.xn2, W1, nullptr, W2, nullptr, L.x1, out,
+                      L.mlp_ws, L.mlp_bytes, stream);
+    return st;
+  });
+}
+
+extern "C" tp_status tp_layer_bwd(const tp_layer_desc* d, const void* dout,
+                                  const void* x, const void* g1,
+                                  const void* Wq, const void* Wk,
+                                  const void* Wv, const void* Wo,
+                                  const void* g2, const void* W1,
+                                  const void* W2, const void* ws, void* dx,
+                                  void* dg1, void* dWq, void* dWk, void* dWv,
+                                  void* dWo, void* dg2, void* dW1, void* dW2,
+                                  void* scratch, size_t scratch_bytes,
+                                  tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    tp_status st = check_layer(d);
+    if (st != TP_OK) return st;
+    if (!dout || !x || !g1 || !g2 || !ws || !dx || !dg1 || !dg2 || !scratch)
+      return TP_ERR_NULL;
+    const LayerFwdLayout F = layer_fwd_layout(d, const_cast<void*>(ws));
+    const LayerBwdLayout L = layer_bwd_layout(d, scratch);
+    if (F.bytes == 0 || L.bytes == 0) return TP_ERR_SHAPE;
+    if (scratch_bytes < L.bytes) return TP_ERR_WORKSPACE;
+    const int64_t T = d->b * d->s, h = d->h;
+    const tp_attn_desc ad = layer_attn(d);
+    const tp_mlp_desc md = layer_mlp(d);
+    // MLP block: d(xn2) into dxn, then RMSNorm₂ with the residual's dout
+    st = tp_mlp_bwd(&md, dout, F.xn2, W1, W2, F.mlp_ws, nullptr, L.dxn, dW1,
+                    nullptr, dW2, nullptr, L.blk, L.blk_bytes, stream);
+    if (st == TP_OK)
+      st = tp_rmsnorm_bwd(T, h, d->eps, TP_BF16, L.dxn, F.x1, g2, F.rstd2,
+                          dout, L.dx1, dg2, L.norm, L.norm_bytes, stream);
+    // attention block: d(xn1) into dxn, then RMSNorm₁ with dx1 as residual
+    if (st == TP_OK)
+      st = tp_attn_bwd(&ad, L.dx1, F.xn1, Wq, Wk, Wv, Wo, F.attn_ws, nullptr,
+                       L.dxn, dWq, dWk, dWv, dWo, nullptr, L.blk, L.blk_bytes,
+                       stream);
+    if (st == TP_OK)
+      st = tp_rmsnorm_bwd(T, h, d->eps, TP_BF16, L.dxn, x, g1, F.rstd1, L.dx1,
+                          dx, dg1, L.norm, L.norm_bytes, stream);
+    return st;
+  });
+}

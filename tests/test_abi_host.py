@@ -228,3 +228,44 @@ def test_ds_budget_sets_the_tile_scratch(tp, causal, tiles):
         tp.attn_set_ds_budget(prev)
     assert whole - one == 3 * pair
     assert whole - two == 2 * pair
+
+
+def test_layer_workspaces_are_the_blocks_plus_the_norm_buffers(tp):
+    b, s, h, f, nq, nkv, d, n = 2, 96, 512, 1024, 4, 2, 128, 2
+    T = b * s
+    up = lambda x: (x + 255) // 256 * 256
+    for dt in (tp.BF16, tp.FP8):
+        ld = tp.layer_desc(b, s, h, f, nq, nkv, d, n, dt)
+        aw = tp.attn_workspace_bytes(tp.attn_desc(b, s, h, nq, nkv, d, n, dt))
+        mw = tp.mlp_workspace_bytes(tp.mlp_desc(T, h, f, n, dt, tp.SWIGLU))
+        assert aw > 0 and mw > 0
+        # xn1, x1, xn2 (bf16), rstd1, rstd2 (fp32), attention ws, MLP ws
+        assert tp.layer_workspace_bytes(ld) == (
+            3 * up(T * h * 2) + 2 * up(T * 4) + up(aw) + mw)
+        ab = tp.attn_bwd_scratch_bytes(tp.attn_desc(b, s, h, nq, nkv, d, n, dt))
+        mb = tp.mlp_bwd_scratch_bytes(tp.mlp_desc(T, h, f, n, dt, tp.SWIGLU))
+        nb = tp.rmsnorm_bwd_scratch_bytes(T, h)
+        assert tp.layer_bwd_scratch_bytes(ld) == (
+            2 * up(T * h * 2) + up(nb) + max(ab, mb))
+
+
+def test_layer_rejects_before_launch(tp):
+    L = tp.lib()
+
+    def call(desc, ws_bytes=1 << 40):
+        return L.tp_layer_fwd(ctypes.byref(desc), FAKE, FAKE, FAKE, FAKE, FAKE,
+                              FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws_bytes,
+                              None)
+
+    ok = tp.layer_desc(1, 64, 512, 1024, 4, 2, 128, 2)
+    assert call(ok, ws_bytes=16) == 4                          # ws too small
+    assert call(tp.layer_desc(1, 64, 512, 1024, 4, 2, 128, 2,
+                              dtype=tp.F32)) == 5
+    assert call(tp.layer_desc(1, 64, 512, 1024, 4, 2, 128, 2, eps=0.0)) == 8
+    assert call(tp.layer_desc(1, 64, 512, 1024, 6, 4, 128, 2)) == 2  # GQA
+    assert call(tp.layer_desc(1, 64, 512, 1000, 4, 2, 128, 16)) == 2
+    assert call(tp.layer_desc(0, 64, 512, 1024, 4, 2, 128, 2)) == 2
+    assert L.tp_layer_fwd(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                          FAKE, FAKE, FAKE, FAKE, 1, None) == 1
+    assert tp.layer_workspace_bytes(tp.layer_desc(1, 64, 512, 1024, 6, 4, 128,
+                                                  2)) == 0

@@ -155,3 +155,47 @@ def test_layer_full_size_sparse_upstream(tp):
     print("\n".join(f"{r[0]}: fro {r[1]:.2e} row max/rms {r[2]:.2e}"
                      for r in report))
     assert not failures, "; ".join(failures)
+
+
+@pytest.mark.parametrize("mode", [B.FUSED, B.OVERLAP])
+def test_layer_entry_is_the_composition_of_the_block_entries(tp, mode):
+    # tp_layer_fwd / tp_layer_bwd against the same steps called one by one
+    # through the block entry points: bit-identical
+    from megatron_tensor_transformer_gate_gb300.blocks import TPAttention
+    b, s, h, f, nq, nkv, d, n = 2, 200, 512, 1024, 8, 2, 128, 2
+    cfg = I.workload("layer_bf16", b=b, s=s, h=h, h_ffn=f, n_q=nq, n_kv=nkv,
+                     n=n)
+    x = I.layer_inputs(cfg, 37, "cuda")
+    P = {k: x[k] for k in ("g1", "Wq", "Wk", "Wv", "Wo", "g2", "W1", "W2")}
+    X, dOut = x["X"], x["dOut"]
+    layer = TPLayer(b, s, h, f, nq, nkv, d, n, mode=mode)
+    out = layer.forward(X, P).clone()
+    g = {k: v.clone() for k, v in layer.backward(dOut, X, P).items()}
+    tp.device_status()
+
+    T, eps = b * s, cfg["eps"]
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    attn = TPAttention(b, s, h, nq, nkv, d, n, mode=mode)
+    mlp = TPMLP(T, h, f, n, act=tp.SWIGLU, mode=mode)
+    xn1, x1, xn2 = (torch.empty((T, h), **bf) for _ in range(3))
+    r1, r2 = (torch.empty(T, dtype=torch.float32, device="cuda")
+              for _ in range(2))
+    tp.rmsnorm_fwd(X, P["g1"], xn1, r1, eps)
+    attn.forward(xn1, P["Wq"], P["Wk"], P["Wv"], P["Wo"], R=X, out=x1)
+    tp.rmsnorm_fwd(x1, P["g2"], xn2, r2, eps)
+    ref_out = mlp.forward(xn2, P["W1"], P["W2"], R=x1)
+    ns = torch.empty(tp.rmsnorm_bwd_scratch_bytes(T, h), dtype=torch.uint8,
+                     device="cuda")
+    dxn, dx1 = torch.empty((T, h), **bf), torch.empty((T, h), **bf)
+    ref = {k: torch.empty_like(v) for k, v in g.items()}
+    mlp.backward(dOut, xn2, P["W1"], P["W2"],
+                 grads={"dX": dxn, "dW1": ref["dW1"], "dW2": ref["dW2"]})
+    tp.rmsnorm_bwd(dxn, x1, P["g2"], r2, dx1, ref["dg2"], ns, dres=dOut)
+    attn.backward(dx1, xn1, P["Wq"], P["Wk"], P["Wv"], P["Wo"],
+                  grads={"dX": dxn, "dWq": ref["dWq"], "dWk": ref["dWk"],
+                         "dWv": ref["dWv"], "dWo": ref["dWo"]})
+    tp.rmsnorm_bwd(dxn, X, P["g1"], r1, ref["dX"], ref["dg1"], ns, dres=dx1)
+    tp.device_status()
+    assert out.equal(ref_out)
+    for k in g:
+        assert g[k].equal(ref[k]), k
