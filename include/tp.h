@@ -418,6 +418,14 @@ tp_status tp_profile_read(int32_t family, tp_profile_entry* out);
  * stream failed. */
 tp_status tp_device_status(tp_stream stream);
 const char* tp_status_string(tp_status s);
+/* Failure-path self-test: enqueues one kernel whose single wait (on an
+ * mbarrier that nothing completes) runs through the same bounded wait as
+ * every kernel of this library.  After about two seconds at the maximum SM
+ * clock the wait gives up, the kernel records the timeout and returns; the
+ * next tp_device_status on the stream then returns TP_ERR_DEVICE_TIMEOUT
+ * (and clears the word), and the context stays usable.  Returns TP_OK once
+ * the kernel is enqueued. */
+tp_status tp_selftest_wait_timeout(tp_stream stream);
 /* The CUDA runtime error code behind the latest TP_ERR_CUDA (0 if none
  * yet) and, when name is not NULL, its name (a static string). */
 int32_t tp_last_cuda_error(const char** name);

@@ -137,6 +137,7 @@ SIGNATURES = {
     "tp_status_string": (ctypes.c_char_p, [_I32]),
     "tp_launch_count": (_U64, []),
     "tp_last_cuda_error": (_I32, [ctypes.POINTER(ctypes.c_char_p)]),
+    "tp_selftest_wait_timeout": (_I32, [_P]),
     "tp_num_sms": (_I32, []),
 }
 
@@ -206,6 +207,12 @@ def quantize_fp8(x, q, scale, amax_work, stream=None):
     check(lib().tp_quantize_fp8(x.numel(), ptr(x), ptr(q), ptr(scale),
                                 ptr(amax_work), stream_handle(stream)),
           "tp_quantize_fp8")
+
+
+def selftest_wait_timeout(stream=None):
+    """Enqueue the kernel whose bounded wait runs out (about 2 s)."""
+    check(lib().tp_selftest_wait_timeout(stream_handle(stream)),
+          "tp_selftest_wait_timeout")
 
 
 def gemm_fp8(qa, scale_a, qb, scale_b, C, stream=None):

@@ -1127,6 +1127,14 @@ extern "C" const char* tp_status_string(tp_status s) {
 
 extern "C" uint64_t tp_launch_count(void) { return g_launches.load(); }
 
+extern "C" tp_status tp_selftest_wait_timeout(tp_stream stream) {
+  return guarded([&]() -> tp_status {
+    unsigned* st = device_status_ptr();
+    if (st == nullptr) return TP_ERR_CUDA;
+    return cuda_status(selftest_wait_timeout(st, stream));
+  });
+}
+
 extern "C" int32_t tp_last_cuda_error(const char** name) {
   const int e = g_last_cuda_error.load();
   if (name != nullptr)

@@ -560,4 +560,30 @@ template int rmsnorm_bwd_noalloc<__nv_bfloat16>(const void*, const void*,
                                                 const void*, void*, void*,
                                                 int64_t, int64_t, void*);
 
+// ------------------------------------------------------- bounded waits --
+// One thread waits on an mbarrier that nothing completes, through the same
+// bounded wait every kernel of the library uses: the wait gives up after
+// kWaitTimeoutCycles, records kDevTimeout (site 90) in the status word and
+// the kernel returns, leaving the context usable.
+__global__ void wait_timeout_selftest_kernel(unsigned* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    mbar_wait(&bar, 0, reinterpret_cast<volatile int*>(&abort_flag), status,
+              90);
+}
+
+int selftest_wait_timeout(unsigned* status, void* stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      status);
+  count_launch();
+  return cudaGetLastError();
+}
+
 }  // namespace tp

@@ -51,6 +51,8 @@ int rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* gamma,
 // Per-tensor scaled E4M3 codes of n bf16 values (n a multiple of 8): writes
 // q (n bytes) and the scale (one device float); amax_work is one device word
 // of scratch.  fp8.cu.
+// A kernel whose one wait runs out (the failure path of the bounded waits).
+int selftest_wait_timeout(unsigned* status, void* stream);
 int quantize_fp8(const void* x, int64_t n, void* q, float* scale,
                  unsigned* amax_work, void* stream);
 
