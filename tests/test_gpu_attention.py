@@ -125,3 +125,12 @@ def test_backward_in_passes_is_bit_identical(tp, causal):
     assert scratch[1] < scratch[0]
     for u, v in zip(*res):
         assert u.equal(v)
+
+
+@pytest.mark.parametrize("n_q,n_kv,n", [(8, 8, 2), (32, 2, 2)])
+def test_group_size_extremes(tp, n_q, n_kv, n):
+    # plain multi-head attention (one q head per kv head) and a wide GQA
+    # group of 16 q heads per kv head, ragged s
+    cfg = I.workload("attn_gqa_bf16", b=1, s=260, h=1024, n_q=n_q, n_kv=n_kv,
+                     n=n, w_std="fan_in")
+    run_case(tp, cfg, 0, 38)
