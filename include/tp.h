@@ -32,7 +32,12 @@
  *    stay alive and unmodified between the two.  Gradients are overwritten,
  *    never accumulated into.
  *  - Asynchrony: compute calls only enqueue work on `stream` (a cudaStream_t;
- *    NULL = the legacy default stream) and never synchronise.
+ *    NULL = the legacy default stream) and never synchronise.  A sequence of
+ *    calls can therefore be captured into a CUDA graph and replayed (the
+ *    overlapped mode forks a library-owned stream from `stream` and joins it
+ *    back inside the call, which the capture follows); make the first call
+ *    of each kind before capturing (it sets kernel attributes once), and
+ *    leave event timing (tp_profile_enable) off while capturing.
  *  - Errors: argument, shape and workspace errors are returned before any
  *    launch, with nothing enqueued.  A failed launch returns TP_ERR_CUDA.
  *    Device-side waits are bounded; one that runs out records a device status

@@ -199,3 +199,43 @@ def test_layer_entry_is_the_composition_of_the_block_entries(tp, mode):
     assert out.equal(ref_out)
     for k in g:
         assert g[k].equal(ref[k]), k
+
+
+@pytest.mark.parametrize("mode", [B.FUSED, B.OVERLAP])
+def test_layer_step_replays_from_a_cuda_graph(tp, mode):
+    # the ABI enqueues only (no allocation, no synchronisation), so a whole
+    # forward + backward step captures into one CUDA graph; its replay is
+    # bit-identical to the eager step (the overlapped mode's second stream is
+    # forked and joined inside the capture)
+    import torch
+    b, s, h, f, nq, nkv, d, n = 1, 256, 512, 1024, 8, 2, 128, 2
+    cfg = I.workload("layer_bf16", b=b, s=s, h=h, h_ffn=f, n_q=nq, n_kv=nkv,
+                     n=n)
+    x = I.layer_inputs(cfg, 39, "cuda")
+    P = {k: x[k] for k in ("g1", "Wq", "Wk", "Wv", "Wo", "g2", "W1", "W2")}
+    X, dOut = x["X"], x["dOut"]
+    layer = TPLayer(b, s, h, f, nq, nkv, d, n, mode=mode)
+    ref_out = layer.forward(X, P).clone()
+    ref = {k: v.clone() for k, v in layer.backward(dOut, X, P).items()}
+    tp.device_status()
+    out = torch.empty_like(ref_out)
+    grads = layer.alloc_grads(P)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # warm-up off the default stream
+        layer.forward(X, P, out=out)
+        layer.backward(dOut, X, P, grads=grads)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(X, P, out=out)
+        layer.backward(dOut, X, P, grads=grads)
+    out.zero_()
+    for v in grads.values():
+        v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    tp.device_status()
+    assert out.equal(ref_out)
+    for k in ref:
+        assert grads[k].equal(ref[k]), k
