@@ -134,3 +134,37 @@ def test_group_size_extremes(tp, n_q, n_kv, n):
     cfg = I.workload("attn_gqa_bf16", b=1, s=260, h=1024, n_q=n_q, n_kv=n_kv,
                      n=n, w_std="fan_in")
     run_case(tp, cfg, 0, 38)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_single_token_sequences(tp, causal):
+    # s = 1: each query attends only to its own key (softmax weight 1), so
+    # the block reduces to the V and output projections and dQ, dWq are
+    # exactly 0.  The kernels form dS = P·(dP − D) with D taken from the
+    # stored bf16 O, so dQ is rounding noise instead: it is held against the
+    # scale of dWv (the same product with dV for dQ); everything else
+    # against the oracle as usual
+    b, s, h, nq, nkv, d, n = 2, 1, 512, 4, 2, 128, 2
+    cfg = I.workload("attn_gqa_bf16", b=b, s=s, h=h, n_q=nq, n_kv=nkv, n=n,
+                     causal=causal, w_std="fan_in")
+    x = I.attn_inputs(cfg, 40, "cpu")
+    dv = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    a = TPAttention(b, s, h, nq, nkv, d, n, causal=causal)
+    out = a.forward(dv["X"], dv["Wq"], dv["Wk"], dv["Wv"], dv["Wo"])
+    g = a.backward(dv["dOut"], dv["X"], dv["Wq"], dv["Wk"], dv["Wv"],
+                   dv["Wo"])
+    tp.device_status()
+    f = {k: I.to_f64(v) for k, v in x.items()}
+    kw = dict(b=b, s=s, n_q=nq, n_kv=nkv, d=d, causal=causal)
+    fo = oracle.attention_forward(f["X"], f["Wq"], f["Wk"], f["Wv"], f["Wo"],
+                                  **kw)
+    go = oracle.attention_backward(f["dOut"], f["X"], f["Wq"], f["Wk"],
+                                   f["Wv"], f["Wo"], fo, **kw)
+    assert np.abs(go["dWq"]).max() == 0.0
+    check(out, fo["Out"], "Out")
+    for k in ("dX", "dWv", "dWo"):
+        check(g[k], go[k], k)
+    scale = np.linalg.norm(go["dWv"])
+    for k in ("dWq", "dWk"):
+        err = np.linalg.norm(g[k].double().cpu().numpy() - go[k])
+        assert err <= 1e-2 * scale, (k, err / scale)

@@ -7,7 +7,7 @@ import torch
 import oracle
 from megatron_tensor_transformer_gate_gb300 import inputs as I
 from megatron_tensor_transformer_gate_gb300.blocks import TPMLP
-from _parity import check, f64
+from _parity import check, check_fro, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -173,3 +173,41 @@ def test_partial_last_wave_in_the_mlp(tp, act):
     cfg = I.workload("mlp_gelu_bf16", b=1, s=2560, h=512, h_ffn=2048, n=2,
                      act=act, b1=(act == "gelu"), p=0.0, w_std="fan_in")
     run_case(tp, cfg, 0, 9)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_single_token(tp, act):
+    # T = 1: one row through every GEMM (a 256-row pair tile with 255 rows
+    # past the end), bias, dropout and residual.  Each weight gradient is
+    # then one outer product, row j scaled by the hidden unit's dH[0, j],
+    # which cancels to near 0 where the activation's derivative does; the
+    # row-wise bound does not apply to such rows, so the weight gradients
+    # are held to the Frobenius bound (Out, dX and the bias gradients to
+    # both)
+    cfg = I.workload("mlp_gelu_bf16", b=1, s=1, h=256, h_ffn=512, n=2,
+                     act=act, b1=(act == "gelu"), b2=True, residual="X",
+                     p=0.1 if act == "gelu" else 0.0, w_std="fan_in")
+    T = 1
+    x = I.mlp_inputs(cfg, 41, "cpu")
+    a = tp.GELU if act == "gelu" else tp.SWIGLU
+    m = TPMLP(T, cfg["h"], cfg["h_ffn"], cfg["n"], act=a, mode=1,
+              dropout_p=cfg["p"], seed=41)
+    d = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    out = m.forward(d["X"], d["W1"], d["W2"], b1=d["b1"], b2=d["b2"],
+                    R=d["X"])
+    g = m.backward(d["dOut"], d["X"], d["W1"], d["W2"], dres=d["dOut"],
+                   want_db1=x["b1"] is not None, want_db2=True)
+    tp.device_status()
+    X, W1, W2 = I.to_f64(x["X"]), I.to_f64(x["W1"]), I.to_f64(x["W2"])
+    kw = dict(act=act, p=cfg["p"], seed=41)
+    fo = oracle.mlp_forward(X, W1, W2, b1=I.to_f64(x["b1"]),
+                            b2=I.to_f64(x["b2"]), R=X, **kw)
+    go = oracle.mlp_backward(I.to_f64(x["dOut"]), X, W1, W2, fo,
+                             dres=I.to_f64(x["dOut"]), **kw)
+    check(out, fo["Out"], "Out")
+    check(g["dX"], go["dX"], "dX")
+    for k in ("db1", "db2"):
+        if k in g:
+            check(g[k], go[k], k)
+    for k in ("dW1", "dW2"):
+        check_fro(g[k], go[k], k)
