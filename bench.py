@@ -255,6 +255,22 @@ def cpu_sample_cfg(cfg):
     return s
 
 
+def oracle_flops_per_step(scfg):
+    """FLOPs of one fwd + bwd step of the sample, counted by the oracle's
+    own accountant (the oracle arm maps no product library)."""
+    import oracle
+    k = scfg["kind"]
+    if k == "layer":
+        return sum(oracle.layer_flops(scfg["b"], scfg["s"], scfg["h"],
+                                      scfg["h_ffn"], scfg["n_q"],
+                                      scfg["n_kv"], scfg["d"]))
+    if k == "mlp":
+        return sum(oracle.mlp_flops(scfg["b"] * scfg["s"], scfg["h"],
+                                    scfg["h_ffn"], scfg["act"]))
+    return sum(oracle.attn_flops(scfg["b"], scfg["s"], scfg["h"],
+                                 scfg["n_q"], scfg["n_kv"], scfg["d"]))
+
+
 def run_oracle_step(scfg, xs):
     import oracle
     k = scfg["kind"]
@@ -312,7 +328,7 @@ def cpu_baseline(cfg, seed, min_seconds=10.0, max_steps=30):
     of host work have run (at least one step)."""
     scfg = cpu_sample_cfg(cfg)
     xs = oracle_inputs(scfg, seed)
-    fl = flops_per_step(scfg)
+    fl = oracle_flops_per_step(scfg)
     steps, t0 = 0, time.perf_counter()
     while True:
         run_oracle_step(scfg, xs)
@@ -365,7 +381,7 @@ def reference_arm(args, cfg, world, rank):
         return
     scfg = cpu_sample_cfg(cfg)
     xs = oracle_inputs(scfg, 20260000)
-    fl = flops_per_step(scfg)
+    fl = oracle_flops_per_step(scfg)
     for _ in range(args.warmup):
         run_oracle_step(scfg, xs)
     t0 = time.perf_counter()

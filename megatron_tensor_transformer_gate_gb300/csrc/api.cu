@@ -661,7 +661,9 @@ struct AttnBwdLayout {
 
 AttnShape attn_shape(const tp_attn_desc* d);
 
-AttnBwdLayout attn_bwd_layout(const tp_attn_desc* d, void* scratch) {
+// `sh` carries the dS pairs per pass, fixed once per call (attn_shape).
+AttnBwdLayout attn_bwd_layout(const tp_attn_desc* d, const AttnShape& sh,
+                              void* scratch) {
   AttnBwdLayout L;
   Carver c(scratch);
   const size_t T = (size_t)d->b * (size_t)d->s;
@@ -673,7 +675,7 @@ AttnBwdLayout attn_bwd_layout(const tp_attn_desc* d, void* scratch) {
   const size_t stats = (size_t)d->b * d->n_q * attn_stats_pad(d->s) * 4;
   L.D = static_cast<float*>(c.take(stats));
   L.L2 = static_cast<float*>(c.take(stats));
-  L.dS = c.take((size_t)attn_ds_bytes(attn_shape(d)));
+  L.dS = c.take((size_t)attn_ds_bytes(sh));
   if (d->mode != TP_REDUCE_FUSED)
     L.partials = c.take((size_t)d->n * T * (size_t)d->h * 2);
   L.colsum = static_cast<float*>(c.take(colsum_scratch_bytes(T, d->h)));
@@ -690,6 +692,7 @@ AttnShape attn_shape(const tp_attn_desc* d) {
   sh.d = d->d;
   sh.causal = d->causal ? 1 : 0;
   sh.scale = 1.0f / std::sqrt((float)d->d);
+  sh.ds_pairs = attn_ds_pairs_per_pass(sh);   // the one read of the budget
   return sh;
 }
 
@@ -717,7 +720,7 @@ extern "C" size_t tp_attn_workspace_bytes(const tp_attn_desc* d) {
 
 extern "C" size_t tp_attn_bwd_scratch_bytes(const tp_attn_desc* d) {
   if (check_attn(d) != TP_OK) return 0;
-  return attn_bwd_layout(d, nullptr).bytes;
+  return attn_bwd_layout(d, attn_shape(d), nullptr).bytes;
 }
 
 extern "C" tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X,
@@ -826,7 +829,10 @@ extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
         !opt_aligned(dres) || !opt_aligned(dbo))
       return TP_ERR_ARG;
     const AttnFwdLayout F = attn_fwd_layout(d, const_cast<void*>(ws));
-    const AttnBwdLayout L = attn_bwd_layout(d, scratch);
+    // one shape (and one read of the dS budget) for the layout and the
+    // kernels, so the tiles written always fit the carved region
+    const AttnShape sh = attn_shape(d);
+    const AttnBwdLayout L = attn_bwd_layout(d, sh, scratch);
     if (scratch_bytes < L.bytes) return TP_ERR_WORKSPACE;
     const int64_t T = d->b * d->s, h = d->h;
     const int64_t qd = (int64_t)d->n_q * d->d, kd = (int64_t)d->n_kv * d->d;
@@ -846,7 +852,7 @@ extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
                           qd),
                      stream);
     if (err) return cuda_status(err);
-    err = flash_bwd(attn_shape(d), F.q, F.k, F.v, F.o, L.dO, F.lse, L.D, L.L2,
+    err = flash_bwd(sh, F.q, F.k, F.v, F.o, L.dO, F.lse, L.D, L.L2,
                     L.dS, L.dQ, L.dK, L.dV, device_status_ptr(), stream);
     if (err) return cuda_status(err);
     err = run_gemm(proj(qd, h, op(L.dQ, qd, 1, qd), op(X, h, 1, h), T, dWq, h),

@@ -13,6 +13,10 @@ struct AttnShape {
   int nq, nkv, d;
   int causal;
   float scale;  // 1/√d
+  // Backward only: (batch, kv head) pairs whose dS tiles are held at once,
+  // fixed when the caller's scratch is carved (attn_ds_pairs_per_pass) so
+  // that the tile region and the passes of flash_bwd agree.
+  int64_t ds_pairs = 0;
 };
 
 // Forward on tcgen05 (attn_fwd_tc.cu); Q, K, V fp16, O bf16.
@@ -22,8 +26,12 @@ int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
 // Dp and L2p are fp32 scratch of b·nq·attn_stats_pad(s) elements each
 // (D = rowsum(dO∘O) and LSE·log2e, zero-padded); dO is fp16.  dS is
 // attn_ds_bytes(sh) bytes of scratch (16-byte aligned) for the fp16 score
-// gradient tiles that the dK/dV kernel writes and the dQ kernel reads.
+// gradient tiles that the dK/dV kernel writes and the dQ kernel reads; the
+// backward runs in passes of sh.ds_pairs (batch, kv head) pairs.
 int64_t attn_stats_pad(int64_t s);
+// Pairs per pass under the current budget (read once; at least one).
+int64_t attn_ds_pairs_per_pass(const AttnShape& sh);
+// Bytes of dS tiles for sh.ds_pairs pairs.
 int64_t attn_ds_bytes(const AttnShape& sh);
 // Bound on the dS tile bytes per pass (0 = the default 8 GiB); returns the
 // previous bound.

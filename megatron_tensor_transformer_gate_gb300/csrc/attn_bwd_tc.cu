@@ -761,26 +761,27 @@ int64_t ds_pair_bytes(const AttnShape& sh) {
 // bytes (at least one), so the scratch stays bounded for long sequences
 constexpr int64_t kDsBudgetDefault = int64_t(8) << 30;
 std::atomic<int64_t> g_ds_budget{kDsBudgetDefault};
-int64_t ds_pairs_per_pass(const AttnShape& sh) {
+}  // namespace
+
+int64_t attn_ds_pairs_per_pass(const AttnShape& sh) {
   return std::max<int64_t>(
       1, std::min<int64_t>(sh.b * sh.nkv,
                            g_ds_budget.load() / ds_pair_bytes(sh)));
 }
-}  // namespace
 
 int64_t attn_set_ds_budget(int64_t bytes) {
   return g_ds_budget.exchange(bytes > 0 ? bytes : kDsBudgetDefault);
 }
 
 int64_t attn_ds_bytes(const AttnShape& sh) {
-  return ds_pairs_per_pass(sh) * ds_pair_bytes(sh);
+  return sh.ds_pairs * ds_pair_bytes(sh);
 }
 
 int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
               const void* O, const void* dO, const float* LSE, float* Dp,
               float* L2p, void* dS, void* dQ, void* dK, void* dV,
               unsigned* status, void* stream) {
-  if (sh.d != HD) return cudaErrorInvalidValue;
+  if (sh.d != HD || sh.ds_pairs < 1) return cudaErrorInvalidValue;
   static cudaError_t e1 = cudaFuncSetAttribute(
       attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
       dq::SMEM);
@@ -842,7 +843,9 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   sms = std::max(sms, 1);
   const int64_t pairs_all = sh.b * sh.nkv;
-  const int64_t chunk = ds_pairs_per_pass(sh);
+  // the pairs the caller's dS region was carved for (never the budget,
+  // which another thread may have changed since)
+  const int64_t chunk = std::min<int64_t>(sh.ds_pairs, pairs_all);
   const int64_t nblk = (sh.s + 127) / 128;
   const int group = sh.nq / sh.nkv;
   int passes = 0;

@@ -85,6 +85,12 @@ def _normal(shape, std, seed, device, dtype, mean=0.0):
     return t.to(dtype)
 
 
+def normal(shape, std, seed, device="cpu", dtype=torch.bfloat16, mean=0.0):
+    """A seeded N(mean, std²) tensor rounded to ``dtype`` (the draw every
+    workload tensor uses)."""
+    return _normal(shape, std, seed, device, dtype, mean)
+
+
 def _std(cfg, fan_in):
     w = cfg["w_std"]
     return fan_in ** -0.5 if w == "fan_in" else float(w)

@@ -269,3 +269,24 @@ def test_layer_rejects_before_launch(tp):
                           FAKE, FAKE, FAKE, FAKE, 1, None) == 1
     assert tp.layer_workspace_bytes(tp.layer_desc(1, 64, 512, 1024, 6, 4, 128,
                                                   2)) == 0
+
+
+def test_ds_budget_is_read_once_per_backward_call(tp):
+    # the dS tile region and the backward's passes come from one read of the
+    # budget inside the call: scratch sized under a small budget is rejected
+    # (before any launch) once the budget has grown, instead of being
+    # written past its dS region by passes sized for the larger budget
+    L = tp.lib()
+    d = tp.attn_desc(2, 200, 512, 8, 2, 128, 2)
+    prev = tp.attn_set_ds_budget(1)            # one (batch, kv head) pair
+    try:
+        one = tp.attn_bwd_scratch_bytes(d)
+        tp.attn_set_ds_budget(0)               # default: all four pairs
+        assert tp.attn_bwd_scratch_bytes(d) > one
+        n0 = tp.launch_count()
+        rc = L.tp_attn_bwd(ctypes.byref(d), *([FAKE] * 7), None,
+                           *([FAKE] * 5), None, FAKE, one, None)
+        assert rc == 4                          # TP_ERR_WORKSPACE
+        assert tp.launch_count() == n0
+    finally:
+        tp.attn_set_ds_budget(prev)

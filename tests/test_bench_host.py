@@ -2,6 +2,7 @@
 DRAM traffic taken from a committed ncu capture."""
 
 import hashlib
+import json
 import os
 import sys
 
@@ -61,3 +62,33 @@ def test_committed_gemm_capture_is_well_formed():
     traffic, note = bench.committed_traffic("gemm_tc", "layer_bf16")
     # either current (bytes per launch) or flagged stale, never an exception
     assert (traffic is not None and traffic > 0) or "stale" in note
+
+
+def test_reference_arm_maps_no_product_library():
+    # the oracle arm counts its FLOPs with the oracle's own accountant: after
+    # a full run of the arm, libtp.so is not mapped into the process
+    import subprocess
+    code = (
+        "import sys, json; sys.argv = ['bench.py', '--impl', 'reference', "
+        "'--workload', 'mlp_gelu_bf16', '--steps', '1', '--warmup', '0']\n"
+        "import bench; bench.main()\n"
+        "maps = open('/proc/self/maps').read()\n"
+        "print('LIBTP' if 'libtp.so' in maps else 'CLEAN')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = r.stdout.strip().splitlines()
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert lines[-1] == "CLEAN"
+
+
+def test_oracle_flop_count_equals_the_library_accountant(tp):
+    # the two counts agree bit for bit on every workload's bench sample and
+    # on the full workloads
+    from megatron_tensor_transformer_gate_gb300 import inputs as I
+    for name in ("layer_bf16", "mlp_swiglu_bf16", "mlp_gelu_bf16",
+                 "attn_gqa_bf16"):
+        cfg = I.workload(name)
+        for c in (cfg, bench.cpu_sample_cfg(cfg)):
+            assert bench.oracle_flops_per_step(c) == bench.flops_per_step(c)

@@ -6,6 +6,8 @@ import math
 import os
 
 import numpy as np
+
+import oracle
 import pytest
 
 from oracle import fp8
@@ -157,3 +159,81 @@ def test_fp8_attention_forward_bias_and_residual():
     plain = fp8.attention_forward(X, Wq, Wk, Wv, Wo, **kw)
     full = fp8.attention_forward(X, Wq, Wk, Wv, Wo, bo=bo, R=R, **kw)
     assert np.array_equal(full["Out"], plain["Z"] + bo + R)
+
+
+# ---------------------------------------------------------------------------
+# The FP8 layer (oracle.layer_forward(fp8=True)) on a structured tiny layer
+# whose every step has a closed form.  b = 1, s = 2, h = d = h_ffn = 8, one q
+# and one kv head, γ1 = γ2 = 1, x = c·σ with sign rows σ0 = (+1)^8 and
+# σ1 = (+1)^4 (−1)^4 (σ0·σ1 = 0, both +1 in column 0).
+#  * Wq = Wk = 64·I: the two tokens' scores differ by ~1.1e4 ≫ 745, so the
+#    causal softmax is exactly one-hot on the diagonal in fp64 and O = V.
+#  * Wv = I, Wo = w·I (w a power of two): O and the attention output keep
+#    the sign pattern, so each quantized activation has one magnitude a: its
+#    E4M3 codes are ±448 and it dequantizes to D(a) = 448 / s(a) with the
+#    fp32 scale s(a) = fp32(448 / a).  Every weight is a power of two or 0,
+#    which its per-tensor scale maps exactly.
+#  * W1 = [64 on column 0 of every gate row; I for the up rows]: G = 64·D2
+#    (≥ 37, where σ(G) = 1 in fp64, so SiLU(G) = G), U = D2·σ,
+#    A = 64·D2²·σ.  W2 = 2⁻⁶·I.
+# With m̂ = bf16(c/√(c² + ε)) the stored first norm output, D1 = D(m̂),
+# r1 = c + w·D1 (x1 = r1·σ), m̂2 = bf16(r1/√(r1² + ε)) the stored second norm
+# output, D2 = D(m̂2) and D3 = D(64·bf16(D2²)):
+#     Out = σ·(r1 + 2⁻⁶·D3).
+# Quantizing a norm output before its bf16 rounding would put the unrounded
+# magnitude in place of m̂ or m̂2 (ε > 0 makes them differ by ~1e-3), and
+# feeding the MLP any tensor other than the stored second norm output breaks
+# the closed form.
+# ---------------------------------------------------------------------------
+def _dequant_uniform(a):
+    """The value a tensor of one magnitude a (exact in fp32) dequantizes to."""
+    return 448.0 / float(np.float32(448.0) / np.float32(a))
+
+
+def _structured_layer(c, w, eps, round_norms=True):
+    from oracle.fp8 import round_bf16
+    rnd = (lambda v: float(round_bf16(v))) if round_norms else float
+    h = 8
+    sig = np.array([[1.0] * 8, [1.0] * 4 + [-1.0] * 4])
+    I8 = np.eye(h)
+    Wg = np.zeros((h, h))
+    Wg[:, 0] = 64.0
+    P = {"g1": np.ones(h), "g2": np.ones(h), "Wq": 64.0 * I8,
+         "Wk": 64.0 * I8, "Wv": I8.copy(), "Wo": w * I8,
+         "W1": np.concatenate([Wg, I8]), "W2": 2.0 ** -6 * I8}
+    x = c * sig
+    r1 = c + w * _dequant_uniform(rnd(c / np.sqrt(c * c + eps)))
+    d2 = _dequant_uniform(rnd(r1 / np.sqrt(r1 * r1 + eps)))
+    d3 = _dequant_uniform(64.0 * float(round_bf16(d2 * d2)))
+    closed = sig * (r1 + 2.0 ** -6 * d3)
+    shp = dict(b=1, s=2, n_q=1, n_kv=1, d=8, eps=eps)
+    return x, P, shp, closed
+
+
+def test_fp8_layer_equals_the_plain_layer_when_every_quantization_is_exact():
+    # ε = 0: every norm output is ±1 (exact in bf16 and E4M3), every weight a
+    # power of two or 0, so the FP8 layer is the plain layer: Out = (c+w+1)σ
+    x, P, shp, closed = _structured_layer(c=1.0, w=2.0, eps=0.0)
+    f8 = oracle.layer_forward(x, P, fp8=True, **shp)
+    plain = oracle.layer_forward(x, P, **shp)
+    np.testing.assert_allclose(f8["Out"], plain["Out"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(f8["Out"], closed, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(closed[:, 0], 4.0)
+    # the first block quantized the ±1 norm output: scale 448 / 1
+    assert f8["attn"]["scales"][0] == np.float32(448.0)
+
+
+@pytest.mark.parametrize("c,w,eps", [(1.0, 2.0, 1e-2), (2.0, 0.5, 0.3),
+                                     (0.5, 4.0, 1e-3)])
+def test_fp8_layer_quantizes_each_norm_output_as_stored_in_bf16(c, w, eps):
+    from oracle.fp8 import round_bf16
+    x, P, shp, closed = _structured_layer(c, w, eps)
+    f8 = oracle.layer_forward(x, P, fp8=True, **shp)
+    np.testing.assert_allclose(f8["Out"], closed, rtol=0, atol=1e-12)
+    # with the norm outputs quantized unrounded the closed form moves by far
+    # more than the tolerance
+    _, _, _, unrounded = _structured_layer(c, w, eps, round_norms=False)
+    assert np.abs(unrounded - closed).max() > 1e-4
+    # per-tensor scale of the quantized first norm output: 448 / bf16(amax)
+    m_hat = float(round_bf16(c / np.sqrt(c * c + eps)))
+    assert f8["attn"]["scales"][0] == np.float32(448.0) / np.float32(m_hat)
