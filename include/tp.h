@@ -78,8 +78,20 @@ typedef enum { TP_GELU = 0, TP_SWIGLU = 1 } tp_act;
  * the result equals TP_REDUCE_MATERIALISED bit for bit.  The library creates
  * that stream (one per device) and orders it against the caller's stream
  * with events; the call returns with all work ordered on `stream`. */
+/* TP_REDUCE_SP: Megatron sequence parallelism ([Troverld] §III.III).  Each
+ * all-reduce becomes a reduce-scatter to the ranks' T/n token rows, the
+ * token-wise ops run on those rows, and an all-gather hands the whole
+ * activation to the next column-parallel GEMM; on one device the gathered
+ * buffer is the reduced one.  A block call computes what
+ * TP_REDUCE_MATERIALISED computes (its token-wise ops — bias, dropout,
+ * residual — already run inside the reduce).  In a layer call the next
+ * block's RMSNorm joins the reduction: forward, one pass sums the attention
+ * partials, adds the residual, writes x1 and the second RMSNorm's output;
+ * backward, each f reduction is summed inside the RMSNorm backward kernel.
+ * Results equal TP_REDUCE_MATERIALISED bit for bit, with one [T, h] write
+ * and read fewer per fused reduction. */
 typedef enum { TP_REDUCE_FUSED = 0, TP_REDUCE_MATERIALISED = 1,
-               TP_REDUCE_OVERLAP = 2 } tp_reduce_mode;
+               TP_REDUCE_OVERLAP = 2, TP_REDUCE_SP = 3 } tp_reduce_mode;
 typedef enum { TP_SCOPE_MLP = 0, TP_SCOPE_ATTN = 1, TP_SCOPE_LAYER = 2 } tp_scope;
 
 typedef void* tp_stream; /* cudaStream_t */
@@ -263,7 +275,17 @@ typedef struct {
 /* ws: saved for backward — RMSNorm₁ output, x1, RMSNorm₂ output (bf16
  * [T, h]), rstd₁, rstd₂ (fp32 [T]), then the attention block's ws and the
  * MLP block's ws (tp_attn_workspace_bytes, tp_mlp_workspace_bytes of the
- * blocks' descs); each region on the next 256-byte boundary. */
+ * blocks' descs); for TP_BF16 then the forward's fp16 operands of the Q, K,
+ * V projections: the RMSNorm₁ output [T, h] and Wq, Wk, Wv.  Each region on
+ * the next 256-byte boundary.
+ * Precision (TP_BF16): the Q, K, V projections multiply fp16 copies of the
+ * RMSNorm₁ output and of Wq, Wk, Wv (fp32 accumulation).  The softmax
+ * multiplies the relative error of its input's rounding by the score scale
+ * (a few units at the layer workload), and fp16 carries 3 more mantissa bits
+ * than bf16; a norm output is bounded by √h·max|γ|, so fp16's range holds it
+ * for |γ| ≤ 65504/√h.  A weight beyond ±65504 reports TP_ERR_RANGE through
+ * tp_device_status; weights below 2^-14 in magnitude lose precision
+ * (fp16 subnormals). */
 size_t tp_layer_workspace_bytes(const tp_layer_desc* d);
 /* scratch: the two block gradients' [T, h] hand-overs (bf16), the RMSNorm
  * scratch, then the larger of the attention and MLP backward scratches

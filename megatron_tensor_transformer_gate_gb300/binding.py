@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(PKG, "libtp.so")
 
 F32, BF16, FP8 = 0, 1, 2
 GELU, SWIGLU = 0, 1
-FUSED, MATERIALISED, OVERLAP = 0, 1, 2
+FUSED, MATERIALISED, OVERLAP, SP = 0, 1, 2, 3
 SCOPE_MLP, SCOPE_ATTN, SCOPE_LAYER = 0, 1, 2
 
 STATUS = {0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_DTYPE",

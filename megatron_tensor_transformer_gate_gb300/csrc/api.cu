@@ -169,7 +169,7 @@ tp_status check_mlp(const tp_mlp_desc* d) {
     return TP_ERR_DTYPE;
   if (d->act != TP_GELU && d->act != TP_SWIGLU) return TP_ERR_DTYPE;
   if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED &&
-      d->mode != TP_REDUCE_OVERLAP)
+      d->mode != TP_REDUCE_OVERLAP && d->mode != TP_REDUCE_SP)
     return TP_ERR_DTYPE;
   if (d->T < 1 || d->h < 8 || d->h_ffn < 8 || d->n < 1) return TP_ERR_SHAPE;
   if (d->T > (1 << 30) || d->h > (1 << 20) || d->h_ffn > (1 << 24))
@@ -460,12 +460,35 @@ extern "C" tp_status tp_mlp_fwd(const tp_mlp_desc* d, const void* X,
   });
 }
 
+namespace {
+// leave_partials (non-fused modes): the f reduction's shard partials of dX
+// are left in the scratch and their address reported to the caller; dX and
+// dres are not touched.
+tp_status mlp_bwd_impl(const tp_mlp_desc* d, const void* dOut, const void* X,
+                       const void* W1, const void* W2, const void* ws,
+                       const void* dres, void* dX, void* dW1, void* db1,
+                       void* dW2, void* db2, void* scratch,
+                       size_t scratch_bytes, tp_stream stream,
+                       void** leave_partials);
+}  // namespace
+
 extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
                                 const void* X, const void* W1, const void* W2,
                                 const void* ws, const void* dres, void* dX,
                                 void* dW1, void* db1, void* dW2, void* db2,
                                 void* scratch, size_t scratch_bytes,
                                 tp_stream stream) {
+  return mlp_bwd_impl(d, dOut, X, W1, W2, ws, dres, dX, dW1, db1, dW2, db2,
+                      scratch, scratch_bytes, stream, nullptr);
+}
+
+namespace {
+tp_status mlp_bwd_impl(const tp_mlp_desc* d, const void* dOut, const void* X,
+                       const void* W1, const void* W2, const void* ws,
+                       const void* dres, void* dX, void* dW1, void* db1,
+                       void* dW2, void* db2, void* scratch,
+                       size_t scratch_bytes, tp_stream stream,
+                       void** leave_partials) {
   return guarded([&]() -> tp_status {
     tp_status st = check_mlp(d);
     if (st != TP_OK) return st;
@@ -581,11 +604,16 @@ extern "C" tp_status tp_mlp_bwd(const tp_mlp_desc* d, const void* dOut,
     gx.nz = n;
     gx.epi.out = L.partials;
     gx.epi.out_z_stride = T * h;
+    if (leave_partials) {
+      *leave_partials = L.partials;
+      return cuda_status(run_gemm(gx, stream));
+    }
     return cuda_status(gemm_and_reduce(gx, sdt, L.partials, n, T, h, nullptr,
                                        dres, dX, DropoutSpec(), d->mode,
                                        stream));
   });
 }
+}  // namespace
 
 // ------------------------------------------------------------- attention --
 namespace {
@@ -595,7 +623,7 @@ tp_status check_attn(const tp_attn_desc* d) {
   if (d->dtype != TP_F32 && d->dtype != TP_BF16 && d->dtype != TP_FP8)
     return TP_ERR_DTYPE;
   if (d->mode != TP_REDUCE_FUSED && d->mode != TP_REDUCE_MATERIALISED &&
-      d->mode != TP_REDUCE_OVERLAP)
+      d->mode != TP_REDUCE_OVERLAP && d->mode != TP_REDUCE_SP)
     return TP_ERR_DTYPE;
   if (d->b < 1 || d->s < 1 || d->h < 8 || d->n_q < 1 || d->n_kv < 1 ||
       d->d < 1 || d->n < 1)
@@ -723,11 +751,41 @@ extern "C" size_t tp_attn_bwd_scratch_bytes(const tp_attn_desc* d) {
   return attn_bwd_layout(d, attn_shape(d), nullptr).bytes;
 }
 
+namespace {
+// fp16 copies of the Q, K, V projections' operands: the input rows and the
+// three weights.  The layer passes them for its first block, whose input is
+// the RMSNorm output: the softmax amplifies the rounding of that input
+// (scores of a few units times its relative error), and fp16 keeps 3 more
+// mantissa bits than bf16 at the same bytes.
+struct QkvF16 {
+  const void *x = nullptr, *wq = nullptr, *wk = nullptr, *wv = nullptr;
+};
+
+tp_status attn_fwd_impl(const tp_attn_desc* d, const void* X, const void* Wq,
+                        const void* Wk, const void* Wv, const void* Wo,
+                        const void* bo, const void* R, void* Out, void* ws,
+                        size_t ws_bytes, tp_stream stream,
+                        const QkvF16* f16in, void** leave_partials = nullptr);
+}  // namespace
+
 extern "C" tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X,
                                  const void* Wq, const void* Wk,
                                  const void* Wv, const void* Wo,
                                  const void* bo, const void* R, void* Out,
                                  void* ws, size_t ws_bytes, tp_stream stream) {
+  return attn_fwd_impl(d, X, Wq, Wk, Wv, Wo, bo, R, Out, ws, ws_bytes, stream,
+                       nullptr);
+}
+
+namespace {
+// leave_partials (non-fused modes): stop after the output projection's
+// shard partials are written and report where they are (the caller reduces
+// them).
+tp_status attn_fwd_impl(const tp_attn_desc* d, const void* X, const void* Wq,
+                        const void* Wk, const void* Wv, const void* Wo,
+                        const void* bo, const void* R, void* Out, void* ws,
+                        size_t ws_bytes, tp_stream stream,
+                        const QkvF16* f16in, void** leave_partials) {
   return guarded([&]() -> tp_status {
     tp_status st = check_attn(d);
     if (st != TP_OK) return st;
@@ -762,6 +820,13 @@ extern "C" tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X,
     GemmProblem gv = proj(T, kd, op(xa, h, 0, T), op(f8 ? L.wvq : Wv, h, 0, kd),
                           h, L.v, kd);
     gq.epi.out_f16 = gk.epi.out_f16 = gv.epi.out_f16 = 1;
+    if (f16in != nullptr && !f8) {
+      gq.parts[0].a.ptr = gk.parts[0].a.ptr = gv.parts[0].a.ptr = f16in->x;
+      gq.parts[0].b.ptr = f16in->wq;
+      gk.parts[0].b.ptr = f16in->wk;
+      gv.parts[0].b.ptr = f16in->wv;
+      gq.f16 = gk.f16 = gv.f16 = 1;
+    }
     if (f8) {
       GemmProblem* gs[3] = {&gq, &gk, &gv};
       for (int i = 0; i < 3; ++i) {
@@ -804,10 +869,29 @@ extern "C" tp_status tp_attn_fwd(const tp_attn_desc* d, const void* X,
     g.nz = n;
     g.epi.out = L.partials;
     g.epi.out_z_stride = T * h;
+    if (leave_partials) {
+      *leave_partials = L.partials;
+      return cuda_status(run_gemm(g, stream));
+    }
     return cuda_status(gemm_and_reduce(g, TP_BF16, L.partials, n, T, h, bo, R,
                                        Out, DropoutSpec(), d->mode, stream));
   });
 }
+
+}  // namespace
+
+namespace {
+// leave_partials (non-fused modes): the f reduction's shard partials of dX
+// are left in the scratch and their address reported to the caller; dX and
+// dres are not touched.
+tp_status attn_bwd_impl(const tp_attn_desc* d, const void* dOut,
+                        const void* X, const void* Wq, const void* Wk,
+                        const void* Wv, const void* Wo, const void* ws,
+                        const void* dres, void* dX, void* dWq, void* dWk,
+                        void* dWv, void* dWo, void* dbo, void* scratch,
+                        size_t scratch_bytes, tp_stream stream,
+                        void** leave_partials);
+}  // namespace
 
 extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
                                  const void* X, const void* Wq, const void* Wk,
@@ -816,6 +900,18 @@ extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
                                  void* dWq, void* dWk, void* dWv, void* dWo,
                                  void* dbo, void* scratch,
                                  size_t scratch_bytes, tp_stream stream) {
+  return attn_bwd_impl(d, dOut, X, Wq, Wk, Wv, Wo, ws, dres, dX, dWq, dWk,
+                       dWv, dWo, dbo, scratch, scratch_bytes, stream, nullptr);
+}
+
+namespace {
+tp_status attn_bwd_impl(const tp_attn_desc* d, const void* dOut,
+                        const void* X, const void* Wq, const void* Wk,
+                        const void* Wv, const void* Wo, const void* ws,
+                        const void* dres, void* dX, void* dWq, void* dWk,
+                        void* dWv, void* dWo, void* dbo, void* scratch,
+                        size_t scratch_bytes, tp_stream stream,
+                        void** leave_partials) {
   return guarded([&]() -> tp_status {
     tp_status st = check_attn(d);
     if (st != TP_OK) return st;
@@ -890,11 +986,16 @@ extern "C" tp_status tp_attn_bwd(const tp_attn_desc* d, const void* dOut,
     g.nz = n;
     g.epi.out = L.partials;
     g.epi.out_z_stride = T * h;
+    if (leave_partials) {
+      *leave_partials = L.partials;
+      return cuda_status(run_gemm(g, stream));
+    }
     return cuda_status(gemm_and_reduce(g, TP_BF16, L.partials, n, T, h,
                                        nullptr, dres, dX, DropoutSpec(),
                                        d->mode, stream));
   });
 }
+}  // namespace
 
 // -------------------------------------------------------------- RMSNorm --
 extern "C" tp_status tp_rmsnorm_fwd(int64_t T, int64_t h, float eps,
@@ -1204,6 +1305,9 @@ struct LayerFwdLayout {
   void *xn1 = nullptr, *x1 = nullptr, *xn2 = nullptr;
   float *rstd1 = nullptr, *rstd2 = nullptr;
   void *attn_ws = nullptr, *mlp_ws = nullptr;
+  // bf16 mode: fp16 copies of the first norm's output and of Wq, Wk, Wv,
+  // the operands of the Q, K, V projections (forward only)
+  void *xn1h = nullptr, *wqh = nullptr, *wkh = nullptr, *wvh = nullptr;
   size_t attn_bytes = 0, mlp_bytes = 0, bytes = 0;
 };
 
@@ -1224,6 +1328,13 @@ LayerFwdLayout layer_fwd_layout(const tp_layer_desc* d, void* ws) {
   L.rstd2 = static_cast<float*>(c.take((size_t)(d->b * d->s) * 4));
   L.attn_ws = c.take(L.attn_bytes);
   L.mlp_ws = c.take(L.mlp_bytes);
+  if (d->dtype == TP_BF16) {
+    const size_t qd = (size_t)d->n_q * d->d, kd = (size_t)d->n_kv * d->d;
+    L.xn1h = c.take(th);
+    L.wqh = c.take(qd * (size_t)d->h * 2);
+    L.wkh = c.take(kd * (size_t)d->h * 2);
+    L.wvh = c.take(kd * (size_t)d->h * 2);
+  }
   L.bytes = c.off;
   return L;
 }
@@ -1283,13 +1394,53 @@ extern "C" tp_status tp_layer_fwd(const tp_layer_desc* d, const void* x,
       return st != TP_OK ? st : check_mlp(&md);
     }
     if (ws_bytes < L.bytes) return TP_ERR_WORKSPACE;
+    if (!Wq || !Wk || !Wv || !Wo || !W1 || !W2) return TP_ERR_NULL;
+    if (!aligned16(x) || !aligned16(g1) || !aligned16(g2) || !aligned16(Wq) ||
+        !aligned16(Wk) || !aligned16(Wv) || !aligned16(Wo) ||
+        !aligned16(W1) || !aligned16(W2) || !aligned16(out) || !aligned16(ws))
+      return TP_ERR_ARG;
     const int64_t T = d->b * d->s, h = d->h;
     const tp_attn_desc ad = layer_attn(d);
     const tp_mlp_desc md = layer_mlp(d);
-    st = tp_rmsnorm_fwd(T, h, d->eps, TP_BF16, x, g1, L.xn1, L.rstd1, stream);
-    if (st == TP_OK)
-      st = tp_attn_fwd(&ad, L.xn1, Wq, Wk, Wv, Wo, nullptr, x, L.x1,
-                       L.attn_ws, L.attn_bytes, stream);
+    if (d->dtype == TP_BF16) {
+      // the first norm writes its output in bf16 (saved for the backward)
+      // and fp16 (the Q, K, V projections' operand, with fp16 weights)
+      unsigned* status = device_status_ptr();
+      const int64_t qd = (int64_t)d->n_q * d->d, kd = (int64_t)d->n_kv * d->d;
+      int err = rmsnorm_fwd<__nv_bfloat16>(x, g1, L.xn1, L.rstd1, T, h, d->eps,
+                                           stream, L.xn1h, status);
+      if (!err) err = convert_f16(Wq, L.wqh, qd * h, status, stream);
+      if (!err) err = convert_f16(Wk, L.wkh, kd * h, status, stream);
+      if (!err) err = convert_f16(Wv, L.wvh, kd * h, status, stream);
+      if (err) return cuda_status(err);
+      QkvF16 f16in;
+      f16in.x = L.xn1h;
+      f16in.wq = L.wqh;
+      f16in.wk = L.wkh;
+      f16in.wv = L.wvh;
+      const bool sp = d->mode == TP_REDUCE_SP;
+      void* partials = nullptr;
+      st = attn_fwd_impl(&ad, L.xn1, Wq, Wk, Wv, Wo, nullptr, x, L.x1,
+                         L.attn_ws, L.attn_bytes, stream, &f16in,
+                         sp ? &partials : nullptr);
+      if (st == TP_OK && sp) {
+        // reduce-scatter of the attention partials + residual, then the
+        // second RMSNorm on the same rows; the all-gathered xn2 is the
+        // MLP's input
+        int err = reduce_norm_fwd<__nv_bfloat16>(
+            partials, d->n, T * h, nullptr, x, L.x1, DropoutSpec(), g2,
+            L.xn2, nullptr, L.rstd2, T, h, d->eps, status, stream);
+        if (err) return cuda_status(err);
+        return tp_mlp_fwd(&md, L.xn2, W1, nullptr, W2, nullptr, L.x1, out,
+                          L.mlp_ws, L.mlp_bytes, stream);
+      }
+    } else {
+      st = tp_rmsnorm_fwd(T, h, d->eps, TP_BF16, x, g1, L.xn1, L.rstd1,
+                          stream);
+      if (st == TP_OK)
+        st = tp_attn_fwd(&ad, L.xn1, Wq, Wk, Wv, Wo, nullptr, x, L.x1,
+                         L.attn_ws, L.attn_bytes, stream);
+    }
     if (st == TP_OK)
       st = tp_rmsnorm_fwd(T, h, d->eps, TP_BF16, L.x1, g2, L.xn2, L.rstd2,
                           stream);
@@ -1322,6 +1473,30 @@ extern "C" tp_status tp_layer_bwd(const tp_layer_desc* d, const void* dout,
     const int64_t T = d->b * d->s, h = d->h;
     const tp_attn_desc ad = layer_attn(d);
     const tp_mlp_desc md = layer_mlp(d);
+    if (d->mode == TP_REDUCE_SP) {
+      // each f reduction (the blocks' input-gradient partials) is summed
+      // inside the RMSNorm backward of the rows it feeds
+      if (!Wq || !Wk || !Wv || !Wo || !W1 || !W2 || !dWq || !dWk || !dWv ||
+          !dWo || !dW1 || !dW2)
+        return TP_ERR_NULL;
+      void* partials = nullptr;
+      st = mlp_bwd_impl(&md, dout, F.xn2, W1, W2, F.mlp_ws, nullptr, L.dxn,
+                        dW1, nullptr, dW2, nullptr, L.blk, L.blk_bytes,
+                        stream, &partials);
+      if (st != TP_OK) return st;
+      int err = rmsnorm_bwd_sum<__nv_bfloat16>(
+          partials, d->n, T * h, F.x1, g2, F.rstd2, dout, L.dx1, dg2,
+          static_cast<float*>(L.norm), T, h, stream);
+      if (err) return cuda_status(err);
+      st = attn_bwd_impl(&ad, L.dx1, F.xn1, Wq, Wk, Wv, Wo, F.attn_ws,
+                         nullptr, L.dxn, dWq, dWk, dWv, dWo, nullptr, L.blk,
+                         L.blk_bytes, stream, &partials);
+      if (st != TP_OK) return st;
+      err = rmsnorm_bwd_sum<__nv_bfloat16>(
+          partials, d->n, T * h, x, g1, F.rstd1, L.dx1, dx, dg1,
+          static_cast<float*>(L.norm), T, h, stream);
+      return cuda_status(err);
+    }
     // MLP block: d(xn2) into dxn, then RMSNorm₂ with the residual's dout
     st = tp_mlp_bwd(&md, dout, F.xn2, W1, W2, F.mlp_ws, nullptr, L.dxn, dW1,
                     nullptr, dW2, nullptr, L.blk, L.blk_bytes, stream);

@@ -10,6 +10,8 @@
 //  * RMSNorm forward / backward ([Troverld] §II.III fused norm).
 // All loads and stores are 16-byte vectors; grids are a multiple of the SM
 // count and grid-stride.
+#include <cuda_fp16.h>
+
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -87,6 +89,12 @@ __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
+}
+
+// v rounded to T and back (the value a T store would hold).
+template <typename T>
+__device__ __forceinline__ float round_to(float v) {
+  return to_f<T>(from_f<T>(v));
 }
 
 // ------------------------------------------------------- reduce_partials --
@@ -214,14 +222,18 @@ __global__ void __launch_bounds__(256)
 
 // -------------------------------------------------------------- RMSNorm --
 // One block per row (grid-stride over rows); each thread owns columns
-// {V·(tid + 256·j)}.
+// {V·(tid + 256·j)}.  y16 (optional) receives the same normalised row in
+// fp16, the operand of fp16 projections; a value beyond the fp16 range
+// records a range error.
 template <typename T>
 __global__ void __launch_bounds__(256)
     rmsnorm_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
-                       T* __restrict__ y, float* __restrict__ rstd_out,
-                       int64_t rows, int64_t h, float eps) {
+                       T* __restrict__ y, __half* __restrict__ y16,
+                       float* __restrict__ rstd_out, int64_t rows, int64_t h,
+                       float eps, unsigned* status) {
   constexpr int V = Vec<T>::N;
   __shared__ float red[8];
+  bool bad = false;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const T* xr = x + r * h;
     float ss = 0.0f;
@@ -247,9 +259,47 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int q = 0; q < V; ++q) v[q] = v[q] * rs * g[q];
       Vec<T>::store(y + r * h + c, v);
+      if (y16 != nullptr) {
+        uint32_t u[V / 2];
+#pragma unroll
+        for (int q = 0; q < V; q += 2) {
+          bad |= !(fabsf(v[q]) <= kF16Max) || !(fabsf(v[q + 1]) <= kF16Max);
+          u[q / 2] = pack_f16x2(v[q], v[q + 1]);
+        }
+        __half* dst = y16 + r * h + c;
+        if constexpr (V == 8)
+          *reinterpret_cast<uint4*>(dst) = make_uint4(u[0], u[1], u[2], u[3]);
+        else
+          *reinterpret_cast<uint2*>(dst) = make_uint2(u[0], u[1]);
+      }
     }
     __syncthreads();
   }
+  if (bad) record_error(status, kDevRange, 30);
+}
+
+// ------------------------------------------------------- bf16 → fp16 copy --
+// dst = fp16(src) over n elements (n a multiple of 8); a value beyond the
+// fp16 range records a range error.  bf16 values of magnitude below 2^-14
+// become fp16 subnormals (below 2^-24: zero).
+__global__ void __launch_bounds__(256)
+    convert_f16_kernel(const __nv_bfloat16* __restrict__ src,
+                       __half* __restrict__ dst, int64_t n, unsigned* status) {
+  bool bad = false;
+  const int64_t nvec = n / 8;
+  for (int64_t iv = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; iv < nvec;
+       iv += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+    Vec<__nv_bfloat16>::load(src + iv * 8, v);
+    uint32_t u[4];
+#pragma unroll
+    for (int q = 0; q < 8; q += 2) {
+      bad |= !(fabsf(v[q]) <= kF16Max) || !(fabsf(v[q + 1]) <= kF16Max);
+      u[q / 2] = pack_f16x2(v[q], v[q + 1]);
+    }
+    reinterpret_cast<uint4*>(dst)[iv] = make_uint4(u[0], u[1], u[2], u[3]);
+  }
+  if (bad) record_error(status, kDevRange, 31);
 }
 
 // One block of 512 threads per chunk of consecutive rows (about one chunk
@@ -258,10 +308,13 @@ __global__ void __launch_bounds__(256)
 // and x while it finishes the current one.  Per row: dot = Σ dy·γ·x (block
 // reduction through a double-buffered slot, one barrier),
 //   dx = dres + rstd·dy·γ − x·rstd³·dot / h,   dγ_partial += dy·x·rstd.
-template <typename T, int NV>
+// SUM (the f reduction fused in, Megatron-SP backward): dy is not read but
+// formed per row as Σ_{i<n} P_i in fp32, in shard order, rounded once to T —
+// the value the materialised reduce would have stored.
+template <typename T, int NV, bool SUM>
 __global__ void __launch_bounds__(512, 1)
-    rmsnorm_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
-                       const T* __restrict__ gamma,
+    rmsnorm_bwd_kernel(const T* __restrict__ dy, int n, int64_t zstride,
+                       const T* __restrict__ x, const T* __restrict__ gamma,
                        const float* __restrict__ rstd,
                        const T* __restrict__ dres, T* __restrict__ dx,
                        float* __restrict__ dg_partial, int64_t rows, int64_t h,
@@ -295,8 +348,9 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     const bool ld = on[j] && r_begin < r_end;
-    cd[j] = ld ? *reinterpret_cast<const uint4*>(dy + r_begin * h + col[j])
-               : zero;
+    cd[j] = (!SUM && ld)
+                ? *reinterpret_cast<const uint4*>(dy + r_begin * h + col[j])
+                : zero;
     cx[j] = ld ? *reinterpret_cast<const uint4*>(x + r_begin * h + col[j])
                : zero;
   }
@@ -305,7 +359,7 @@ __global__ void __launch_bounds__(512, 1)
     const bool more = r + 1 < r_end;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      nd[j] = (more && on[j])
+      nd[j] = (!SUM && more && on[j])
                   ? *reinterpret_cast<const uint4*>(dy + (r + 1) * h + col[j])
                   : zero;
       nx[j] = (more && on[j])
@@ -319,7 +373,23 @@ __global__ void __launch_bounds__(512, 1)
     float d[NV * V], xv[NV * V];
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      Vec<T>::from_raw(cd[j], d + j * V);
+      if constexpr (SUM) {
+        float acc[V], v[V];
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] = 0.0f;
+        if (on[j]) {
+          Vec<T>::load(dy + r * h + col[j], acc);
+          for (int i = 1; i < n; ++i) {
+            Vec<T>::load(dy + (int64_t)i * zstride + r * h + col[j], v);
+#pragma unroll
+            for (int q = 0; q < V; ++q) acc[q] += v[q];
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < V; ++q) d[j * V + q] = round_to<T>(acc[q]);
+      } else {
+        Vec<T>::from_raw(cd[j], d + j * V);
+      }
       Vec<T>::from_raw(cx[j], xv + j * V);
     }
     float dot = 0.0f;
@@ -357,6 +427,106 @@ __global__ void __launch_bounds__(512, 1)
     if (on[j])
       Vec<T>::store_f32(dg_partial + (int64_t)blockIdx.x * h + col[j],
                         dgacc + j * V);
+}
+
+// The g reduction with the next block's RMSNorm fused in (Megatron-SP
+// forward, [Troverld] §III.III: the reduce-scatter leaves each rank its rows
+// of the block output, the token-wise ops of the next block run on them, and
+// the all-gather hands the normalised rows to the next column-parallel
+// GEMM — on one device the gathered buffer is the output itself).  One block
+// of 256 threads per row, thread t owning the column vectors {V·(t + 256·j)}
+// as the RMSNorm forward does:
+//   out = resid + Dropout(Σ_{i<n} P_i + bias)   (the materialised reduce)
+//   rstd = 1/√(mean(out²) + ε),  y = out·rstd·γ  (the RMSNorm forward, on the
+//                                                 stored values of out)
+// Both halves round and reduce exactly as the two separate kernels do.
+template <typename T, int NV>
+__global__ void __launch_bounds__(256)
+    reduce_norm_fwd_kernel(const T* __restrict__ P, int n, int64_t zstride,
+                           const T* __restrict__ bias,
+                           const T* __restrict__ resid, T* __restrict__ out,
+                           int dropout, uint32_t thr, float scale,
+                           uint64_t seed, const T* __restrict__ gamma,
+                           T* __restrict__ y, __half* __restrict__ y16,
+                           float* __restrict__ rstd_out, int64_t rows,
+                           int64_t h, float eps, unsigned* status) {
+  constexpr int V = Vec<T>::N;
+  __shared__ float red[8];
+  bool bad = false;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    float row[NV * V];
+    float ss = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int64_t c = ((int64_t)threadIdx.x + 256 * j) * V;
+      if (c >= h) break;
+      const int64_t i0 = r * h + c;
+      float acc[V], v[V];
+      Vec<T>::load(P + i0, acc);
+      for (int sh = 1; sh < n; ++sh) {
+        Vec<T>::load(P + (int64_t)sh * zstride + i0, v);
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] += v[q];
+      }
+      if (bias != nullptr) {
+        Vec<T>::load(bias + c, v);
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] += v[q];
+      }
+      if (dropout) {
+#pragma unroll
+        for (int q = 0; q < V; ++q)
+          acc[q] = dropout_keep(seed, (uint64_t)(i0 + q), thr)
+                       ? acc[q] * scale
+                       : 0.0f;
+      }
+      if (resid != nullptr) {
+        Vec<T>::load(resid + i0, v);
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] += v[q];
+      }
+      Vec<T>::store(out + i0, acc);
+#pragma unroll
+      for (int q = 0; q < V; ++q) {
+        row[j * V + q] = round_to<T>(acc[q]);
+        ss += row[j * V + q] * row[j * V + q];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    const float rs = rsqrtf(tot / (float)h + eps);
+    if (threadIdx.x == 0) rstd_out[r] = rs;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int64_t c = ((int64_t)threadIdx.x + 256 * j) * V;
+      if (c >= h) break;
+      float g[V], v[V];
+      Vec<T>::load(gamma + c, g);
+#pragma unroll
+      for (int q = 0; q < V; ++q) v[q] = row[j * V + q] * rs * g[q];
+      Vec<T>::store(y + r * h + c, v);
+      if (y16 != nullptr) {
+        uint32_t u[V / 2];
+#pragma unroll
+        for (int q = 0; q < V; q += 2) {
+          bad |= !(fabsf(v[q]) <= kF16Max) || !(fabsf(v[q + 1]) <= kF16Max);
+          u[q / 2] = pack_f16x2(v[q], v[q + 1]);
+        }
+        __half* dst = y16 + r * h + c;
+        if constexpr (V == 8)
+          *reinterpret_cast<uint4*>(dst) = make_uint4(u[0], u[1], u[2], u[3]);
+        else
+          *reinterpret_cast<uint2*>(dst) = make_uint2(u[0], u[1]);
+      }
+    }
+    __syncthreads();
+  }
+  if (bad) record_error(status, kDevRange, 32);
 }
 
 int grid_for(int64_t work_items, int per_block) {
@@ -430,13 +600,28 @@ int colsum(const void* X, int64_t rows, int64_t cols, int64_t ld, void* out,
 
 template <typename T>
 int rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
-                int64_t rows, int64_t h, float eps, void* stream) {
+                int64_t rows, int64_t h, float eps, void* stream, void* y16,
+                unsigned* status) {
   if (rows == 0) return cudaSuccess;
   const int grid = (int)std::min<int64_t>(rows, (int64_t)device_sm_count() * 8);
-  ProfScope ps(stream, KF_NORM, 4.0 * rows * h, 2.0 * sizeof(T) * rows * h);
+  ProfScope ps(stream, KF_NORM, 4.0 * rows * h,
+               (2.0 * sizeof(T) + (y16 != nullptr ? 2.0 : 0.0)) * rows * h);
   rmsnorm_fwd_kernel<T><<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const T*>(x), static_cast<const T*>(gamma),
-      static_cast<T*>(y), rstd, rows, h, eps);
+      static_cast<T*>(y), static_cast<__half*>(y16), rstd, rows, h, eps,
+      status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+int convert_f16(const void* src, void* dst, int64_t n, unsigned* status,
+                void* stream) {
+  if (n == 0) return cudaSuccess;
+  const int grid = grid_for(n / 8, 256);
+  ProfScope ps(stream, KF_ELEMENTWISE, 0.0, 4.0 * n);
+  convert_f16_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(src), static_cast<__half*>(dst), n,
+      status);
   count_launch();
   return cudaGetLastError();
 }
@@ -450,10 +635,13 @@ size_t rmsnorm_bwd_scratch(int64_t rows, int64_t h) {
   return (size_t)rmsnorm_bwd_chunks(rows) * (size_t)h * sizeof(float);
 }
 
+// The RMSNorm backward; with n > 1 dy is the sum of n partials (zstride
+// elements apart) formed in the kernel.
 template <typename T>
-int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
-                const float* rstd, const void* dres, void* dx, void* dgamma,
-                float* scratch, int64_t rows, int64_t h, void* stream) {
+int rmsnorm_bwd_sum(const void* dy, int n, int64_t zstride, const void* x,
+                    const void* gamma, const float* rstd, const void* dres,
+                    void* dx, void* dgamma, float* scratch, int64_t rows,
+                    int64_t h, void* stream) {
   if (rows == 0) return cudaSuccess;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // at most one chunk per SM (the scratch holds rmsnorm_bwd_chunks rows)
@@ -463,26 +651,70 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
   constexpr int V = Vec<T>::N;
   // 16-byte vectors per thread: 512 threads × V columns per sweep
   const int64_t sweeps = (h + 512 * V - 1) / (512 * V);
-  if (sweeps > 4) return cudaErrorInvalidValue;
-  ProfScope ps(stream, KF_NORM, 8.0 * rows * h,
-               (double)sizeof(T) * rows * h * (dres != nullptr ? 4 : 3));
+  if (sweeps > 4 || n < 1) return cudaErrorInvalidValue;
+  const int kind = n > 1 ? KF_REDUCE : KF_NORM;
+  ProfScope ps(stream, kind, 8.0 * rows * h + (n - 1.0) * rows * h,
+               (double)sizeof(T) * rows * h * (n + (dres != nullptr ? 3 : 2)));
   const T* dyp = static_cast<const T*>(dy);
   const T* xp = static_cast<const T*>(x);
   const T* gp = static_cast<const T*>(gamma);
   const T* rp = static_cast<const T*>(dres);
   T* dxp = static_cast<T*>(dx);
-  if (sweeps <= 1)
-    rmsnorm_bwd_kernel<T, 1><<<chunks, 512, 0, s>>>(dyp, xp, gp, rstd, rp, dxp,
-                                                    scratch, rows, h, rpc);
-  else if (sweeps <= 2)
-    rmsnorm_bwd_kernel<T, 2><<<chunks, 512, 0, s>>>(dyp, xp, gp, rstd, rp, dxp,
-                                                    scratch, rows, h, rpc);
-  else
-    rmsnorm_bwd_kernel<T, 4><<<chunks, 512, 0, s>>>(dyp, xp, gp, rstd, rp, dxp,
-                                                    scratch, rows, h, rpc);
+#define TP_BWD(NVV, SUMV)                                                     \
+  rmsnorm_bwd_kernel<T, NVV, SUMV><<<chunks, 512, 0, s>>>(                    \
+      dyp, n, zstride, xp, gp, rstd, rp, dxp, scratch, rows, h, rpc)
+  if (n == 1) {
+    if (sweeps <= 1) TP_BWD(1, false);
+    else if (sweeps <= 2) TP_BWD(2, false);
+    else TP_BWD(4, false);
+  } else {
+    if (sweeps <= 1) TP_BWD(1, true);
+    else if (sweeps <= 2) TP_BWD(2, true);
+    else TP_BWD(4, true);
+  }
+#undef TP_BWD
   colsum_stage2<T><<<(unsigned)((h + 31) / 32), 256, 0, s>>>(scratch, chunks, h,
                                                     static_cast<T*>(dgamma));
   count_launch(2);
+  return cudaGetLastError();
+}
+
+template <typename T>
+int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
+                const float* rstd, const void* dres, void* dx, void* dgamma,
+                float* scratch, int64_t rows, int64_t h, void* stream) {
+  return rmsnorm_bwd_sum<T>(dy, 1, 0, x, gamma, rstd, dres, dx, dgamma,
+                            scratch, rows, h, stream);
+}
+
+template <typename T>
+int reduce_norm_fwd(const void* P, int n, int64_t zstride, const void* bias,
+                    const void* resid, void* out, const DropoutSpec& d,
+                    const void* gamma, void* y, void* y16, float* rstd,
+                    int64_t rows, int64_t h, float eps, unsigned* status,
+                    void* stream) {
+  if (rows == 0) return cudaSuccess;
+  constexpr int V = Vec<T>::N;
+  const int64_t sweeps = (h + 256 * V - 1) / (256 * V);
+  if (sweeps > 8 || n < 1) return cudaErrorInvalidValue;
+  const int grid = (int)std::min<int64_t>(rows, (int64_t)device_sm_count() * 8);
+  ProfScope ps(stream, KF_REDUCE, (double)(n + 4) * rows * h,
+               (double)sizeof(T) * rows * h *
+                       (n + 2 + (resid != nullptr ? 1 : 0)) +
+                   (y16 != nullptr ? 2.0 * rows * h : 0.0));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+#define TP_FWD(NVV)                                                           \
+  reduce_norm_fwd_kernel<T, NVV><<<grid, 256, 0, s>>>(                        \
+      static_cast<const T*>(P), n, zstride, static_cast<const T*>(bias),      \
+      static_cast<const T*>(resid), static_cast<T*>(out), d.enabled, d.thr,   \
+      d.scale, d.seed, static_cast<const T*>(gamma), static_cast<T*>(y),      \
+      static_cast<__half*>(y16), rstd, rows, h, eps, status)
+  if (sweeps <= 1) TP_FWD(1);
+  else if (sweeps <= 2) TP_FWD(2);
+  else if (sweeps <= 4) TP_FWD(4);
+  else TP_FWD(8);
+#undef TP_FWD
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -495,10 +727,19 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
   template int colsum<T>(const void*, int64_t, int64_t, int64_t, void*,       \
                          float*, void*);                                      \
   template int rmsnorm_fwd<T>(const void*, const void*, void*, float*,        \
-                              int64_t, int64_t, float, void*);                \
+                              int64_t, int64_t, float, void*, void*,          \
+                              unsigned*);                                     \
   template int rmsnorm_bwd<T>(const void*, const void*, const void*,          \
                               const float*, const void*, void*, void*,        \
-                              float*, int64_t, int64_t, void*);
+                              float*, int64_t, int64_t, void*);               \
+  template int rmsnorm_bwd_sum<T>(const void*, int, int64_t, const void*,     \
+                                  const void*, const float*, const void*,     \
+                                  void*, void*, float*, int64_t, int64_t,     \
+                                  void*);                                     \
+  template int reduce_norm_fwd<T>(const void*, int, int64_t, const void*,     \
+                                  const void*, void*, const DropoutSpec&,     \
+                                  const void*, void*, void*, float*, int64_t, \
+                                  int64_t, float, unsigned*, void*);
 TP_INST(float)
 TP_INST(__nv_bfloat16)
 #undef TP_INST

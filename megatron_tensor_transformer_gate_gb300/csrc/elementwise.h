@@ -31,14 +31,39 @@ size_t colsum_scratch_bytes(int64_t rows, int64_t cols);
 template <typename T>
 int colsum(const void* X, int64_t rows, int64_t cols, int64_t ld, void* out,
            float* scratch, void* stream);
+// y16 (optional): the normalised rows also in fp16 (range errors recorded in
+// status).
 template <typename T>
 int rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
-                int64_t rows, int64_t h, float eps, void* stream);
+                int64_t rows, int64_t h, float eps, void* stream,
+                void* y16 = nullptr, unsigned* status = nullptr);
+// dst = fp16(src) for n bf16 values (n a multiple of 8, 16-byte aligned);
+// a value beyond the fp16 range records a range error in status.
+int convert_f16(const void* src, void* dst, int64_t n, unsigned* status,
+                void* stream);
 size_t rmsnorm_bwd_scratch(int64_t rows, int64_t h);
 template <typename T>
 int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
                 const float* rstd, const void* dres, void* dx, void* dgamma,
                 float* scratch, int64_t rows, int64_t h, void* stream);
+// Megatron-SP fusions (the reduce-scatter and the token-wise op after it):
+// rmsnorm_bwd_sum takes dy as the sum of n partials zstride elements apart
+// (rounded once to T, as the materialised reduce stores it), then runs the
+// RMSNorm backward (n = 1: plain dy, same as rmsnorm_bwd);
+// reduce_norm_fwd writes out = resid + Dropout(Σ P_i + bias) and the RMSNorm
+// of those stored rows (y, optional fp16 copy y16, rstd) in one pass.  Both
+// give the same bits as the separate kernels.
+template <typename T>
+int rmsnorm_bwd_sum(const void* dy, int n, int64_t zstride, const void* x,
+                    const void* gamma, const float* rstd, const void* dres,
+                    void* dx, void* dgamma, float* scratch, int64_t rows,
+                    int64_t h, void* stream);
+template <typename T>
+int reduce_norm_fwd(const void* P, int n, int64_t zstride, const void* bias,
+                    const void* resid, void* out, const DropoutSpec& d,
+                    const void* gamma, void* y, void* y16, float* rstd,
+                    int64_t rows, int64_t h, float eps, unsigned* status,
+                    void* stream);
 
 // The RMSNorm backward with its dγ partial sums in a fixed device array
 // (no caller scratch); h ≤ kNoallocNormMaxH.

@@ -75,6 +75,8 @@ struct GemmProblem {
   // tp_dtype: 0 fp32 (CUDA cores), 1 bf16 (tensor cores), 2 E4M3 operands
   // (tensor cores, K-major only, bf16 outputs, scales in the epilogue)
   int dtype = 1;
+  // dtype 1 only: the operands are fp16 instead of bf16 (same layouts)
+  int f16 = 0;
   int64_t M = 0, N = 0;
   int nparts = 1;
   GemmPart parts[3];

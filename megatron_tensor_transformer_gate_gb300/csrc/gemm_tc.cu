@@ -59,6 +59,7 @@ struct TcParams {
   int nparts;
   int M, N;            // N is the logical output width
   int m_tiles, n_tiles, nz, total_tiles, group_m;
+  int f16;             // fp16 A and B (kind::f16 with the F16 formats)
   GemmEpilogue epi;
   unsigned* status;
 };
@@ -393,8 +394,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (leader && lane == 0) {
       // -------------------------------------------------------- MMA issue --
-      constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(2 * BM, BN)
-                                    : idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+      const uint32_t IDESC =
+          F8 ? idesc_e4m3_f32(2 * BM, BN)
+             : (p.f16 ? idesc_f16_f32(2 * BM, BN, A_MN, B_MN)
+                      : idesc_bf16_f32(2 * BM, BN, A_MN, B_MN));
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int it = 0;
@@ -515,16 +518,19 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
 // K-major operand (rows × K, row stride ld): dims {kseg, nseg, rows}.
 // MN-major operand (K × rows, row stride ld): dims {rows, kseg, nseg}.
 bool encode_operand(CUtensorMap* m, const GemmOperand& o, int64_t kseg,
-                    int nseg, uint32_t box_rows, bool f8 = false) {
+                    int nseg, uint32_t box_rows, bool f8 = false,
+                    bool f16 = false) {
   if (f8)   // E4M3, K-major: 128-element (128-byte) K boxes
     return !o.mn_major &&
            encode_3d(m, o.ptr, kseg, nseg, o.rows, kseg, o.ld, 2 * BK, 1,
                      box_rows, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+  const CUtensorMapDataType ty = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (o.mn_major)
     return encode_3d(m, o.ptr, o.rows, kseg, nseg, o.ld * 2,
-                     (uint64_t)kseg * o.ld * 2, 64, BK, 1);
+                     (uint64_t)kseg * o.ld * 2, 64, BK, 1, ty);
   return encode_3d(m, o.ptr, kseg, nseg, o.rows, kseg * 2, o.ld * 2, BK, 1,
-                   box_rows);
+                   box_rows, ty);
 }
 
 // One CTA pair per two SMs: the grid is as many pairs as can be resident
@@ -586,6 +592,7 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
   if (e.kind == EPI_SWIGLU && (b_mn || a_mn || pr.nparts != 1))
     return cudaErrorInvalidValue;
   const bool f8 = pr.dtype == 2;
+  const bool f16 = !f8 && pr.f16 != 0;
   if (f8 && (a_mn || b_mn ||
              (e.kind != EPI_STORE && e.kind != EPI_GELU &&
               e.kind != EPI_SWIGLU)))
@@ -597,13 +604,13 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
   prm.nparts = pr.nparts;
   for (int i = 0; i < pr.nparts; ++i) {
     const GemmPart& pt = pr.parts[i];
-    if (!encode_operand(&prm.ma[i], pt.a, pt.kseg, pt.nseg, BM, f8))
+    if (!encode_operand(&prm.ma[i], pt.a, pt.kseg, pt.nseg, BM, f8, f16))
       return cudaErrorInvalidValue;
     const uint32_t brows = BNH;   // each CTA of the pair loads half of B
-    if (!encode_operand(&prm.mb[i], pt.b, pt.kseg, pt.nseg, brows, f8))
+    if (!encode_operand(&prm.mb[i], pt.b, pt.kseg, pt.nseg, brows, f8, f16))
       return cudaErrorInvalidValue;
     if (e.kind == EPI_SWIGLU &&
-        !encode_operand(&prm.mb2, pt.b2, pt.kseg, pt.nseg, brows, f8))
+        !encode_operand(&prm.mb2, pt.b2, pt.kseg, pt.nseg, brows, f8, f16))
       return cudaErrorInvalidValue;
     prm.part[i].kblocks = (int)((pt.kseg + bke - 1) / bke);
     prm.part[i].nsub = pt.nsub;
@@ -618,6 +625,7 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
   prm.nz = pr.nz;
   prm.total_tiles = prm.m_tiles * prm.n_tiles * pr.nz;
   prm.group_m = 8;
+  prm.f16 = f16 ? 1 : 0;
   prm.epi = e;
   prm.status = status;
   if (prm.total_tiles == 0) return cudaSuccess;
