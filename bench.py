@@ -57,6 +57,13 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the block workloads timed after the headline")
+    ap.add_argument("--kernel", default=None,
+                    choices=["gemm", "rmsnorm_fwd", "rmsnorm_bwd", "reduce"],
+                    help="time one kernel alone on --shape (small cases for "
+                         "profiler captures) instead of the workload")
+    ap.add_argument("--shape", default="8192,57344,8192",
+                    help="gemm: M,N,K (C = A·Bᵀ, both K-major); rmsnorm_*: "
+                         "T,h; reduce: n,T,h")
     return ap.parse_args(argv)
 
 
@@ -558,8 +565,84 @@ def secondary_runs(steps, seed, dev, peaks, stream):
     return out
 
 
+def single_kernel(args):
+    """One kernel of the path launched alone, --warmup + --steps times on
+    resident seeded inputs, timed with CUDA events on the launching stream:
+    the small, single-launch cases that profiler counter captures run on."""
+    import torch
+    import __graft_entry__
+    from megatron_tensor_transformer_gate_gb300 import binding as B
+    from megatron_tensor_transformer_gate_gb300 import inputs as I
+    __graft_entry__.build()
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    dims = [int(v) for v in args.shape.split(",")]
+    bf = torch.bfloat16
+    if args.kernel == "gemm":
+        M, N, K = dims
+        A = I.normal((M, K), 1.0, 1, dev, bf)
+        Bm = I.normal((N, K), 0.02, 2, dev, bf)
+        C = torch.empty((M, N), dtype=bf, device=dev)
+        run = lambda: B.gemm(A, Bm, C)
+        flops, nbytes = 2.0 * M * N * K, 2.0 * (M * K + N * K + M * N)
+    elif args.kernel in ("rmsnorm_fwd", "rmsnorm_bwd"):
+        T, h = dims
+        x = I.normal((T, h), 1.0, 1, dev, bf)
+        g = I.normal((h,), 0.02, 2, dev, bf, mean=1.0)
+        y = torch.empty_like(x)
+        rstd = torch.empty(T, dtype=torch.float32, device=dev)
+        B.rmsnorm_fwd(x, g, y, rstd)
+        if args.kernel == "rmsnorm_fwd":
+            run = lambda: B.rmsnorm_fwd(x, g, y, rstd)
+            nbytes = 4.0 * T * h
+        else:
+            dy = I.normal((T, h), 1.0, 3, dev, bf)
+            dres = I.normal((T, h), 1.0, 4, dev, bf)
+            dx, dg = torch.empty_like(x), torch.empty_like(g)
+            sc = torch.empty(B.rmsnorm_bwd_scratch_bytes(T, h),
+                             dtype=torch.uint8, device=dev)
+            run = lambda: B.rmsnorm_bwd(dy, x, g, rstd, dx, dg, sc, dres=dres)
+            nbytes = 8.0 * T * h
+        flops = 0.0
+    else:   # reduce: a materialised MLP forward's g reduction on n partials
+        n, T, h = dims
+        d = B.mlp_desc(T, h, 8 * n, n, act=B.GELU, mode=B.MATERIALISED)
+        ws = torch.empty(B.mlp_workspace_bytes(d), dtype=torch.uint8,
+                         device=dev)
+        X = I.normal((T, h), 1.0, 1, dev, bf)
+        W1 = I.normal((8 * n, h), 0.02, 2, dev, bf)
+        W2 = I.normal((h, 8 * n), 0.02, 3, dev, bf)
+        out = torch.empty_like(X)
+        run = lambda: B.mlp_fwd(d, X, W1, W2, out, ws, R=X)
+        flops, nbytes = 0.0, 2.0 * T * h * (n + 2)
+    fam = {"gemm": "gemm_tc", "rmsnorm_fwd": "rmsnorm",
+           "rmsnorm_bwd": "rmsnorm", "reduce": "reduce"}[args.kernel]
+    for _ in range(max(args.warmup, 3)):
+        run()
+    torch.cuda.synchronize()
+    B.profile_enable(16 * (args.steps + 1))
+    B.profile_reset()
+    for _ in range(args.steps):
+        run()
+    torch.cuda.synchronize()
+    prof = B.profile_read()[fam]
+    B.profile_enable(0)
+    B.device_status()
+    ms = prof["ms"] / max(prof["launches"], 1)
+    rec = {"kernel": args.kernel, "family": fam, "shape": dims,
+           "launches": prof["launches"], "ms_per_launch": ms,
+           "algorithmic_bytes_per_launch": prof["bytes"] / prof["launches"]}
+    if flops:
+        rec["tflops"] = flops / (ms / 1e3) / 1e12
+    rec["gbs"] = rec["algorithmic_bytes_per_launch"] / (ms / 1e3) / 1e9
+    print(json.dumps(rec), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.kernel:
+        single_kernel(args)
+        return
     cfg = workload_cfg(args.workload, args.seq)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

@@ -97,6 +97,36 @@ __device__ __forceinline__ float round_to(float v) {
   return to_f<T>(from_f<T>(v));
 }
 
+// acc = Σ_{s<n} P[s·zstride] for one 16-byte vector, summed in fp32 in shard
+// order.  The loads of the first AHEAD shards are issued together (AHEAD
+// 16-byte requests in flight per thread instead of one), the rest one by one.
+template <typename T, int AHEAD = 8>
+__device__ __forceinline__ void sum_shards(const T* __restrict__ p, int n,
+                                           int64_t zstride, float* acc) {
+  constexpr int V = Vec<T>::N;
+  uint4 raw[AHEAD];
+#pragma unroll
+  for (int s = 0; s < AHEAD; ++s)
+    if (s < n)
+      raw[s] = *reinterpret_cast<const uint4*>(p + (int64_t)s * zstride);
+  Vec<T>::from_raw(raw[0], acc);
+#pragma unroll
+  for (int s = 1; s < AHEAD; ++s) {
+    if (s < n) {
+      float v[V];
+      Vec<T>::from_raw(raw[s], v);
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] += v[q];
+    }
+  }
+  for (int s = AHEAD; s < n; ++s) {
+    float v[V];
+    Vec<T>::load(p + (int64_t)s * zstride, v);
+#pragma unroll
+    for (int q = 0; q < V; ++q) acc[q] += v[q];
+  }
+}
+
 // ------------------------------------------------------- reduce_partials --
 template <typename T>
 __global__ void __launch_bounds__(256)
@@ -112,12 +142,7 @@ __global__ void __launch_bounds__(256)
        iv += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = iv * V;
     float acc[V], v[V];
-    Vec<T>::load(P + i, acc);
-    for (int s = 1; s < n; ++s) {
-      Vec<T>::load(P + (int64_t)s * zstride + i, v);
-#pragma unroll
-      for (int q = 0; q < V; ++q) acc[q] += v[q];
-    }
+    sum_shards<T>(P + i, n, zstride, acc);
     if (bias != nullptr) {
       Vec<T>::load(bias + (i % h), v);
 #pragma unroll
@@ -222,9 +247,10 @@ __global__ void __launch_bounds__(256)
 
 // -------------------------------------------------------------- RMSNorm --
 // One block per row (grid-stride over rows); each thread owns columns
-// {V·(tid + 256·j)}.  y16 (optional) receives the same normalised row in
+// {V·(tid + 256·j)}: the sum of squares in that order, then the row read
+// again (from L2) and normalised.  y16 (optional) receives the same rows in
 // fp16, the operand of fp16 projections; a value beyond the fp16 range
-// records a range error.
+// records a range error.  Same bits as the norm half of reduce_norm_fwd.
 template <typename T>
 __global__ void __launch_bounds__(256)
     rmsnorm_fwd_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
@@ -374,17 +400,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       if constexpr (SUM) {
-        float acc[V], v[V];
+        float acc[V];
 #pragma unroll
         for (int q = 0; q < V; ++q) acc[q] = 0.0f;
-        if (on[j]) {
-          Vec<T>::load(dy + r * h + col[j], acc);
-          for (int i = 1; i < n; ++i) {
-            Vec<T>::load(dy + (int64_t)i * zstride + r * h + col[j], v);
-#pragma unroll
-            for (int q = 0; q < V; ++q) acc[q] += v[q];
-          }
-        }
+        if (on[j]) sum_shards<T>(dy + r * h + col[j], n, zstride, acc);
 #pragma unroll
         for (int q = 0; q < V; ++q) d[j * V + q] = round_to<T>(acc[q]);
       } else {
@@ -439,8 +458,10 @@ __global__ void __launch_bounds__(512, 1)
 //   out = resid + Dropout(Σ_{i<n} P_i + bias)   (the materialised reduce)
 //   rstd = 1/√(mean(out²) + ε),  y = out·rstd·γ  (the RMSNorm forward, on the
 //                                                 stored values of out)
-// Both halves round and reduce exactly as the two separate kernels do.
-template <typename T, int NV>
+// Both halves round and reduce exactly as the two separate kernels do.  y16
+// (optional) receives the normalised rows also in fp16; a value beyond the
+// fp16 range records a range error.  out may be NULL (not stored).
+template <typename T, int NV, int AHEAD>
 __global__ void __launch_bounds__(256)
     reduce_norm_fwd_kernel(const T* __restrict__ P, int n, int64_t zstride,
                            const T* __restrict__ bias,
@@ -462,12 +483,7 @@ __global__ void __launch_bounds__(256)
       if (c >= h) break;
       const int64_t i0 = r * h + c;
       float acc[V], v[V];
-      Vec<T>::load(P + i0, acc);
-      for (int sh = 1; sh < n; ++sh) {
-        Vec<T>::load(P + (int64_t)sh * zstride + i0, v);
-#pragma unroll
-        for (int q = 0; q < V; ++q) acc[q] += v[q];
-      }
+      sum_shards<T, AHEAD>(P + i0, n, zstride, acc);
       if (bias != nullptr) {
         Vec<T>::load(bias + c, v);
 #pragma unroll
@@ -485,7 +501,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int q = 0; q < V; ++q) acc[q] += v[q];
       }
-      Vec<T>::store(out + i0, acc);
+      if (out != nullptr) Vec<T>::store(out + i0, acc);
 #pragma unroll
       for (int q = 0; q < V; ++q) {
         row[j * V + q] = round_to<T>(acc[q]);
@@ -598,6 +614,34 @@ int colsum(const void* X, int64_t rows, int64_t cols, int64_t ld, void* out,
   return cudaGetLastError();
 }
 
+template <typename T, int AHEAD>
+int norm_rows(const void* P, int n, int64_t zstride, const void* bias,
+              const void* resid, void* out, const DropoutSpec& d,
+              const void* gamma, void* y, void* y16, float* rstd, int64_t rows,
+              int64_t h, float eps, unsigned* status, int family,
+              double bytes, void* stream) {
+  if (rows == 0) return cudaSuccess;
+  constexpr int V = Vec<T>::N;
+  const int64_t sweeps = (h + 256 * V - 1) / (256 * V);
+  if (sweeps > 8 || n < 1) return cudaErrorInvalidValue;
+  const int grid = (int)std::min<int64_t>(rows, (int64_t)device_sm_count() * 8);
+  ProfScope ps(stream, family, (double)(n + 3) * rows * h, bytes);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+#define TP_FWD(NVV)                                                           \
+  reduce_norm_fwd_kernel<T, NVV, AHEAD><<<grid, 256, 0, s>>>(                 \
+      static_cast<const T*>(P), n, zstride, static_cast<const T*>(bias),      \
+      static_cast<const T*>(resid), static_cast<T*>(out), d.enabled, d.thr,   \
+      d.scale, d.seed, static_cast<const T*>(gamma), static_cast<T*>(y),      \
+      static_cast<__half*>(y16), rstd, rows, h, eps, status)
+  if (sweeps <= 1) TP_FWD(1);
+  else if (sweeps <= 2) TP_FWD(2);
+  else if (sweeps <= 4) TP_FWD(4);
+  else TP_FWD(8);
+#undef TP_FWD
+  count_launch();
+  return cudaGetLastError();
+}
+
 template <typename T>
 int rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
                 int64_t rows, int64_t h, float eps, void* stream, void* y16,
@@ -693,29 +737,11 @@ int reduce_norm_fwd(const void* P, int n, int64_t zstride, const void* bias,
                     const void* gamma, void* y, void* y16, float* rstd,
                     int64_t rows, int64_t h, float eps, unsigned* status,
                     void* stream) {
-  if (rows == 0) return cudaSuccess;
-  constexpr int V = Vec<T>::N;
-  const int64_t sweeps = (h + 256 * V - 1) / (256 * V);
-  if (sweeps > 8 || n < 1) return cudaErrorInvalidValue;
-  const int grid = (int)std::min<int64_t>(rows, (int64_t)device_sm_count() * 8);
-  ProfScope ps(stream, KF_REDUCE, (double)(n + 4) * rows * h,
-               (double)sizeof(T) * rows * h *
-                       (n + 2 + (resid != nullptr ? 1 : 0)) +
-                   (y16 != nullptr ? 2.0 * rows * h : 0.0));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-#define TP_FWD(NVV)                                                           \
-  reduce_norm_fwd_kernel<T, NVV><<<grid, 256, 0, s>>>(                        \
-      static_cast<const T*>(P), n, zstride, static_cast<const T*>(bias),      \
-      static_cast<const T*>(resid), static_cast<T*>(out), d.enabled, d.thr,   \
-      d.scale, d.seed, static_cast<const T*>(gamma), static_cast<T*>(y),      \
-      static_cast<__half*>(y16), rstd, rows, h, eps, status)
-  if (sweeps <= 1) TP_FWD(1);
-  else if (sweeps <= 2) TP_FWD(2);
-  else if (sweeps <= 4) TP_FWD(4);
-  else TP_FWD(8);
-#undef TP_FWD
-  count_launch();
-  return cudaGetLastError();
+  const double bytes = (double)sizeof(T) * rows * h *
+                           (n + 2 + (resid != nullptr ? 1 : 0)) +
+                       (y16 != nullptr ? 2.0 * rows * h : 0.0);
+  return norm_rows<T, 8>(P, n, zstride, bias, resid, out, d, gamma, y, y16,
+                         rstd, rows, h, eps, status, KF_REDUCE, bytes, stream);
 }
 
 #define TP_INST(T)                                                            \
