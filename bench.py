@@ -62,8 +62,11 @@ def parse_args(argv=None):
                     help="time one kernel alone on --shape (small cases for "
                          "profiler captures) instead of the workload")
     ap.add_argument("--shape", default="8192,57344,8192",
-                    help="gemm: M,N,K (C = A·Bᵀ, both K-major); rmsnorm_*: "
-                         "T,h; reduce: n,T,h")
+                    help="gemm: M,N,K (C = A·Bᵀ); rmsnorm_*: T,h; reduce: "
+                         "n,T,h")
+    ap.add_argument("--layout", default="kk", choices=["kk", "km", "mk", "mm"],
+                    help="gemm operand storage: A then B, k = K-major "
+                         "([rows, K]), m = MN-major ([K, rows])")
     return ap.parse_args(argv)
 
 
@@ -580,10 +583,11 @@ def single_kernel(args):
     bf = torch.bfloat16
     if args.kernel == "gemm":
         M, N, K = dims
-        A = I.normal((M, K), 1.0, 1, dev, bf)
-        Bm = I.normal((N, K), 0.02, 2, dev, bf)
+        a_mn, b_mn = args.layout[0] == "m", args.layout[1] == "m"
+        A = I.normal((K, M) if a_mn else (M, K), 1.0, 1, dev, bf)
+        Bm = I.normal((K, N) if b_mn else (N, K), 0.02, 2, dev, bf)
         C = torch.empty((M, N), dtype=bf, device=dev)
-        run = lambda: B.gemm(A, Bm, C)
+        run = lambda: B.gemm(A, Bm, C, a_mn_major=a_mn, b_mn_major=b_mn)
         flops, nbytes = 2.0 * M * N * K, 2.0 * (M * K + N * K + M * N)
     elif args.kernel in ("rmsnorm_fwd", "rmsnorm_bwd"):
         T, h = dims
@@ -630,6 +634,7 @@ def single_kernel(args):
     B.device_status()
     ms = prof["ms"] / max(prof["launches"], 1)
     rec = {"kernel": args.kernel, "family": fam, "shape": dims,
+           "layout": args.layout if args.kernel == "gemm" else None,
            "launches": prof["launches"], "ms_per_launch": ms,
            "algorithmic_bytes_per_launch": prof["bytes"] / prof["launches"]}
     if flops:
