@@ -21,7 +21,6 @@ workload.  `--impl reference` times that oracle alone (the reference arm).
 """
 
 import argparse
-import hashlib
 import json
 import os
 import subprocess
@@ -417,40 +416,14 @@ def reference_arm(args, cfg, world, rank):
     print(json.dumps(line), flush=True)
 
 
-# DRAM bytes per launch of the dominant kernel, from a committed ncu capture
-# of the same workload (profiles/): used only while the kernel's sources still
-# hash to the value recorded with the counters, else the traffic is unknown.
-TRAFFIC_PROFILES = {
-    ("gemm_tc", "layer_bf16"): (
-        "profiles/gemm_tc_traffic_layer_bf16_s8192.md",
-        ["megatron_tensor_transformer_gate_gb300/csrc/gemm_tc.cu",
-         "megatron_tensor_transformer_gate_gb300/csrc/gemm.h",
-         "megatron_tensor_transformer_gate_gb300/csrc/common.cuh"]),
+# DRAM traffic of the dominant kernel: the GEMM launches of the layer step
+# differ in shape, and profiler counter captures stay on single launches of a
+# few GB, so the line carries no per-launch traffic figure; each shape's
+# single-launch DRAM bytes are in this summary.
+TRAFFIC_NOTES = {
+    "gemm_tc": "profiles/gemm_tc_dram_single_launch.md (DRAM bytes of one "
+               "launch of each GEMM shape of the layer step)",
 }
-
-
-def committed_traffic(kernel, workload):
-    entry = TRAFFIC_PROFILES.get((kernel, workload))
-    if entry is None:
-        return None, None
-    summary, sources = entry
-    root = os.path.dirname(os.path.abspath(__file__))
-    try:
-        fields = {}
-        for line in open(os.path.join(root, summary)):
-            if ":" in line and line.split(":")[0] in (
-                    "traffic_per_launch_bytes", "source_sha256"):
-                k, v = line.split(":", 1)
-                fields[k.strip()] = v.strip()
-        h = hashlib.sha256()
-        for f in sources:
-            with open(os.path.join(root, f), "rb") as fh:
-                h.update(fh.read())
-    except OSError:
-        return None, None
-    if fields.get("source_sha256") != h.hexdigest():
-        return None, f"{summary} (stale: kernel sources changed since capture)"
-    return float(fields["traffic_per_launch_bytes"]), summary
 
 
 def roofline(prof, steps, peaks, peaks_src, workload=None):
@@ -478,10 +451,9 @@ def roofline(prof, steps, peaks, peaks_src, workload=None):
         sust = float(peaks.get("bf16_tflops_sustained",
                                peaks.get("bf16_tflops"))) * mult
         ach = (v["flops"] / v["launches"]) / (per_ms / 1e3) / 1e12
-        traffic, tsrc = committed_traffic(dom, workload)
         return {"bound": "tensor", "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
-                "traffic_source": tsrc, "kernel": dom,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "traffic_source": TRAFFIC_NOTES.get(dom), "kernel": dom,
                 "peak_sustained": sust, "frac_sustained": ach / sust,
                 "peak_source": f"{peaks_src} bf16_tflops (burst)" + (
                     " x 2 (nominal e4m3 / bf16 ratio)"
