@@ -276,8 +276,8 @@ typedef struct {
  * [T, h]), rstd₁, rstd₂ (fp32 [T]), then the attention block's ws and the
  * MLP block's ws (tp_attn_workspace_bytes, tp_mlp_workspace_bytes of the
  * blocks' descs); for TP_BF16 then the forward's fp16 operands of the Q, K,
- * V projections: the RMSNorm₁ output [T, h] and Wq, Wk, Wv.  Each region on
- * the next 256-byte boundary.
+ * V projections (one launch): the RMSNorm₁ output [T, h] and [Wq; Wk; Wv]
+ * stacked.  Each region on the next 256-byte boundary.
  * Precision (TP_BF16): the Q, K, V projections multiply fp16 copies of the
  * RMSNorm₁ output and of Wq, Wk, Wv (fp32 accumulation).  The softmax
  * multiplies the relative error of its input's rounding by the score scale

@@ -753,12 +753,13 @@ extern "C" size_t tp_attn_bwd_scratch_bytes(const tp_attn_desc* d) {
 
 namespace {
 // fp16 copies of the Q, K, V projections' operands: the input rows and the
-// three weights.  The layer passes them for its first block, whose input is
+// three weights, stacked [Wq; Wk; Wv] so that one launch computes all three
+// projections.  The layer passes them for its first block, whose input is
 // the RMSNorm output: the softmax amplifies the rounding of that input
 // (scores of a few units times its relative error), and fp16 keeps 3 more
 // mantissa bits than bf16 at the same bytes.
 struct QkvF16 {
-  const void *x = nullptr, *wq = nullptr, *wk = nullptr, *wv = nullptr;
+  const void *x = nullptr, *wqkv = nullptr;
 };
 
 tp_status attn_fwd_impl(const tp_attn_desc* d, const void* X, const void* Wq,
@@ -820,12 +821,20 @@ tp_status attn_fwd_impl(const tp_attn_desc* d, const void* X, const void* Wq,
     GemmProblem gv = proj(T, kd, op(xa, h, 0, T), op(f8 ? L.wvq : Wv, h, 0, kd),
                           h, L.v, kd);
     gq.epi.out_f16 = gk.epi.out_f16 = gv.epi.out_f16 = 1;
-    if (f16in != nullptr && !f8) {
-      gq.parts[0].a.ptr = gk.parts[0].a.ptr = gv.parts[0].a.ptr = f16in->x;
-      gq.parts[0].b.ptr = f16in->wq;
-      gk.parts[0].b.ptr = f16in->wk;
-      gv.parts[0].b.ptr = f16in->wv;
-      gq.f16 = gk.f16 = gv.f16 = 1;
+    const bool fused_qkv = f16in != nullptr && !f8;
+    if (fused_qkv) {
+      // one launch over the stacked fp16 weights: columns [0, qd) are Q,
+      // [qd, qd + kd) K and the rest V (tile widths divide qd and kd)
+      gq = proj(T, qd + 2 * kd, op(f16in->x, h, 0, T),
+                op(f16in->wqkv, h, 0, qd + 2 * kd), h, L.q, qd);
+      gq.f16 = 1;
+      gq.epi.out_f16 = 1;
+      gq.epi.split1 = qd;
+      gq.epi.out2 = L.k;
+      gq.epi.ldo2 = kd;
+      gq.epi.split2 = qd + kd;
+      gq.epi.out3 = L.v;
+      gq.epi.ldo3 = kd;
     }
     if (f8) {
       GemmProblem* gs[3] = {&gq, &gk, &gv};
@@ -836,8 +845,8 @@ tp_status attn_fwd_impl(const tp_attn_desc* d, const void* X, const void* Wq,
       }
     }
     err = run_gemm(gq, stream);
-    if (!err) err = run_gemm(gk, stream);
-    if (!err) err = run_gemm(gv, stream);
+    if (!err && !fused_qkv) err = run_gemm(gk, stream);
+    if (!err && !fused_qkv) err = run_gemm(gv, stream);
     if (err) return cuda_status(err);
     err = flash_fwd(attn_shape(d), L.q, L.k, L.v, L.o, L.lse,
                     device_status_ptr(), stream);
@@ -1305,9 +1314,9 @@ struct LayerFwdLayout {
   void *xn1 = nullptr, *x1 = nullptr, *xn2 = nullptr;
   float *rstd1 = nullptr, *rstd2 = nullptr;
   void *attn_ws = nullptr, *mlp_ws = nullptr;
-  // bf16 mode: fp16 copies of the first norm's output and of Wq, Wk, Wv,
-  // the operands of the Q, K, V projections (forward only)
-  void *xn1h = nullptr, *wqh = nullptr, *wkh = nullptr, *wvh = nullptr;
+  // bf16 mode: fp16 copies of the first norm's output and of [Wq; Wk; Wv]
+  // stacked, the operands of the Q, K, V projections (forward only)
+  void *xn1h = nullptr, *wqkvh = nullptr;
   size_t attn_bytes = 0, mlp_bytes = 0, bytes = 0;
 };
 
@@ -1331,9 +1340,7 @@ LayerFwdLayout layer_fwd_layout(const tp_layer_desc* d, void* ws) {
   if (d->dtype == TP_BF16) {
     const size_t qd = (size_t)d->n_q * d->d, kd = (size_t)d->n_kv * d->d;
     L.xn1h = c.take(th);
-    L.wqh = c.take(qd * (size_t)d->h * 2);
-    L.wkh = c.take(kd * (size_t)d->h * 2);
-    L.wvh = c.take(kd * (size_t)d->h * 2);
+    L.wqkvh = c.take((qd + 2 * kd) * (size_t)d->h * 2);
   }
   L.bytes = c.off;
   return L;
@@ -1409,15 +1416,18 @@ extern "C" tp_status tp_layer_fwd(const tp_layer_desc* d, const void* x,
       const int64_t qd = (int64_t)d->n_q * d->d, kd = (int64_t)d->n_kv * d->d;
       int err = rmsnorm_fwd<__nv_bfloat16>(x, g1, L.xn1, L.rstd1, T, h, d->eps,
                                            stream, L.xn1h, status);
-      if (!err) err = convert_f16(Wq, L.wqh, qd * h, status, stream);
-      if (!err) err = convert_f16(Wk, L.wkh, kd * h, status, stream);
-      if (!err) err = convert_f16(Wv, L.wvh, kd * h, status, stream);
+      char* wqkv = static_cast<char*>(L.wqkvh);
+      if (!err) err = convert_f16(Wq, wqkv, qd * h, status, stream);
+      if (!err)
+        err = convert_f16(Wk, wqkv + (size_t)qd * h * 2, kd * h, status,
+                          stream);
+      if (!err)
+        err = convert_f16(Wv, wqkv + (size_t)(qd + kd) * h * 2, kd * h,
+                          status, stream);
       if (err) return cuda_status(err);
       QkvF16 f16in;
       f16in.x = L.xn1h;
-      f16in.wq = L.wqh;
-      f16in.wk = L.wkh;
-      f16in.wv = L.wvh;
+      f16in.wqkv = L.wqkvh;
       const bool sp = d->mode == TP_REDUCE_SP;
       void* partials = nullptr;
       st = attn_fwd_impl(&ad, L.xn1, Wq, Wk, Wv, Wo, nullptr, x, L.x1,

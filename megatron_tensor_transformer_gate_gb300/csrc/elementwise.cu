@@ -330,9 +330,10 @@ __global__ void __launch_bounds__(256)
 
 // One block of 512 threads per chunk of consecutive rows (about one chunk
 // per SM); each thread owns the 16-byte column vectors {V·(tid + 512·j)},
-// keeps γ and its dγ partial sums in registers, and loads the next row's dy
-// and x while it finishes the current one.  Per row: dot = Σ dy·γ·x (block
-// reduction through a double-buffered slot, one barrier),
+// keeps its dγ partial sums in registers (γ comes from L1 each row), and
+// loads the next row's dy, x and dres while it finishes the current one.
+// Per row: dot = Σ dy·γ·x (block reduction through a double-buffered slot,
+// one barrier),
 //   dx = dres + rstd·dy·γ − x·rstd³·dot / h,   dγ_partial += dy·x·rstd.
 // SUM (the f reduction fused in, Megatron-SP backward): dy is not read but
 // formed per row as Σ_{i<n} P_i in fp32, in shard order, rounded once to T —
@@ -355,22 +356,14 @@ __global__ void __launch_bounds__(512, 1)
     col[j] = ((int64_t)threadIdx.x + 512 * j) * V;
     on[j] = col[j] < h;
   }
-  float g[NV * V], dgacc[NV * V];
+  float dgacc[NV * V];
 #pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    if (on[j]) {
-      Vec<T>::load(gamma + col[j], g + j * V);
-    } else {
-#pragma unroll
-      for (int q = 0; q < V; ++q) g[j * V + q] = 0.0f;
-    }
-#pragma unroll
-    for (int q = 0; q < V; ++q) dgacc[j * V + q] = 0.0f;
-  }
+  for (int q = 0; q < NV * V; ++q) dgacc[q] = 0.0f;
   const int64_t r_begin = (int64_t)blockIdx.x * rpc;
   const int64_t r_end = min(rows, r_begin + rpc);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 cd[NV], cx[NV];   // current row, raw 16-byte vectors
+  const bool has_res = dres != nullptr;
+  uint4 cd[NV], cx[NV], cr[NV];   // current row, raw 16-byte vectors
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     const bool ld = on[j] && r_begin < r_end;
@@ -379,9 +372,12 @@ __global__ void __launch_bounds__(512, 1)
                 : zero;
     cx[j] = ld ? *reinterpret_cast<const uint4*>(x + r_begin * h + col[j])
                : zero;
+    cr[j] = (has_res && ld)
+                ? *reinterpret_cast<const uint4*>(dres + r_begin * h + col[j])
+                : zero;
   }
   for (int64_t r = r_begin; r < r_end; ++r) {
-    uint4 nd[NV], nx[NV], dr[NV];
+    uint4 nd[NV], nx[NV], nr[NV];
     const bool more = r + 1 < r_end;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
@@ -391,12 +387,22 @@ __global__ void __launch_bounds__(512, 1)
       nx[j] = (more && on[j])
                   ? *reinterpret_cast<const uint4*>(x + (r + 1) * h + col[j])
                   : zero;
-      dr[j] = (dres != nullptr && on[j])
-                  ? *reinterpret_cast<const uint4*>(dres + r * h + col[j])
+      nr[j] = (has_res && more && on[j])
+                  ? *reinterpret_cast<const uint4*>(dres + (r + 1) * h +
+                                                    col[j])
                   : zero;
     }
     const float rs = rstd[r];
-    float d[NV * V], xv[NV * V];
+    float d[NV * V], xv[NV * V], g[NV * V];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      if (on[j]) {
+        Vec<T>::load(gamma + col[j], g + j * V);
+      } else {
+#pragma unroll
+        for (int q = 0; q < V; ++q) g[j * V + q] = 0.0f;
+      }
+    }
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       if constexpr (SUM) {
@@ -429,7 +435,7 @@ __global__ void __launch_bounds__(512, 1)
     for (int j = 0; j < NV; ++j) {
       if (!on[j]) continue;
       float o[V];
-      Vec<T>::from_raw(dr[j], o);
+      Vec<T>::from_raw(cr[j], o);
 #pragma unroll
       for (int q = 0; q < V; ++q)
         o[q] += rs * d[j * V + q] * g[j * V + q] - xv[j * V + q] * coef;
@@ -439,6 +445,7 @@ __global__ void __launch_bounds__(512, 1)
     for (int j = 0; j < NV; ++j) {
       cd[j] = nd[j];
       cx[j] = nx[j];
+      cr[j] = nr[j];
     }
   }
 #pragma unroll

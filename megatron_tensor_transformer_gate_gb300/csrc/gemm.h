@@ -64,6 +64,10 @@ struct GemmEpilogue {
   // EPI_STORE only: write fp16 instead of bf16 (the attention-core operands);
   // a value beyond the fp16 range records a range error in the status word
   int out_f16 = 0;
+  // EPI_STORE only: output columns [split1, split2) go to out2 (row stride
+  // ldo2) and [split2, N) to out3 (row stride ldo3), each from its own column
+  // 0 — one launch writing several tensors (0 = no split; multiples of 32)
+  int64_t split1 = 0, split2 = 0, ldo3 = 0;
   // FP8 operands (GemmProblem::dtype 2): device pointers to the per-tensor
   // quantization scales of A and B; the accumulator is multiplied by
   // 1 / (scale_a·scale_b) before the rest of the epilogue

@@ -211,12 +211,24 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p,
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] += rr[i];
         }
-        const int64_t off =
-            (int64_t)z * e.out_z_stride + (int64_t)m * e.ldo + n;
+        void* dst = e.out;
+        int64_t ld = e.ldo, col = n;
+        if (e.split1 != 0 && n >= e.split1) {
+          if (e.split2 != 0 && n >= e.split2) {
+            dst = e.out3;
+            ld = e.ldo3;
+            col = n - e.split2;
+          } else {
+            dst = e.out2;
+            ld = e.ldo2;
+            col = n - e.split1;
+          }
+        }
+        const int64_t off = (int64_t)z * e.out_z_stride + (int64_t)m * ld + col;
         if (e.out_f16)
-          store32_f16(static_cast<__half*>(e.out) + off, v, valid, p.status);
+          store32_f16(static_cast<__half*>(dst) + off, v, valid, p.status);
         else
-          store32_bf16(static_cast<__nv_bfloat16*>(e.out) + off, v, valid);
+          store32_bf16(static_cast<__nv_bfloat16*>(dst) + off, v, valid);
       } else if constexpr (EPI == EPI_GELU) {
         if (e.bias != nullptr) {
           float b[32];
@@ -590,6 +602,10 @@ int launch_gemm_tc(const GemmProblem& pr, void* stream, unsigned* status) {
     if (pr.parts[i].a.mn_major != a_mn || pr.parts[i].b.mn_major != b_mn)
       return cudaErrorInvalidValue;
   if (e.kind == EPI_SWIGLU && (b_mn || a_mn || pr.nparts != 1))
+    return cudaErrorInvalidValue;
+  if ((e.split1 || e.split2) &&
+      (e.kind != EPI_STORE || e.split1 % 32 || e.split2 % 32 ||
+       (e.split2 && e.split2 < e.split1) || pr.nz != 1))
     return cudaErrorInvalidValue;
   const bool f8 = pr.dtype == 2;
   const bool f16 = !f8 && pr.f16 != 0;

@@ -240,13 +240,12 @@ def test_layer_workspaces_are_the_blocks_plus_the_norm_buffers(tp):
         mw = tp.mlp_workspace_bytes(tp.mlp_desc(T, h, f, n, dt, tp.SWIGLU))
         assert aw > 0 and mw > 0
         # xn1, x1, xn2 (bf16), rstd1, rstd2 (fp32), attention ws, MLP ws;
-        # bf16 mode: then the fp16 copies of xn1, Wq, Wk, Wv
+        # bf16 mode: then the fp16 copies of xn1 and of [Wq; Wk; Wv]
         base = 3 * up(T * h * 2) + 2 * up(T * 4) + up(aw)
         qd, kd = nq * d, nkv * d
         if dt == tp.BF16:
             assert tp.layer_workspace_bytes(ld) == (
-                base + up(mw) + up(T * h * 2) + up(qd * h * 2)
-                + up(kd * h * 2) + kd * h * 2)
+                base + up(mw) + up(T * h * 2) + (qd + 2 * kd) * h * 2)
         else:
             assert tp.layer_workspace_bytes(ld) == base + mw
         ab = tp.attn_bwd_scratch_bytes(tp.attn_desc(b, s, h, nq, nkv, d, n, dt))
