@@ -4,25 +4,27 @@
 // head over the sequence; [Troverld] §I.O FlashAttention: row-blocked with an
 // online softmax, O(S) statistics written for the backward pass).
 //
-// One CTA = 128 query rows of one (batch, q head); 192 threads:
-//   warp 0     TMA: the Q tile once, then K_j and V_j (128 keys each) into
-//              two independent 2-stage rings (fp16, 128-byte swizzle, two
-//              64-column halves); lane 0 feeds K, lane 1 feeds V.
-//   warp 1     allocates 512 TMEM columns and issues, per key block j,
-//                S_j = Q·K_jᵀ   (M=128, N=128, K=128) into TMEM S[j mod 2]
-//                O += P_j·V_j   (M=128, N=128, K=128) into TMEM O, with
-//                               P_j read from TMEM P[j mod 2]
-//              with the scores two blocks ahead (S_0, S_1, S_2, PV_0, S_3,
-//              PV_1, …) so the tensor cores never wait for a softmax block.
-//   warps 2–9  softmax, two threads per query row (same TMEM lane, one per
-//              64-column half), reference
-//              max m and sum l in fp32, P_j = exp2(S·scale·log2e − m) stored
-//              as fp16 pairs into TMEM (double-buffered, so block j+1 is
-//              written while O += P_j·V_j runs).
-//              O accumulates in TMEM; when a block's max exceeds
-//              m by more than 2^8 the softmax rescales O and l by
-//              exp2(m − m_new) first.  The epilogue writes O / l (bf16) and
-//              LSE = (m + log2 l)·ln 2.
+// One CTA = two query tiles of 128 rows that read the same keys and values:
+// two q heads of one GQA group at the same query block when the group size is
+// even, else two consecutive query blocks of one head.  320 threads:
+//   warp 0     TMA: both Q tiles once, then K_0, K_1, V_0, K_2, V_1, … (the
+//              order the MMAs use them) through one 3-slot ring (fp16,
+//              128-byte swizzle, two 64-column halves per tile).
+//   warp 1     allocates 512 TMEM columns (S and O of each tile) and issues,
+//              per key block j and tile t,
+//                S_t = Q_t·K_jᵀ     (M=128, N=128, K=128) into TMEM S[t]
+//                O_t += P_t·V_j     (M=128, N=128, K=128) into TMEM O[t],
+//                                   P_t read from shared memory
+//              S_t for block j+1 as soon as tile t's softmax has copied S_t
+//              of block j to registers, so the scores of the next block are
+//              computed while the softmax of this one runs, and the other
+//              tile's MMAs fill the tensor pipe meanwhile.
+//   warps 2–9  softmax, one thread per query row (warps 2–5 tile 0, 6–9
+//              tile 1): reference max m and sum l in fp32, P = exp2(S·scale·
+//              log2e − m) stored as fp16 into the tile's P buffer.  O
+//              accumulates in TMEM; when a block's max exceeds m by more than
+//              2^8 the softmax rescales O and l by exp2(m − m_new) first.  The
+//              epilogue writes O / l (bf16) and LSE = (m + log2 l)·ln 2.
 // Operands are fp16 and accumulation fp32: the softmax amplifies score
 // errors, and bf16 operands (8-bit mantissa) put the row-wise error of causal
 // outputs above 3e-2 of the row rms, while fp16 (10-bit mantissa, same bytes)
@@ -42,65 +44,74 @@ namespace tp {
 namespace {
 
 constexpr int HD = 128;
-constexpr int BLK = 128;                 // queries per CTA, keys per block
+constexpr int BLK = 128;                 // queries per tile, keys per block
 constexpr int ATOM = BLK * 128;          // one 64-column half: 128 rows × 128 B
 constexpr int TILE = 2 * ATOM;           // 32 KB fp16 tile [128][128]
-constexpr int THREADS = 320;   // TMA, MMA, 8 softmax warps
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE;      // 2 stages
-constexpr int OFF_V = OFF_K + 2 * TILE;  // 2 stages
-constexpr int OFF_BAR = OFF_V + 2 * TILE;
-constexpr int OFF_RED = OFF_BAR + 256;   // row-max / row-sum exchange
-constexpr int RED_SLOTS = 3;             // 2 for block parity, 1 for the end
-constexpr int OFF_SEQ = OFF_RED + RED_SLOTS * 2 * 128 * 4;
-constexpr int SMEM = OFF_SEQ + RED_SLOTS * 2 * 128 * 4 + 1024;
+constexpr int NT = 2;                    // query tiles per CTA
+constexpr int NSLOT = 3;                 // K/V ring slots
+constexpr int THREADS = 64 + NT * 128;   // TMA warp, MMA warp, softmax rows
+constexpr int OFF_Q = 0;                 // NT tiles
+constexpr int OFF_P = OFF_Q + NT * TILE; // NT tiles (A operand of O += P·V)
+constexpr int OFF_KV = OFF_P + NT * TILE;
+constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
+constexpr int SMEM = OFF_BAR + 256 + 1024;   // + slack for 1024-B alignment
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM: S[2] in columns 0-255, O in 256-383, P[2] (fp16 pairs, the A
-// operand of O += P·V) in 384-511.
-constexpr uint32_t COL_O = 256, COL_P = 384;
+// TMEM: S of tile t in columns [128·t, 128·t + 128), O of tile t in
+// [256 + 128·t, 384 + 128·t).
+constexpr uint32_t COL_O = 256;
 // The output accumulates in TMEM against a reference max m; it is rescaled
 // only when a block's row max exceeds m by more than this (log2 units), which
 // keeps the fp16 probabilities ≤ 2^8 and the fp32 accumulator far from
 // overflow.
 constexpr float RESCALE_LOG2 = 8.0f;
 
-// Exchange of one float between the two threads that own a query row: write
-// this thread's value with a sequence tag, then wait (bounded, abort-aware)
-// until the partner's entry carries the same tag.  Returns false when it gave
-// up.
-__device__ __forceinline__ bool pair_exchange(float* val, int* seq, int self,
-                                              int other, float mine, int tag,
-                                              float* theirs,
-                                              volatile int* abort_flag,
-                                              unsigned* status) {
-  val[self] = mine;
-  __threadfence_block();
-  reinterpret_cast<volatile int*>(seq)[self] = tag;
-  volatile int* ps = reinterpret_cast<volatile int*>(seq) + other;
-  if (*ps != tag) {
-    const long long t0 = clock64();
-    while (*ps != tag) {
-      if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitTimeoutCycles) {
-        record_error(status, kDevTimeout, 20);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-  __threadfence_block();
-  *theirs = reinterpret_cast<volatile float*>(val)[other];
-  return true;
-}
-
 struct FwdTcArgs {
   CUtensorMap mq, mk, mv;
   __nv_bfloat16* O;
   float* LSE;
-  int s, nq, nkv, causal;
+  int s, nb, nq, nkv, causal, pair_heads;
   float scale_log2;
   unsigned* status;
 };
+
+// The CTA's two query tiles: batch, kv head, and per tile its q head, first
+// query row and number of key blocks (0 for a tile past the sequence end).
+// The 1-D grid has the block rank slowest, so the heaviest (last, under the
+// causal mask) query blocks of every head start first.
+struct Tiles {
+  int b, kvh;
+  int head[NT], q0[NT], nkb[NT];
+};
+
+__device__ __forceinline__ Tiles cta_tiles(const FwdTcArgs& a) {
+  Tiles T;
+  const int nblk = (a.s + BLK - 1) / BLK;
+  if (a.pair_heads) {
+    const int hp = a.nq / 2;
+    const int per = a.nb * hp;
+    const int rank = blockIdx.x / per, rem = blockIdx.x % per;
+    T.b = rem / hp;
+    for (int t = 0; t < NT; ++t) {
+      T.head[t] = 2 * (rem % hp) + t;
+      T.q0[t] = (nblk - 1 - rank) * BLK;
+    }
+  } else {
+    const int npair = (nblk + 1) / 2;
+    const int per = a.nb * a.nq;
+    const int rank = blockIdx.x / per, rem = blockIdx.x % per;
+    T.b = rem / a.nq;
+    for (int t = 0; t < NT; ++t) {
+      T.head[t] = rem % a.nq;
+      T.q0[t] = (2 * (npair - 1 - rank) + t) * BLK;
+    }
+  }
+  T.kvh = T.head[0] / (a.nq / a.nkv);
+  for (int t = 0; t < NT; ++t) {
+    const int kv_end = a.causal ? min(a.s, T.q0[t] + BLK) : a.s;
+    T.nkb[t] = T.q0[t] < a.s ? (kv_end + BLK - 1) / BLK : 0;
+  }
+  return T;
+}
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk) {
   // K-major tile of two 64-column halves: K step kk (16 columns)
@@ -111,55 +122,62 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
   return smem_desc_sw128(base + kk * 2048, ATOM, 1024);
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+// Row r of a 128-row K-major swizzled half tile (128-byte rows): its eight
+// 16-byte chunks from 32 packed words (the layout TMA writes with the 128-byte
+// swizzle, which the MMA descriptors above read).
+__device__ __forceinline__ void st_row(uint8_t* half_tile, int r,
+                                       const uint32_t (&pk)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    *reinterpret_cast<uint4*>(half_tile + r * 128 + ((q ^ (r & 7)) << 4)) =
+        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+
+__device__ __forceinline__ float max3f(float x, float y, float z) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+  return r;
+}
+
+// 168 registers a thread: ten warps, three on some SM sub-partitions
+// (16384 registers each)
+__global__ void __maxnreg__(168)
     attn_fwd_tc_kernel(const __grid_constant__ FwdTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* k_full = bar + 1;     // [2]
-  uint64_t* k_empty = bar + 3;    // [2]
-  uint64_t* v_full = bar + 5;     // [2]
-  uint64_t* v_empty = bar + 7;    // [2]
-  uint64_t* s_full = bar + 9;     // [2]
-  uint64_t* s_free = bar + 11;    // [2] scores copied to registers
-  uint64_t* p_full = bar + 13;    // [2]
-  uint64_t* pv_done = bar + 15;   // [2]
-  uint64_t* drain = bar + 17;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 18);
+  uint64_t* kv_full = bar + 1;    // [NSLOT]
+  uint64_t* kv_empty = bar + 4;   // [NSLOT]
+  uint64_t* s_full = bar + 7;     // [NT] S_t written
+  uint64_t* s_free = bar + 9;     // [NT] S_t copied to registers
+  uint64_t* p_full = bar + 11;    // [NT] P_t written (and O_t rescaled)
+  uint64_t* pv_done = bar + 13;   // [NT] O_t += P_t·V done (P_t free)
+  uint64_t* drain = bar + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // 1-D grid, block rank slowest: the heaviest (last, under the causal
-  // mask) query blocks of every head start first, which shortens the tail
-  const int nblk = (a.s + BLK - 1) / BLK;
-  const int per = gridDim.x / nblk;   // n_q · batch
-  const int rank = blockIdx.x / per, rem = blockIdx.x % per;
-  const int b = rem / a.nq, j = rem % a.nq;
-  const int q0 = (nblk - 1 - rank) * BLK;
-  const int kvh = j / (a.nq / a.nkv);
-  const int kv_end = a.causal ? min(a.s, q0 + BLK) : a.s;
-  const int nkb = (kv_end + BLK - 1) / BLK;
+  const Tiles T = cta_tiles(a);
+  const int nk = max(T.nkb[0], T.nkb[1]);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 256);
-      mbar_init(&p_full[i], 256);
-      mbar_init(&pv_done[i], 1);
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 128);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&pv_done[t], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < RED_SLOTS * 2 * 128; i += THREADS)
-    reinterpret_cast<int*>(sm + OFF_SEQ)[i] = 0;
   if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -167,94 +185,121 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane < 2) {
+    if (lane == 0) {
       // ------------------------------------------------------------- TMA --
-      // lane 0: Q, then the K ring; lane 1: the V ring.  K_j is released as
-      // soon as S_j is done, V_j only after O += P_j·V_j, so the two rings
-      // advance independently.
-      const bool is_k = lane == 0;
-      const CUtensorMap* map = is_k ? &a.mk : &a.mv;
-      uint64_t* full = is_k ? k_full : v_full;
-      uint64_t* empty = is_k ? k_empty : v_empty;
-      uint8_t* ring = sm + (is_k ? OFF_K : OFF_V);
-      tma_prefetch_desc(map);
+      // The ring carries K_0, then K_{j+1} and V_j for each block j: a K
+      // slot is released once both tiles' S MMAs have read it, a V slot once
+      // both O += P·V have.
+      tma_prefetch_desc(&a.mq);
+      tma_prefetch_desc(&a.mk);
+      tma_prefetch_desc(&a.mv);
+      const int ntiles = T.nkb[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, ntiles * TILE);
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+        if (t < ntiles)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+          tma_load_3d(sm + OFF_Q + t * TILE + hh * ATOM, &a.mq, q_full,
+                      T.head[t] * HD + hh * 64, T.q0[t], T.b);
       uint32_t armed = 0, armed_par = 0;
-      if (is_k) {
-        tma_prefetch_desc(&a.mq);
-        mbar_arrive_expect_tx(q_full, TILE);
-        for (int hh = 0; hh < 2; ++hh)
-          tma_load_3d(sm + OFF_Q + hh * ATOM, &a.mq, q_full, j * HD + hh * 64,
-                      q0, b);
-      }
-      for (int jb = 0; jb < nkb; ++jb) {
-        const int st = jb & 1;
-        const uint32_t ph = (jb >> 1) & 1;
-        if (!mbar_wait(&empty[st], ph ^ 1, abort_flag, a.status, 11)) break;
-        mbar_arrive_expect_tx(&full[st], TILE);
+      int e = 0;
+      auto put = [&](const CUtensorMap* map, int jb) -> bool {
+        const int st = e % NSLOT;
+        const uint32_t ph = (e / NSLOT) & 1;
+        if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, a.status, 11))
+          return false;
+        mbar_arrive_expect_tx(&kv_full[st], TILE);
         armed |= 1u << st;
         armed_par = (armed_par & ~(1u << st)) | (ph << st);
         for (int hh = 0; hh < 2; ++hh)
-          tma_load_3d(ring + st * TILE + hh * ATOM, map, &full[st],
-                      kvh * HD + hh * 64, jb * BLK, b);
+          tma_load_3d(sm + OFF_KV + st * TILE + hh * ATOM, map, &kv_full[st],
+                      T.kvh * HD + hh * 64, jb * BLK, T.b);
+        ++e;
+        return true;
+      };
+      bool ok = put(&a.mk, 0);
+      for (int jb = 0; ok && jb < nk; ++jb) {
+        if (jb + 1 < nk) ok = put(&a.mk, jb + 1);
+        if (ok) ok = put(&a.mv, jb);
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
-        if (is_k) mbar_wait(q_full, 0, &no_abort, nullptr, 0);
-        for (int st = 0; st < 2; ++st)
+        mbar_wait(q_full, 0, &no_abort, nullptr, 0);
+        for (int st = 0; st < NSLOT; ++st)
           if (armed & (1u << st))
-            mbar_wait(&full[st], (armed_par >> st) & 1u, &no_abort, nullptr, 0);
+            mbar_wait(&kv_full[st], (armed_par >> st) & 1u, &no_abort, nullptr,
+                      0);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------- MMA --
-      // Score tiles run two blocks ahead of O += P·V: S_{j+2} is issued as
-      // soon as the softmax has copied S_j to registers, so the tensor
-      // cores never wait for the softmax to finish a block.
       constexpr uint32_t IDESC_S = idesc_f16_f32(128, 128, 0, 0);
       constexpr uint32_t IDESC_O = idesc_f16_f32(128, 128, 0, 1);
-      const uint32_t sQ = smem_u32(sm + OFF_Q);
       bool ok = mbar_wait(q_full, 0, abort_flag, a.status, 12);
-      auto s_mma = [&](int jb) -> bool {
-        const int st = jb & 1;
-        if (!mbar_wait(&k_full[st], (jb >> 1) & 1, abort_flag, a.status, 15))
+      int e = 0;
+      uint32_t sKV = 0;
+      auto take = [&]() -> bool {
+        if (!mbar_wait(&kv_full[e % NSLOT], (e / NSLOT) & 1, abort_flag,
+                       a.status, 13))
           return false;
         tc_fence_after();
-        const uint32_t sK = smem_u32(sm + OFF_K + st * TILE);
+        sKV = smem_u32(sm + OFF_KV + (e % NSLOT) * TILE);
+        return true;
+      };
+      auto give = [&]() {
+        tc_commit(&kv_empty[e % NSLOT]);
+        ++e;
+      };
+      auto s_mma = [&](int t) {
+        const uint32_t sQ = smem_u32(sm + OFF_Q + t * TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem + st * 128, desc_kmajor(sQ, kk), desc_kmajor(sK, kk),
+          tc_mma_f16(tmem + t * 128, desc_kmajor(sQ, kk), desc_kmajor(sKV, kk),
                      IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(&s_full[st]);
-        tc_commit(&k_empty[st]);
-        return true;
+        tc_commit(&s_full[t]);
       };
-      // O += P_i·V_i; the softmax rescaled O (if needed) before p_full[i]
-      auto pv = [&](int i) -> bool {
-        if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort_flag, a.status, 13) ||
-            !mbar_wait(&v_full[i & 1], (i >> 1) & 1, abort_flag, a.status, 14))
-          return false;
-        tc_fence_after();
-        const uint32_t sV = smem_u32(sm + OFF_V + (i & 1) * TILE);
+      if (ok && (ok = take())) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16_ts(tmem + COL_O, tmem + COL_P + (i & 1) * 64 + kk * 8,
-                        desc_mnmajor(sV, kk), IDESC_O,
-                        (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&pv_done[i & 1]);
-        tc_commit(&v_empty[i & 1]);
-        return true;
-      };
-      if (ok) ok = s_mma(0);
-      if (ok && nkb > 1) ok = s_mma(1);
-      for (int jb = 0; ok && jb < nkb; ++jb) {
-        if (jb + 2 < nkb) {
-          ok = mbar_wait(&s_free[jb & 1], (jb >> 1) & 1, abort_flag, a.status,
-                         16) &&
-               s_mma(jb + 2);
+        for (int t = 0; t < NT; ++t)
+          if (T.nkb[t] > 0) s_mma(t);
+        give();
+      }
+      for (int jb = 0; ok && jb < nk; ++jb) {
+        if (jb + 1 < nk) {
+          if (!(ok = take())) break;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (!ok || jb + 1 >= T.nkb[t]) continue;
+            // S_t is free once tile t's softmax has copied block jb out
+            if (!(ok = mbar_wait(&s_free[t], jb & 1, abort_flag, a.status, 14)))
+              break;
+            tc_fence_after();
+            s_mma(t);
+          }
           if (!ok) break;
+          give();
         }
-        ok = pv(jb);
+        if (!(ok = take())) break;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (!ok || jb >= T.nkb[t]) continue;
+          // O_t += P_t·V_jb; the softmax rescaled O_t (if needed) before
+          // signalling P_t
+          if (!(ok = mbar_wait(&p_full[t], jb & 1, abort_flag, a.status, 15)))
+            break;
+          tc_fence_after();
+          const uint32_t sP = smem_u32(sm + OFF_P + t * TILE);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_f16(tmem + COL_O + t * 128, desc_kmajor(sP, kk),
+                       desc_mnmajor(sKV, kk), IDESC_O,
+                       (jb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&pv_done[t]);
+        }
+        if (!ok) break;
+        give();
       }
       if (*abort_flag) {
         volatile int no_abort = 0;
@@ -264,110 +309,81 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // --------------------------------------------------------- softmax --
-    // Two warps per row: `half` 0 owns key columns and output columns 0-63,
-    // half 1 owns 64-127; the two threads of a row (same TMEM lane) exchange
-    // the row max through shared memory each block, tagged with the block
-    // index (slots alternate by block parity; slot 2 carries the final sums).
-    const int sw = warp - 2;
-    const int half = sw >> 2;
+    // thread: query row r of tile t (TMEM lane r), all 128 key columns
+    const int t = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
+    const int nkb = t ? T.nkb[1] : T.nkb[0];
+    const int q0 = t ? T.q0[1] : T.q0[0];
+    const int head = t ? T.head[1] : T.head[0];
     const int qi = q0 + r;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* red = reinterpret_cast<float*>(sm + OFF_RED);  // [slot][half][row]
-    int* seq = reinterpret_cast<int*>(sm + OFF_SEQ);
+    const uint32_t lane_base =
+        tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t s_col = lane_base + t * 128;
+    const uint32_t o_col = lane_base + COL_O + t * 128;
+    uint8_t* ptile = sm + OFF_P + t * TILE;
     const float c = a.scale_log2;
     const float thr = RESCALE_LOG2 / c;   // the rescale threshold in raw units
-    float m_ref = -INFINITY, l_part = 0.0f;
+    float m_ref = -INFINITY, l_run = 0.0f;
     bool ok = true;
     for (int jb = 0; jb < nkb; ++jb) {
-      const int st = jb & 1;
-      if (!mbar_wait_warp(&s_full[st], (jb >> 1) & 1, abort_flag, a.status,
-                          16)) {
+      if (!mbar_wait_warp(&s_full[t], jb & 1, abort_flag, a.status, 16)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t v[2][32];
-      tmem_ld32(lane_base + st * 128 + half * 64, v[0]);
-      tmem_ld32(lane_base + st * 128 + half * 64 + 32, v[1]);
+      uint32_t v[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(s_col + cc * 32, v[cc]);
       tmem_ld_wait(v[0]);
       reg_fence32(v[1]);
+      reg_fence32(v[2]);
+      reg_fence32(v[3]);
       tc_fence_before();
-      mbar_arrive(&s_free[st]);   // S buffer st may take S_{j+2} now
-      const int k0 = jb * BLK + half * 64;
+      mbar_arrive(&s_free[t]);   // S_t may take the next block's scores now
       if ((jb + 1) * BLK > a.s || (a.causal && (jb + 1) * BLK - 1 > q0)) {
         // diagonal or ragged block: invalid keys become −inf (branch-free)
-        const int kmax = a.causal ? min(qi, a.s - 1) : a.s - 1;
+        const int lim = (a.causal ? min(qi, a.s - 1) : a.s - 1) - jb * BLK;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc)
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            v[cc][i] = (k0 + cc * 32 + i <= kmax) ? v[cc][i]
-                                                  : __float_as_uint(-INFINITY);
+            v[cc][i] = (cc * 32 + i <= lim) ? v[cc][i]
+                                            : __float_as_uint(-INFINITY);
       }
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         mx8[i] = fmaxf(__uint_as_float(v[0][i]), __uint_as_float(v[0][i + 8]));
 #pragma unroll
-      for (int i = 16; i < 64; ++i)
-        mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(v[i >> 5][i & 31]));
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      float mx_other;
-      const bool got = pair_exchange(red, seq, (st * 2 + half) * 128 + r,
-                                     (st * 2 + (half ^ 1)) * 128 + r, mx,
-                                     jb + 1, &mx_other, abort_flag, a.status);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, mx_other);
+      for (int i = 16; i < 128; i += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mx8[k] = max3f(mx8[k], __uint_as_float(v[i >> 5][(i & 31) + k]),
+                         __uint_as_float(v[i >> 5][(i & 31) + k + 8]));
+      const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]),
+                             max3f(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
+      // a new reference max when the block's max exceeds it by more than
+      // the threshold (warp-uniform decision, rows that keep theirs get 1)
+      float alpha = 1.0f;
+      bool rescale = false;
       if (jb == 0) {
         m_ref = mx;
       } else if (__any_sync(0xffffffffu, mx > m_ref + thr)) {
-        // rescale this warp's half of the TMEM accumulator once
-        // O += P_{j-1}·V_{j-1} has landed; the whole warp takes part (TMEM
-        // access is warp-collective), rows that keep their reference scale
-        // by 1.  Both warps of a pair see the same rows and decide alike.
-        const int pj = jb - 1;
-        if (!mbar_wait_warp(&pv_done[pj & 1], (pj >> 1) & 1, abort_flag,
-                            a.status, 17)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
         const float m_new = mx > m_ref + thr ? mx : m_ref;
-        const float alpha = ex2_approx((m_ref - m_new) * c);
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t o[32];
-          const uint32_t ta = lane_base + COL_O + half * 64 + cc * 32;
-          tmem_ld32(ta, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(ta, o);
-        }
-        l_part *= alpha;
+        alpha = ex2_approx((m_ref - m_new) * c);
         m_ref = m_new;
+        rescale = true;
       }
-      // P buffer st is free once O += P_{j-2}·V_{j-2} has completed
-      if (jb >= 2 && !mbar_wait_warp(&pv_done[st], ((jb - 2) >> 1) & 1,
-                                     abort_flag, a.status, 18)) {
-        ok = false;
-        break;
-      }
-      // P = exp2(c·(s − m)) in fp16 pairs into this half's 32 columns of P[st]
+      // P = exp2(c·(s − m)) in fp16 pairs: keys 0–63 in pk[0], 64–127 in pk[1]
       const float neg = -m_ref * c;
       float sum8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
-      uint32_t pk[32];
+      uint32_t pk[2][32];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(v[cc][i]), c, neg));
@@ -375,35 +391,52 @@ __global__ void __launch_bounds__(THREADS, 1)
               ex2_approx(fmaf(__uint_as_float(v[cc][i + 1]), c, neg));
           sum8[i & 7] += p0;
           sum8[(i + 1) & 7] += p1;
-          pk[cc * 16 + (i >> 1)] = pack_f16x2(p0, p1);
+          pk[cc >> 1][(cc & 1) * 16 + (i >> 1)] = pack_f16x2(p0, p1);
         }
       }
-      tmem_st32(lane_base + COL_P + st * 64 + half * 32, pk);
-      l_part += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      tc_fence_before();
-      mbar_arrive(&p_full[st]);
-    }
-    // epilogue: the row sum is the two halves' partial sums; wait for the
-    // last O += P·V, then O / l for this warp's 64 columns and the LSE
-    float l_other = 0.0f;
-    if (__all_sync(0xffffffffu, ok))
-      ok = pair_exchange(red, seq, (4 + half) * 128 + r,
-                         (4 + (half ^ 1)) * 128 + r, l_part, nkb + 1, &l_other,
-                         abort_flag, a.status);
-    const int last = nkb - 1;
-    if (__all_sync(0xffffffffu, ok) &&
-        mbar_wait_warp(&pv_done[last & 1], (last >> 1) & 1, abort_flag,
-                       a.status, 19)) {
-      tc_fence_after();
-      const float l_run = l_part + l_other;
-      const float inv = 1.0f / l_run;
-      __nv_bfloat16* dst = a.O + ((int64_t)b * a.s + qi) * (int64_t)(a.nq * HD) +
-                           j * HD + half * 64;
+      // O_t += P·V of the previous block must have completed before O_t is
+      // rescaled and before the P buffer is overwritten
+      if (jb >= 1 && !mbar_wait_warp(&pv_done[t], (jb - 1) & 1, abort_flag,
+                                     a.status, 17)) {
+        ok = false;
+        break;
+      }
+      if (rescale) {
+        // the whole warp takes part (TMEM access is warp-collective)
+        tc_fence_after();
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(o_col + cc * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(o_col + cc * 32, o);
+        }
+      }
+      st_row(ptile, r, pk[0]);
+      st_row(ptile + ATOM, r, pk[1]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+      l_run = l_run * alpha +
+              (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+               ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+    }
+    // epilogue: wait for the last O_t += P·V, then O / l and the LSE
+    const int last = nkb - 1;
+    if (nkb > 0 && __all_sync(0xffffffffu, ok) &&
+        mbar_wait_warp(&pv_done[t], last & 1, abort_flag, a.status, 19)) {
+      tc_fence_after();
+      const float inv = 1.0f / l_run;
+      __nv_bfloat16* dst = a.O + ((int64_t)T.b * a.s + qi) *
+                                     (int64_t)(a.nq * HD) +
+                           head * HD;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t o[32];
-        tmem_ld32(lane_base + COL_O + half * 64 + cc * 32, o);
+        tmem_ld32(o_col + cc * 32, o);
         tmem_ld_wait(o);
         if (qi < a.s) {
 #pragma unroll
@@ -421,8 +454,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (half == 0 && qi < a.s)
-        a.LSE[((int64_t)b * a.nq + j) * a.s + qi] =
+      if (qi < a.s)
+        a.LSE[((int64_t)T.b * a.nq + head) * a.s + qi] =
             (m_ref * c + log2f(l_run)) * 0.69314718055994531f;
     }
   }
@@ -455,12 +488,18 @@ int flash_fwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   a.O = static_cast<__nv_bfloat16*>(O);
   a.LSE = LSE;
   a.s = (int)sh.s;
+  a.nb = (int)sh.b;
   a.nq = sh.nq;
   a.nkv = sh.nkv;
   a.causal = sh.causal;
+  // two heads of a GQA group share a CTA when the group size is even
+  a.pair_heads = (sh.nq / sh.nkv) % 2 == 0;
   a.scale_log2 = sh.scale * 1.4426950408889634f;
   a.status = status;
-  const unsigned grid = (unsigned)(((sh.s + BLK - 1) / BLK) * sh.nq * sh.b);
+  const int64_t nblk = (sh.s + BLK - 1) / BLK;
+  const unsigned grid =
+      (unsigned)(a.pair_heads ? nblk * (sh.nq / 2) * sh.b
+                              : (nblk + 1) / 2 * sh.nq * sh.b);
   const double s = (double)sh.s;
   const double pairs = sh.causal ? s * (s + 1.0) / 2.0 : s * s;
   {
