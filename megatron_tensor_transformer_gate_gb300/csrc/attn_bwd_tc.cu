@@ -118,9 +118,14 @@ __device__ __forceinline__ void store_bf16_row64(__nv_bfloat16* dst,
 }
 
 // ---------------------------------------------------------------- pre-pass --
-// One warp per (batch, head, padded position): D = Σ_d dO·O (dO fp16, O
-// bf16) and L2 = LSE·log2e.  Past the sequence end D = 0 and L2 = +∞, so
-// that P = exp2(S·c − L2) of a padded query is exactly 0 without a mask.
+// D = Σ_d dO·O (dO fp16, O bf16) and L2 = LSE·log2e per (batch, head,
+// padded position).  One warp takes eight consecutive positions of one
+// (batch, head), half a warp per row and 16 bytes of each tensor per lane,
+// and issues all eight rows' loads before it uses any, so that enough bytes
+// are in flight to stream the two tensors.  Past the sequence end D = 0 and
+// L2 = +∞, so that P = exp2(S·c − L2) of a padded query is exactly 0
+// without a mask.
+constexpr int PRE_ROWS = 8;
 __global__ void __launch_bounds__(256)
     attn_bwd_prepass_kernel(const __nv_bfloat16* __restrict__ O,
                             const __half* __restrict__ dO,
@@ -129,25 +134,45 @@ __global__ void __launch_bounds__(256)
                             int b_, int nq, int s, int s_pad) {
   const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (w >= (int64_t)b_ * nq * s_pad) return;
-  const int pos = (int)(w % s_pad);
-  const int64_t bh = w / s_pad;   // b·nq + head
+  const int per = s_pad / PRE_ROWS;
+  if (w >= (int64_t)b_ * nq * per) return;
+  const int64_t bh = w / per;      // b·nq + head
+  const int pos0 = (int)(w % per) * PRE_ROWS;
   const int head = (int)(bh % nq);
   const int64_t bb = bh / nq;
-  float acc = 0.0f;
-  if (pos < s) {
-    const int64_t off = ((bb * s + pos) * nq + head) * HD + lane * 4;
-    const uint2 uo = *reinterpret_cast<const uint2*>(O + off);
-    const uint2 ud = *reinterpret_cast<const uint2*>(dO + off);
-    const float2 o0 = unpack_bf16x2(uo.x), o1 = unpack_bf16x2(uo.y);
-    const float2 d0 = unpack_f16x2(ud.x), d1 = unpack_f16x2(ud.y);
-    acc = o0.x * d0.x + o0.y * d0.y + o1.x * d1.x + o1.y * d1.y;
+  const int half = lane >> 4, col = (lane & 15) * 8;
+  uint4 uo[PRE_ROWS / 2], ud[PRE_ROWS / 2];
+#pragma unroll
+  for (int i = 0; i < PRE_ROWS / 2; ++i) {
+    const int pos = pos0 + 2 * i + half;
+    if (pos < s) {
+      const int64_t off = ((bb * s + pos) * nq + head) * HD + col;
+      uo[i] = __ldg(reinterpret_cast<const uint4*>(O + off));
+      ud[i] = __ldg(reinterpret_cast<const uint4*>(dO + off));
+    } else {
+      uo[i] = make_uint4(0u, 0u, 0u, 0u);
+      ud[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
-    Dp[w] = acc;
-    L2p[w] = pos < s ? LSE[bh * s + pos] * LOG2E_F : __int_as_float(0x7f800000);
+  for (int i = 0; i < PRE_ROWS / 2; ++i) {
+    const uint32_t ow[4] = {uo[i].x, uo[i].y, uo[i].z, uo[i].w};
+    const uint32_t dw[4] = {ud[i].x, ud[i].y, ud[i].z, ud[i].w};
+    float acc = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 o = unpack_bf16x2(ow[q]);
+      const float2 d = unpack_f16x2(dw[q]);
+      acc += o.x * d.x + o.y * d.y;
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    const int pos = pos0 + 2 * i + half;
+    if ((lane & 15) == 0) {
+      Dp[bh * s_pad + pos] = acc;
+      L2p[bh * s_pad + pos] =
+          pos < s ? LSE[bh * s + pos] * LOG2E_F : __int_as_float(0x7f800000);
+    }
   }
 }
 
@@ -800,7 +825,7 @@ int flash_bwd(const AttnShape& sh, const void* Q, const void* K, const void* V,
   const double ds_bytes_all =
       (double)ds_pair_bytes(sh) * (double)(sh.b * sh.nkv);
   {
-    const int64_t warps = sh.b * sh.nq * s_pad;
+    const int64_t warps = sh.b * sh.nq * (s_pad / PRE_ROWS);
     ProfScope ps(stream, KF_ELEMENTWISE, 2.0 * sh.b * sh.s * sh.nq * HD,
                  2.0 * io * sh.nq);
     attn_bwd_prepass_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0,
