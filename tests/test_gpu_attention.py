@@ -136,14 +136,15 @@ def test_group_size_extremes(tp, n_q, n_kv, n):
     run_case(tp, cfg, 0, 38)
 
 
-@pytest.mark.parametrize("s", [384, 500])
+@pytest.mark.parametrize("b,s", [(1, 384), (2, 500)])
 @pytest.mark.parametrize("causal", [True, False])
-def test_odd_group_size(tp, s, causal):
+def test_odd_group_size(tp, b, s, causal):
     # three q heads per kv head on each rank: the forward then puts two
     # consecutive query blocks of one head in a CTA instead of two heads of
     # a group; s = 384 leaves the last CTA's second block past the end
-    # (three blocks), s = 500 fills both with a ragged tail (four blocks)
-    cfg = I.workload("attn_gqa_bf16", b=1, s=s, h=1024, n_q=12, n_kv=4, n=2,
+    # (three blocks), s = 500 fills both with a ragged tail (four blocks),
+    # over two sequences
+    cfg = I.workload("attn_gqa_bf16", b=b, s=s, h=1024, n_q=12, n_kv=4, n=2,
                      causal=causal, w_std="fan_in")
     run_case(tp, cfg, 0, 41)
 
