@@ -196,12 +196,13 @@ __global__ void __maxnreg__(168)
       const int ntiles = T.nkb[1] > 0 ? 2 : 1;
       mbar_arrive_expect_tx(q_full, ntiles * TILE);
 #pragma unroll
-      for (int t = 0; t < NT; ++t)
-        if (t < ntiles)
+      for (int t = 0; t < NT; ++t) {
+        if (t >= ntiles) continue;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
+        for (int hh = 0; hh < 2; ++hh)
           tma_load_3d(sm + OFF_Q + t * TILE + hh * ATOM, &a.mq, q_full,
                       T.head[t] * HD + hh * 64, T.q0[t], T.b);
+      }
       uint32_t armed = 0, armed_par = 0;
       int e = 0;
       auto put = [&](const CUtensorMap* map, int jb) -> bool {
