@@ -2,11 +2,12 @@
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from megatron_tensor_transformer_gate_gb300 import inputs as I
 from megatron_tensor_transformer_gate_gb300.blocks import TPAttention
-from _parity import check
+from _parity import check, check_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -181,3 +182,72 @@ def test_single_token_sequences(tp, causal):
     for k in ("dWq", "dWk"):
         err = np.linalg.norm(g[k].double().cpu().numpy() - go[k])
         assert err <= 1e-2 * scale, (k, err / scale)
+
+
+def _rescaled_rows(f, cfg):
+    """Rows whose running reference max the forward kernel moves: the first
+    key block's row max is the reference, and a later block's row max above
+    it by more than 2^8 in exp2 units (8 / (scale·log2 e) in raw scores)
+    replaces it."""
+    b, s, d = cfg["b"], cfg["s"], cfg["d"]
+    nq, nkv = cfg["n_q"], cfg["n_kv"]
+    thr = 8.0 / ((1.0 / np.sqrt(d)) * np.log2(np.e))
+    X = f["X"].reshape(b, s, -1)
+    count = 0
+    for bi in range(b):
+        for j in range(nq):
+            q = X[bi] @ f["Wq"][j * d:(j + 1) * d].T
+            kv = j // (nq // nkv)
+            k = X[bi] @ f["Wk"][kv * d:(kv + 1) * d].T
+            S = q @ k.T
+            if cfg.get("causal", True):
+                S = np.where(np.tril(np.ones((s, s), dtype=bool)), S, -np.inf)
+            for r in range(s):
+                m_ref = None
+                for k0 in range(0, s, 128):
+                    bm = S[r, k0:k0 + 128].max()
+                    if bm == -np.inf:
+                        break
+                    if m_ref is None:
+                        m_ref = bm
+                    elif bm > m_ref + thr:
+                        m_ref = bm
+                        count += 1
+                        break
+    return count
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_growing_scores_rescale_the_output(tp, causal):
+    # inputs whose rows grow along the sequence, so that a query's scores
+    # against later key blocks exceed the first block's maximum by far more
+    # than the kernel's rescale threshold: the accumulated output and row
+    # sum are rescaled, possibly several times per row.  The output is held
+    # to both bounds.  Such rows' softmax is nearly one-hot, where
+    # dS = P·(dP − D) cancels exactly in the oracle but leaves rounding
+    # noise in the kernels (D from the stored bf16 O), so the gradients are
+    # held to the Frobenius bound
+    b, s, h, nq, nkv, d, n = 1, 512, 512, 8, 2, 128, 2
+    cfg = I.workload("attn_gqa_bf16", b=b, s=s, h=h, n_q=nq, n_kv=nkv, n=n,
+                     causal=causal, w_std="fan_in")
+    x = I.attn_inputs(cfg, 42, "cpu")
+    grow = 1.0 + np.arange(s) / 128.0
+    x["X"] = (x["X"].float() *
+              torch.from_numpy(np.tile(grow, b)).float()[:, None]).to(
+                  x["X"].dtype)
+    f = {k: I.to_f64(v) for k, v in x.items()}
+    assert _rescaled_rows(f, cfg) > s * nq // 4   # the path is exercised
+    dv = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    a = TPAttention(b, s, h, nq, nkv, d, n, causal=causal)
+    out = a.forward(dv["X"], dv["Wq"], dv["Wk"], dv["Wv"], dv["Wo"])
+    g = a.backward(dv["dOut"], dv["X"], dv["Wq"], dv["Wk"], dv["Wv"],
+                   dv["Wo"])
+    tp.device_status()
+    kw = dict(b=b, s=s, n_q=nq, n_kv=nkv, d=d, causal=causal)
+    fo = oracle.attention_forward(f["X"], f["Wq"], f["Wk"], f["Wv"], f["Wo"],
+                                  **kw)
+    go = oracle.attention_backward(f["dOut"], f["X"], f["Wq"], f["Wk"],
+                                   f["Wv"], f["Wo"], fo, **kw)
+    check(out, fo["Out"], "Out")
+    for k in ("dX", "dWq", "dWk", "dWv", "dWo"):
+        check_fro(g[k], go[k], k)
