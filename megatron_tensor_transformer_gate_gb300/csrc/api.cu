@@ -1496,7 +1496,7 @@ extern "C" tp_status tp_layer_bwd(const tp_layer_desc* d, const void* dout,
       if (st != TP_OK) return st;
       int err = rmsnorm_bwd_sum<__nv_bfloat16>(
           partials, d->n, T * h, F.x1, g2, F.rstd2, dout, L.dx1, dg2,
-          static_cast<float*>(L.norm), T, h, stream);
+          static_cast<float*>(L.norm), T, h, stream, device_status_ptr());
       if (err) return cuda_status(err);
       st = attn_bwd_impl(&ad, L.dx1, F.xn1, Wq, Wk, Wv, Wo, F.attn_ws,
                          nullptr, L.dxn, dWq, dWk, dWv, dWo, nullptr, L.blk,
@@ -1504,7 +1504,7 @@ extern "C" tp_status tp_layer_bwd(const tp_layer_desc* d, const void* dout,
       if (st != TP_OK) return st;
       err = rmsnorm_bwd_sum<__nv_bfloat16>(
           partials, d->n, T * h, x, g1, F.rstd1, L.dx1, dx, dg1,
-          static_cast<float*>(L.norm), T, h, stream);
+          static_cast<float*>(L.norm), T, h, stream, device_status_ptr());
       return cuda_status(err);
     }
     // MLP block: d(xn2) into dxn, then RMSNorm₂ with the residual's dout

@@ -455,6 +455,170 @@ __global__ void __launch_bounds__(512, 1)
                         dgacc + j * V);
 }
 
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src,
+                                         uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// rmsnorm_bwd_kernel<T, NV, true> for rows whose n shard partials fit in
+// shared memory: one thread copies the n partial rows of the next row into
+// shared memory by bulk copies (the bytes in flight are the copy engine's,
+// not registers) while the block finishes the current row.  Per row, as
+// there: dy = Σ_{i<n} P_i in fp32 in shard order, rounded once to T, then the
+// RMSNorm backward.  Waits are bounded (site 33); the block agrees on every
+// outcome before it leaves the loop.
+template <typename T, int NV>
+__global__ void __launch_bounds__(512, 1)
+    rmsnorm_bwd_bulk_kernel(const T* __restrict__ P, int n, int64_t zstride,
+                            const T* __restrict__ x,
+                            const T* __restrict__ gamma,
+                            const float* __restrict__ rstd,
+                            const T* __restrict__ dres, T* __restrict__ dx,
+                            float* __restrict__ dg_partial, int64_t rows,
+                            int64_t h, int64_t rpc, unsigned* status) {
+  constexpr int V = Vec<T>::N;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  T* buf = reinterpret_cast<T*>(smem_raw);   // n partial rows of h
+  uint64_t* full =
+      reinterpret_cast<uint64_t*>(smem_raw + (size_t)n * h * sizeof(T));
+  __shared__ float red[2][16];
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int64_t col[NV];
+  bool on[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    col[j] = ((int64_t)threadIdx.x + 512 * j) * V;
+    on[j] = col[j] < h;
+  }
+  float dgacc[NV * V];
+#pragma unroll
+  for (int q = 0; q < NV * V; ++q) dgacc[q] = 0.0f;
+  const int64_t r_begin = (int64_t)blockIdx.x * rpc;
+  const int64_t r_end = min(rows, r_begin + rpc);
+  const uint32_t row_bytes = (uint32_t)(h * (int64_t)sizeof(T));
+  if (threadIdx.x == 0) {
+    mbar_init(full, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // thread 0: the n partial rows of row r into buf
+  auto issue = [&](int64_t r) {
+    mbar_arrive_expect_tx(full, (uint32_t)n * row_bytes);
+    for (int i = 0; i < n; ++i)
+      bulk_g2s(buf + (int64_t)i * h, P + (int64_t)i * zstride + r * h,
+               row_bytes, full);
+  };
+  if (threadIdx.x == 0 && r_begin < r_end) issue(r_begin);
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const bool has_res = dres != nullptr;
+  uint4 cx[NV], cr[NV];   // current row of x and dres, raw 16-byte vectors
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const bool ld = on[j] && r_begin < r_end;
+    cx[j] = ld ? *reinterpret_cast<const uint4*>(x + r_begin * h + col[j])
+               : zero;
+    cr[j] = (has_res && ld)
+                ? *reinterpret_cast<const uint4*>(dres + r_begin * h + col[j])
+                : zero;
+  }
+  int64_t r = r_begin;
+  for (; r < r_end; ++r) {
+    uint4 nx[NV], nr[NV];
+    const bool more = r + 1 < r_end;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      nx[j] = (more && on[j])
+                  ? *reinterpret_cast<const uint4*>(x + (r + 1) * h + col[j])
+                  : zero;
+      nr[j] = (has_res && more && on[j])
+                  ? *reinterpret_cast<const uint4*>(dres + (r + 1) * h +
+                                                    col[j])
+                  : zero;
+    }
+    const bool got =
+        mbar_wait(full, (uint32_t)((r - r_begin) & 1),
+                  reinterpret_cast<volatile int*>(&abort_flag), status, 33);
+    if (!__syncthreads_and(got)) break;
+    float d[NV * V], xv[NV * V], g[NV * V];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      float acc[V];
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] = 0.0f;
+      if (on[j]) {
+        for (int i = 0; i < n; ++i) {
+          float v[V];
+          Vec<T>::load(buf + (int64_t)i * h + col[j], v);
+#pragma unroll
+          for (int q = 0; q < V; ++q) acc[q] += v[q];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < V; ++q) d[j * V + q] = round_to<T>(acc[q]);
+    }
+    __syncthreads();   // the partial rows are consumed
+    if (threadIdx.x == 0 && more) issue(r + 1);
+    const float rs = rstd[r];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      if (on[j]) {
+        Vec<T>::load(gamma + col[j], g + j * V);
+      } else {
+#pragma unroll
+        for (int q = 0; q < V; ++q) g[j * V + q] = 0.0f;
+      }
+      Vec<T>::from_raw(cx[j], xv + j * V);
+    }
+    float dot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV * V; ++i) {
+      dot = fmaf(d[i] * g[i], xv[i], dot);
+      dgacc[i] = fmaf(d[i] * xv[i], rs, dgacc[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (lane == 0) red[r & 1][w] = dot;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) tot += red[r & 1][i];
+    const float coef = rs * rs * rs * tot / (float)h;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      if (!on[j]) continue;
+      float o[V];
+      Vec<T>::from_raw(cr[j], o);
+#pragma unroll
+      for (int q = 0; q < V; ++q)
+        o[q] += rs * d[j * V + q] * g[j * V + q] - xv[j * V + q] * coef;
+      Vec<T>::store(dx + r * h + col[j], o);
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      cx[j] = nx[j];
+      cr[j] = nr[j];
+    }
+  }
+  if (r < r_end && threadIdx.x == 0) {
+    // gave up: let the copies of row r land before the block exits
+    volatile int no_abort = 0;
+    mbar_wait(full, (uint32_t)((r - r_begin) & 1), &no_abort, nullptr, 0);
+  }
+#pragma unroll
+  for (int j = 0; j < NV; ++j)
+    if (on[j])
+      Vec<T>::store_f32(dg_partial + (int64_t)blockIdx.x * h + col[j],
+                        dgacc + j * V);
+}
+
 // The g reduction with the next block's RMSNorm fused in (Megatron-SP
 // forward, [Troverld] §III.III: the reduce-scatter leaves each rank its rows
 // of the block output, the token-wise ops of the next block run on them, and
@@ -688,11 +852,30 @@ size_t rmsnorm_bwd_scratch(int64_t rows, int64_t h) {
 
 // The RMSNorm backward; with n > 1 dy is the sum of n partials (zstride
 // elements apart) formed in the kernel.
+// The bulk-copy form of the summed backward (n partial rows in shared
+// memory) up to this many bytes of partials per row.
+constexpr int64_t kBulkRowBytes = 200 * 1024;
+
+template <typename T, int NV>
+int launch_rmsnorm_bwd_bulk(int chunks, size_t smem, cudaStream_t s,
+                            const T* P, int n, int64_t zstride, const T* x,
+                            const T* gamma, const float* rstd, const T* dres,
+                            T* dx, float* scratch, int64_t rows, int64_t h,
+                            int64_t rpc, unsigned* status) {
+  static cudaError_t attr = cudaFuncSetAttribute(
+      rmsnorm_bwd_bulk_kernel<T, NV>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kBulkRowBytes + 64));
+  if (attr != cudaSuccess) return attr;
+  rmsnorm_bwd_bulk_kernel<T, NV><<<chunks, 512, smem, s>>>(
+      P, n, zstride, x, gamma, rstd, dres, dx, scratch, rows, h, rpc, status);
+  return cudaSuccess;
+}
+
 template <typename T>
 int rmsnorm_bwd_sum(const void* dy, int n, int64_t zstride, const void* x,
                     const void* gamma, const float* rstd, const void* dres,
                     void* dx, void* dgamma, float* scratch, int64_t rows,
-                    int64_t h, void* stream) {
+                    int64_t h, void* stream, unsigned* status) {
   if (rows == 0) return cudaSuccess;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // at most one chunk per SM (the scratch holds rmsnorm_bwd_chunks rows)
@@ -714,7 +897,24 @@ int rmsnorm_bwd_sum(const void* dy, int n, int64_t zstride, const void* x,
 #define TP_BWD(NVV, SUMV)                                                     \
   rmsnorm_bwd_kernel<T, NVV, SUMV><<<chunks, 512, 0, s>>>(                    \
       dyp, n, zstride, xp, gp, rstd, rp, dxp, scratch, rows, h, rpc)
-  if (n == 1) {
+  const int64_t part_bytes = (int64_t)n * h * (int64_t)sizeof(T);
+  if (n > 1 && part_bytes <= kBulkRowBytes) {
+    const size_t smem = (size_t)part_bytes + 16;
+    int err;
+    if (sweeps <= 1)
+      err = launch_rmsnorm_bwd_bulk<T, 1>(chunks, smem, s, dyp, n, zstride, xp,
+                                          gp, rstd, rp, dxp, scratch, rows, h,
+                                          rpc, status);
+    else if (sweeps <= 2)
+      err = launch_rmsnorm_bwd_bulk<T, 2>(chunks, smem, s, dyp, n, zstride, xp,
+                                          gp, rstd, rp, dxp, scratch, rows, h,
+                                          rpc, status);
+    else
+      err = launch_rmsnorm_bwd_bulk<T, 4>(chunks, smem, s, dyp, n, zstride, xp,
+                                          gp, rstd, rp, dxp, scratch, rows, h,
+                                          rpc, status);
+    if (err) return err;
+  } else if (n == 1) {
     if (sweeps <= 1) TP_BWD(1, false);
     else if (sweeps <= 2) TP_BWD(2, false);
     else TP_BWD(4, false);
@@ -735,7 +935,7 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
                 const float* rstd, const void* dres, void* dx, void* dgamma,
                 float* scratch, int64_t rows, int64_t h, void* stream) {
   return rmsnorm_bwd_sum<T>(dy, 1, 0, x, gamma, rstd, dres, dx, dgamma,
-                            scratch, rows, h, stream);
+                            scratch, rows, h, stream, nullptr);
 }
 
 template <typename T>
@@ -768,7 +968,7 @@ int reduce_norm_fwd(const void* P, int n, int64_t zstride, const void* bias,
   template int rmsnorm_bwd_sum<T>(const void*, int, int64_t, const void*,     \
                                   const void*, const float*, const void*,     \
                                   void*, void*, float*, int64_t, int64_t,     \
-                                  void*);                                     \
+                                  void*, unsigned*);                          \
   template int reduce_norm_fwd<T>(const void*, int, int64_t, const void*,     \
                                   const void*, void*, const DropoutSpec&,     \
                                   const void*, void*, void*, float*, int64_t, \

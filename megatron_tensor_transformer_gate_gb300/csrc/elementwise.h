@@ -53,11 +53,13 @@ int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
 // reduce_norm_fwd writes out = resid + Dropout(Σ P_i + bias) and the RMSNorm
 // of those stored rows (y, optional fp16 copy y16, rstd) in one pass.  Both
 // give the same bits as the separate kernels.
+// (status: the device status word a bounded wait of the n > 1 form records
+// a time-out in.)
 template <typename T>
 int rmsnorm_bwd_sum(const void* dy, int n, int64_t zstride, const void* x,
                     const void* gamma, const float* rstd, const void* dres,
                     void* dx, void* dgamma, float* scratch, int64_t rows,
-                    int64_t h, void* stream);
+                    int64_t h, void* stream, unsigned* status = nullptr);
 template <typename T>
 int reduce_norm_fwd(const void* P, int n, int64_t zstride, const void* bias,
                     const void* resid, void* out, const DropoutSpec& d,
