@@ -10,20 +10,26 @@
 //   warp 0     TMA: both Q tiles once, then K_0, K_1, V_0, K_2, V_1, … (the
 //              order the MMAs use them) through one 3-slot ring (fp16,
 //              128-byte swizzle, two 64-column halves per tile).
-//   warp 1     allocates 512 TMEM columns (S and O of each tile) and issues,
-//              per key block j and tile t,
-//                S_t = Q_t·K_jᵀ     (M=128, N=128, K=128) into TMEM S[t]
-//                O_t += P_t·V_j     (M=128, N=128, K=128) into TMEM O[t],
-//                                   P_t read from shared memory
+//   warp 1     allocates 512 TMEM columns (S of each tile, O of both) and
+//              issues, per key block j,
+//                S_t = Q_t·K_jᵀ     (M=128, N=128, K=128) into TMEM S[t],
+//                                   for each tile t
+//                Oᵀ += Vᵀ_j·Pᵀ      (M=128 features, N=256 queries of both
+//                                   tiles, K=128 keys) into TMEM Oᵀ, P of
+//                                   both tiles read from shared memory
 //              S_t for block j+1 as soon as tile t's softmax has copied S_t
 //              of block j to registers, so the scores of the next block are
-//              computed while the softmax of this one runs, and the other
-//              tile's MMAs fill the tensor pipe meanwhile.
+//              computed while the softmax of this one runs.  The output is
+//              accumulated transposed so that one N=256 instruction serves
+//              both tiles: on this tensor core an M=128 instruction costs
+//              nearly as much at N=128 as at N=256.
 //   warps 2–9  softmax, one thread per query row (warps 2–5 tile 0, 6–9
 //              tile 1): reference max m and sum l in fp32, P = exp2(S·scale·
-//              log2e − m) stored as fp16 into the tile's P buffer.  O
-//              accumulates in TMEM; when a block's max exceeds m by more than
-//              2^8 the softmax rescales O and l by exp2(m − m_new) first.  The
+//              log2e − m) stored as fp16 into the P buffer.  Oᵀ accumulates
+//              in TMEM; when a block's max exceeds m by more than 2^12 the row
+//              takes a new m, and its column of Oᵀ and l are scaled by
+//              exp2(m − m_new) first (each thread holds one feature lane of
+//              every column, so the factors pass through shared memory).  The
 //              epilogue writes O / l (bf16) and LSE = (m + log2 l)·ln 2.
 // Operands are fp16 and accumulation fp32: the softmax amplifies score
 // errors, and bf16 operands (8-bit mantissa) put the row-wise error of causal
@@ -51,19 +57,26 @@ constexpr int NT = 2;                    // query tiles per CTA
 constexpr int NSLOT = 3;                 // K/V ring slots
 constexpr int THREADS = 64 + NT * 128;   // TMA warp, MMA warp, softmax rows
 constexpr int OFF_Q = 0;                 // NT tiles
-constexpr int OFF_P = OFF_Q + NT * TILE; // NT tiles (A operand of O += P·V)
+// P of both tiles as one 256-row K-major operand: half hh (keys 64·hh to
+// 64·hh + 63) of tile t's row r at OFF_P + hh·2·ATOM + (128·t + r)·128.
+constexpr int OFF_P = OFF_Q + NT * TILE;
 constexpr int OFF_KV = OFF_P + NT * TILE;
 constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
-constexpr int SMEM = OFF_BAR + 256 + 1024;   // + slack for 1024-B alignment
+constexpr int OFF_COLF = OFF_BAR + 256;      // per-query factors, NT × 128 fp32
+constexpr int SMEM = OFF_COLF + NT * BLK * 4 + 1024;   // + 1024-B alignment
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM: S of tile t in columns [128·t, 128·t + 128), O of tile t in
+// TMEM: S of tile t in columns [128·t, 128·t + 128); the output transposed,
+// Oᵀ (lane = feature d, column = query), tile t's queries in columns
 // [256 + 128·t, 384 + 128·t).
 constexpr uint32_t COL_O = 256;
 // The output accumulates in TMEM against a reference max m; it is rescaled
 // only when a block's row max exceeds m by more than this (log2 units), which
-// keeps the fp16 probabilities ≤ 2^8 and the fp32 accumulator far from
-// overflow.
-constexpr float RESCALE_LOG2 = 8.0f;
+// keeps the fp16 probabilities ≤ 2^12 (a factor 16 below the fp16 maximum)
+// and the fp32 accumulator far from overflow.  A rescale makes the four warps
+// of a tile wait for one another, and with scores of a few units of spread a
+// 2^8 threshold let some row of a 128-row tile cross it in about a third of
+// the key blocks, 2^12 in under 2 %.
+constexpr float RESCALE_LOG2 = 12.0f;
 
 struct FwdTcArgs {
   CUtensorMap mq, mk, mv;
@@ -118,8 +131,13 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk) {
   return smem_desc_sw128(base + (kk >> 2) * ATOM + (kk & 3) * 32, 16, 1024);
 }
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
-  // MN-major B (V: rows = keys = K, two 64-wide d halves ATOM apart)
+  // MN-major Vᵀ as A (rows = keys = K, M = d in two 64-wide halves ATOM apart)
   return smem_desc_sw128(base + kk * 2048, ATOM, 1024);
+}
+__device__ __forceinline__ uint64_t desc_p(uint32_t base, int kk) {
+  // K-major P (rows = queries = N; its two key halves 2·ATOM apart)
+  return smem_desc_sw128(base + (kk >> 2) * 2 * ATOM + (kk & 3) * 32, 16,
+                         1024);
 }
 
 // Row r of a 128-row K-major swizzled half tile (128-byte rows): its eight
@@ -153,10 +171,17 @@ __global__ void __maxnreg__(168)
   uint64_t* s_full = bar + 7;     // [NT] S_t written
   uint64_t* s_free = bar + 9;     // [NT] S_t copied to registers
   uint64_t* p_full = bar + 11;    // [NT] P_t written (and O_t rescaled)
-  uint64_t* pv_done = bar + 13;   // [NT] O_t += P_t·V done (P_t free)
+  uint64_t* pv_done = bar + 13;   // [NT] Oᵀ += Vᵀ·P_tᵀ done (P_t free)
   uint64_t* drain = bar + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* f_full = bar + 17;    // [NT] tile t's rescale flags written
+  uint64_t* g_full = bar + 19;    // [NT] tile t's per-query factors written
+  // [NT][2][4]: per tile and key-block parity, the last block at which a row
+  // of warp quarter q took a new reference max (only ever increases, so it
+  // needs no reset)
+  volatile int* rescale_at = reinterpret_cast<volatile int*>(bar + 21);
+  float* colf = reinterpret_cast<float*>(sm + OFF_COLF);   // [NT][BLK]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Tiles T = cta_tiles(a);
@@ -173,6 +198,9 @@ __global__ void __maxnreg__(168)
       mbar_init(&s_free[t], 128);
       mbar_init(&p_full[t], 128);
       mbar_init(&pv_done[t], 1);
+      mbar_init(&f_full[t], 128);
+      mbar_init(&g_full[t], 128);
+      for (int q = 0; q < 8; ++q) rescale_at[t * 8 + q] = 0;
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -237,7 +265,10 @@ __global__ void __maxnreg__(168)
     if (lane == 0) {
       // ------------------------------------------------------------- MMA --
       constexpr uint32_t IDESC_S = idesc_f16_f32(128, 128, 0, 0);
-      constexpr uint32_t IDESC_O = idesc_f16_f32(128, 128, 0, 1);
+      // Oᵀ += Vᵀ·Pᵀ: A = V read MN-major, B = P K-major; N = 256 covers
+      // both tiles' queries in one instruction, N = 128 one tile
+      constexpr uint32_t IDESC_O2 = idesc_f16_f32(128, 256, 1, 0);
+      constexpr uint32_t IDESC_O1 = idesc_f16_f32(128, 128, 1, 0);
       bool ok = mbar_wait(q_full, 0, abort_flag, a.status, 12);
       int e = 0;
       uint32_t sKV = 0;
@@ -283,23 +314,28 @@ __global__ void __maxnreg__(168)
           give();
         }
         if (!(ok = take())) break;
+        // Oᵀ += Vᵀ_jb·Pᵀ over the tiles still reading keys at block jb; the
+        // softmax rescaled Oᵀ (if needed) before signalling P_t
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           if (!ok || jb >= T.nkb[t]) continue;
-          // O_t += P_t·V_jb; the softmax rescaled O_t (if needed) before
-          // signalling P_t
-          if (!(ok = mbar_wait(&p_full[t], jb & 1, abort_flag, a.status, 15)))
-            break;
-          tc_fence_after();
-          const uint32_t sP = smem_u32(sm + OFF_P + t * TILE);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tc_mma_f16(tmem + COL_O + t * 128, desc_kmajor(sP, kk),
-                       desc_mnmajor(sKV, kk), IDESC_O,
-                       (jb > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&pv_done[t]);
+          ok = mbar_wait(&p_full[t], jb & 1, abort_flag, a.status, 15);
         }
         if (!ok) break;
+        tc_fence_after();
+        {
+          const bool both = jb < T.nkb[0] && jb < T.nkb[1];
+          const int t0 = jb < T.nkb[0] ? 0 : 1;
+          const uint32_t sP = smem_u32(sm + OFF_P + t0 * ATOM);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_f16(tmem + COL_O + t0 * 128, desc_mnmajor(sKV, kk),
+                       desc_p(sP, kk), both ? IDESC_O2 : IDESC_O1,
+                       (jb > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            if (jb < T.nkb[t]) tc_commit(&pv_done[t]);
+        }
         give();
       }
       if (*abort_flag) {
@@ -322,10 +358,13 @@ __global__ void __maxnreg__(168)
         tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t s_col = lane_base + t * 128;
     const uint32_t o_col = lane_base + COL_O + t * 128;
-    uint8_t* ptile = sm + OFF_P + t * TILE;
+    uint8_t* ptile = sm + OFF_P + t * ATOM;
+    float* tcolf = colf + t * BLK;
     const float c = a.scale_log2;
     const float thr = RESCALE_LOG2 / c;   // the rescale threshold in raw units
     float m_ref = -INFINITY, l_run = 0.0f;
+    int n_g = 0;   // completed phases of g_full[t]
+    bool read_f = false;   // the last block's factors may still be read
     bool ok = true;
     for (int jb = 0; jb < nkb; ++jb) {
       if (!mbar_wait_warp(&s_full[t], jb & 1, abort_flag, a.status, 16)) {
@@ -366,16 +405,23 @@ __global__ void __maxnreg__(168)
                              max3f(mx8[3], mx8[4], mx8[5]),
                              fmaxf(mx8[6], mx8[7]));
       // a new reference max when the block's max exceeds it by more than
-      // the threshold (warp-uniform decision, rows that keep theirs get 1)
+      // the threshold; rows that keep theirs get the factor 1
       float alpha = 1.0f;
-      bool rescale = false;
+      bool new_ref = false;
       if (jb == 0) {
         m_ref = mx;
-      } else if (__any_sync(0xffffffffu, mx > m_ref + thr)) {
-        const float m_new = mx > m_ref + thr ? mx : m_ref;
-        alpha = ex2_approx((m_ref - m_new) * c);
-        m_ref = m_new;
-        rescale = true;
+      } else if (mx > m_ref + thr) {
+        alpha = ex2_approx((m_ref - mx) * c);
+        m_ref = mx;
+        new_ref = true;
+      }
+      // query r's factor scales column r of Oᵀ, which every warp of the tile
+      // holds 32 feature lanes of; columns 32·q to 32·q + 31 are the rows of
+      // warp quarter q, which flags them here (read after the exponentials)
+      if (jb >= 1) {
+        if (__any_sync(0xffffffffu, new_ref) && lane == 0)
+          rescale_at[t * 8 + (jb & 1) * 4 + quarter] = jb;
+        mbar_arrive(&f_full[t]);
       }
       // P = exp2(c·(s − m)) in fp16 pairs: keys 0–63 in pk[0], 64–127 in pk[1]
       const float neg = -m_ref * c;
@@ -395,29 +441,59 @@ __global__ void __maxnreg__(168)
           pk[cc >> 1][(cc & 1) * 16 + (i >> 1)] = pack_f16x2(p0, p1);
         }
       }
-      // O_t += P·V of the previous block must have completed before O_t is
-      // rescaled and before the P buffer is overwritten
-      if (jb >= 1 && !mbar_wait_warp(&pv_done[t], (jb - 1) & 1, abort_flag,
-                                     a.status, 17)) {
-        ok = false;
-        break;
-      }
-      if (rescale) {
-        // the whole warp takes part (TMEM access is warp-collective)
-        tc_fence_after();
+      if (jb >= 1) {
+        // the tile's flags of this block (complete by now: every warp set
+        // them before its exponentials), read while Oᵀ += Vᵀ·Pᵀ of the
+        // previous block may still run
+        if (!mbar_wait_warp(&f_full[t], (jb - 1) & 1, abort_flag, a.status,
+                            18)) {
+          ok = false;
+          break;
+        }
+        volatile int* flags = rescale_at + t * 8 + (jb & 1) * 4;
+        const int f0 = flags[0], f1 = flags[1], f2 = flags[2], f3 = flags[3];
+        const bool any = __any_sync(
+            0xffffffffu, (f0 == jb) | (f1 == jb) | (f2 == jb) | (f3 == jb));
+        // that product must have completed before Oᵀ is rescaled, the P
+        // buffer overwritten or the factors rewritten (its start needed every
+        // row of the tile past its reads of them)
+        if (!mbar_wait_warp(&pv_done[t], (jb - 1) & 1, abort_flag, a.status,
+                            17)) {
+          ok = false;
+          break;
+        }
+        read_f = any;
+        if (any) {
+          tcolf[r] = alpha;
+          mbar_arrive(&g_full[t]);
+          if (!mbar_wait_warp(&g_full[t], n_g & 1, abort_flag, a.status, 22)) {
+            ok = false;
+            break;
+          }
+          ++n_g;
+          tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(o_col + cc * 32, o);
-          tmem_ld_wait(o);
+          for (int cc = 0; cc < 4; ++cc) {
+            const int fc = cc == 0 ? f0 : cc == 1 ? f1 : cc == 2 ? f2 : f3;
+            if (fc != jb) continue;
+            uint32_t o[32];
+            tmem_ld32(o_col + cc * 32, o);
+            tmem_ld_wait(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(o_col + cc * 32, o);
+            for (int i = 0; i < 32; i += 4) {
+              const float4 f =
+                  *reinterpret_cast<const float4*>(tcolf + cc * 32 + i);
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * f.x);
+              o[i + 1] = __float_as_uint(__uint_as_float(o[i + 1]) * f.y);
+              o[i + 2] = __float_as_uint(__uint_as_float(o[i + 2]) * f.z);
+              o[i + 3] = __float_as_uint(__uint_as_float(o[i + 3]) * f.w);
+            }
+            tmem_st32(o_col + cc * 32, o);
+          }
         }
       }
       st_row(ptile, r, pk[0]);
-      st_row(ptile + ATOM, r, pk[1]);
+      st_row(ptile + 2 * ATOM, r, pk[1]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[t]);
@@ -425,39 +501,73 @@ __global__ void __maxnreg__(168)
               (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
                ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
     }
-    // epilogue: wait for the last O_t += P·V, then O / l and the LSE
+    // epilogue: wait for the last Oᵀ += Vᵀ·Pᵀ, then O / l and the LSE.  Each
+    // thread holds feature r of every query of the tile; with query q's 1 / l
+    // from shared memory it writes O[q][r] (bf16) into the tile's P rows,
+    // free now, as two 64-feature halves of 128-byte rows (a warp's 32
+    // features of one query are 64 contiguous bytes, no bank conflict).
+    // Then each warp stores 32 whole rows of 256 bytes to the output.
+    // Unless the last block rescaled, nothing reads the factors any more and
+    // the 1 / l exchange runs while the last product completes.
     const int last = nkb - 1;
-    if (nkb > 0 && __all_sync(0xffffffffu, ok) &&
-        mbar_wait_warp(&pv_done[t], last & 1, abort_flag, a.status, 19)) {
-      tc_fence_after();
-      const float inv = 1.0f / l_run;
-      __nv_bfloat16* dst = a.O + ((int64_t)T.b * a.s + qi) *
-                                     (int64_t)(a.nq * HD) +
-                           head * HD;
+    if (nkb > 0 && __all_sync(0xffffffffu, ok)) {
+      bool fine = true;
+      if (read_f)
+        fine = mbar_wait_warp(&pv_done[t], last & 1, abort_flag, a.status, 19);
+      if (fine) {
+        tcolf[r] = 1.0f / l_run;
+        mbar_arrive(&f_full[t]);
+        if (!read_f)
+          fine = mbar_wait_warp(&pv_done[t], last & 1, abort_flag, a.status,
+                                19);
+      }
+      fine = fine &&
+             mbar_wait_warp(&f_full[t], last & 1, abort_flag, a.status, 20);
+      if (fine) {
+        tc_fence_after();
+        __nv_bfloat16* ohalf = reinterpret_cast<__nv_bfloat16*>(
+            ptile + (r >> 6) * 2 * ATOM + (r & 63) * 2);
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(o_col + cc * 32, o);
-        tmem_ld_wait(o);
-        if (qi < a.s) {
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(o_col + cc * 32, o);
+          tmem_ld_wait(o);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv,
-                              __uint_as_float(o[8 * q + 1]) * inv);
-            u.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv,
-                              __uint_as_float(o[8 * q + 3]) * inv);
-            u.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv,
-                              __uint_as_float(o[8 * q + 5]) * inv);
-            u.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv,
-                              __uint_as_float(o[8 * q + 7]) * inv);
-            reinterpret_cast<uint4*>(dst)[cc * 4 + q] = u;
+          for (int i = 0; i < 32; i += 4) {
+            const float4 f =
+                *reinterpret_cast<const float4*>(tcolf + cc * 32 + i);
+            ohalf[(cc * 32 + i) * 64] =
+                __float2bfloat16_rn(__uint_as_float(o[i]) * f.x);
+            ohalf[(cc * 32 + i + 1) * 64] =
+                __float2bfloat16_rn(__uint_as_float(o[i + 1]) * f.y);
+            ohalf[(cc * 32 + i + 2) * 64] =
+                __float2bfloat16_rn(__uint_as_float(o[i + 2]) * f.z);
+            ohalf[(cc * 32 + i + 3) * 64] =
+                __float2bfloat16_rn(__uint_as_float(o[i + 3]) * f.w);
           }
         }
+        mbar_arrive(&f_full[t]);
+        fine = mbar_wait_warp(&f_full[t], (last + 1) & 1, abort_flag, a.status,
+                              21);
       }
-      if (qi < a.s)
-        a.LSE[((int64_t)T.b * a.nq + head) * a.s + qi] =
-            (m_ref * c + log2f(l_run)) * 0.69314718055994531f;
+      if (fine) {
+        // lanes 0–15 one row, 16–31 the next: 16 chunks of 16 bytes each
+        const int ld = a.nq * HD;
+        const int chunk = lane & 15;
+        const uint8_t* src =
+            ptile + (chunk >> 3) * 2 * ATOM + (chunk & 7) * 16;
+#pragma unroll 1
+        for (int k = 0; k < 16; ++k) {
+          const int q = quarter * 32 + 2 * k + (lane >> 4);
+          const uint4 u = *reinterpret_cast<const uint4*>(src + q * 128);
+          if (q0 + q < a.s)
+            reinterpret_cast<uint4*>(a.O + ((int64_t)T.b * a.s + q0 + q) * ld +
+                                     head * HD)[chunk] = u;
+        }
+        if (qi < a.s)
+          a.LSE[((int64_t)T.b * a.nq + head) * a.s + qi] =
+              (m_ref * c + log2f(l_run)) * 0.69314718055994531f;
+      }
     }
   }
 
