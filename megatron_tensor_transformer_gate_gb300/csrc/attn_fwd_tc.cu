@@ -151,6 +151,39 @@ __device__ __forceinline__ void st_row(uint8_t* half_tile, int r,
         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
+// 16 TMEM lanes × 64 columns (eight 8-column units) into 32 registers: in
+// unit u a thread holds lanes base + lane/4 (r[4u], r[4u+1]) and base + 8 +
+// lane/4 (r[4u+2], r[4u+3]), columns 8u + 2·(lane % 4) and the next one.
+__device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr,
+                                                  uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+// Four 8×8 b16 matrices stored transposed: register j of a lane holds
+// elements (lane/4, 2·(lane % 4)) and (lane/4, 2·(lane % 4) + 1) of matrix j;
+// lane 8j + i gives the address of stored row i of matrix j, which receives
+// column i (16 bytes).
+__device__ __forceinline__ void stmatrix_x4_trans(const void* row, uint32_t a0,
+                                                  uint32_t a1, uint32_t a2,
+                                                  uint32_t a3) {
+  asm volatile(
+      "stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};"
+      ::"r"(smem_u32(row)), "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+      : "memory");
+}
+
 __device__ __forceinline__ float max3f(float x, float y, float z) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
@@ -501,14 +534,13 @@ __global__ void __maxnreg__(168)
               (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
                ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
     }
-    // epilogue: wait for the last Oᵀ += Vᵀ·Pᵀ, then O / l and the LSE.  Each
-    // thread holds feature r of every query of the tile; with query q's 1 / l
-    // from shared memory it writes O[q][r] (bf16) into the tile's P rows,
-    // free now, as two 64-feature halves of 128-byte rows (a warp's 32
-    // features of one query are 64 contiguous bytes, no bank conflict).
-    // Then each warp stores 32 whole rows of 256 bytes to the output.
-    // Unless the last block rescaled, nothing reads the factors any more and
-    // the 1 / l exchange runs while the last product completes.
+    // epilogue: wait for the last Oᵀ += Vᵀ·Pᵀ, then O / l and the LSE.  The
+    // queries' 1 / l pass through shared memory (unless the last block
+    // rescaled, nothing reads the factors any more and this exchange runs
+    // while the last product completes); the scaled bf16 output goes,
+    // transposed by stmatrix, into the tile's P rows (free now) as two
+    // 64-feature halves of 128-byte rows in the 128-byte swizzle (conflict-
+    // free), and each warp then stores 32 whole rows of 256 bytes.
     const int last = nkb - 1;
     if (nkb > 0 && __all_sync(0xffffffffu, ok)) {
       bool fine = true;
@@ -524,26 +556,41 @@ __global__ void __maxnreg__(168)
       fine = fine &&
              mbar_wait_warp(&f_full[t], last & 1, abort_flag, a.status, 20);
       if (fine) {
+        // Oᵀ read in 8×8 blocks of (feature, query), scaled by the queries'
+        // 1 / l and stored transposed: 8 query rows of 8 features each.
+        // This lane addresses stored row i of matrix j: features f0 to f0 + 7
+        // of query 8·(u + j/2) + i.
         tc_fence_after();
-        __nv_bfloat16* ohalf = reinterpret_cast<__nv_bfloat16*>(
-            ptile + (r >> 6) * 2 * ATOM + (r & 63) * 2);
+        const int j = lane >> 3, i = lane & 7;
+        const int qp = 2 * (lane & 3);
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(o_col + cc * 32, o);
-          tmem_ld_wait(o);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t x[2][32];
+          const uint32_t ta = o_col + (static_cast<uint32_t>(hh * 16) << 16);
+          tmem_ld16x256b_x8(ta, x[0]);
+          tmem_ld16x256b_x8(ta + 64, x[1]);
+          tmem_ld_wait(x[0]);
+          reg_fence32(x[1]);
+          const int f0 = quarter * 32 + hh * 16 + 8 * (j & 1);
+          uint8_t* row = ptile + (f0 >> 6) * 2 * ATOM + (j >> 1) * 1024 +
+                         i * 128 + ((((f0 & 63) >> 3) ^ i) << 4);
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 f =
-                *reinterpret_cast<const float4*>(tcolf + cc * 32 + i);
-            ohalf[(cc * 32 + i) * 64] =
-                __float2bfloat16_rn(__uint_as_float(o[i]) * f.x);
-            ohalf[(cc * 32 + i + 1) * 64] =
-                __float2bfloat16_rn(__uint_as_float(o[i + 1]) * f.y);
-            ohalf[(cc * 32 + i + 2) * 64] =
-                __float2bfloat16_rn(__uint_as_float(o[i + 2]) * f.z);
-            ohalf[(cc * 32 + i + 3) * 64] =
-                __float2bfloat16_rn(__uint_as_float(o[i + 3]) * f.w);
+          for (int u = 0; u < 16; u += 2) {
+            const uint32_t* xa = &x[u >> 3][(u & 7) * 4];
+            const float2 c0 =
+                *reinterpret_cast<const float2*>(tcolf + 8 * u + qp);
+            const float2 c1 =
+                *reinterpret_cast<const float2*>(tcolf + 8 * u + 8 + qp);
+            stmatrix_x4_trans(
+                row + u * 1024,
+                pack_bf16x2(__uint_as_float(xa[0]) * c0.x,
+                            __uint_as_float(xa[1]) * c0.y),
+                pack_bf16x2(__uint_as_float(xa[2]) * c0.x,
+                            __uint_as_float(xa[3]) * c0.y),
+                pack_bf16x2(__uint_as_float(xa[4]) * c1.x,
+                            __uint_as_float(xa[5]) * c1.y),
+                pack_bf16x2(__uint_as_float(xa[6]) * c1.x,
+                            __uint_as_float(xa[7]) * c1.y));
           }
         }
         mbar_arrive(&f_full[t]);
@@ -554,12 +601,12 @@ __global__ void __maxnreg__(168)
         // lanes 0–15 one row, 16–31 the next: 16 chunks of 16 bytes each
         const int ld = a.nq * HD;
         const int chunk = lane & 15;
-        const uint8_t* src =
-            ptile + (chunk >> 3) * 2 * ATOM + (chunk & 7) * 16;
-#pragma unroll 1
+        const uint8_t* src = ptile + (chunk >> 3) * 2 * ATOM;
+#pragma unroll 4
         for (int k = 0; k < 16; ++k) {
           const int q = quarter * 32 + 2 * k + (lane >> 4);
-          const uint4 u = *reinterpret_cast<const uint4*>(src + q * 128);
+          const uint4 u = *reinterpret_cast<const uint4*>(
+              src + q * 128 + (((chunk & 7) ^ (q & 7)) << 4));
           if (q0 + q < a.s)
             reinterpret_cast<uint4*>(a.O + ((int64_t)T.b * a.s + q0 + q) * ld +
                                      head * HD)[chunk] = u;
