@@ -251,3 +251,99 @@ def test_growing_scores_rescale_the_output(tp, causal):
     check(out, fo["Out"], "Out")
     for k in ("dX", "dWq", "dWk", "dWv", "dWo"):
         check_fro(g[k], go[k], k)
+
+
+def _rescale_events(f, cfg, thr_log2=12.0):
+    """(q head, query row, key block) of every new reference max under the
+    forward kernel's rule: the first key block's row max is the reference,
+    and a later block's row max above it by more than 2^12 in exp2 units
+    replaces it."""
+    b, s, d = cfg["b"], cfg["s"], cfg["d"]
+    nq, nkv = cfg["n_q"], cfg["n_kv"]
+    thr = thr_log2 / ((1.0 / np.sqrt(d)) * np.log2(np.e))
+    X = f["X"].reshape(b, s, -1)
+    ev = set()
+    for bi in range(b):
+        for j in range(nq):
+            kv = j // (nq // nkv)
+            S = (X[bi] @ f["Wq"][j * d:(j + 1) * d].T) @ (
+                X[bi] @ f["Wk"][kv * d:(kv + 1) * d].T).T
+            if cfg.get("causal", True):
+                S = np.where(np.tril(np.ones((s, s), dtype=bool)), S, -np.inf)
+            for r in range(s):
+                m_ref = None
+                for k0 in range(0, s, 128):
+                    bm = S[r, k0:k0 + 128].max()
+                    if bm == -np.inf:
+                        break
+                    if m_ref is None:
+                        m_ref = bm
+                    elif bm > m_ref + thr:
+                        m_ref = bm
+                        ev.add((j, r, k0 // 128))
+    return ev
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_rescale_of_a_few_rows_of_one_tile(tp, causal):
+    # The forward accumulates Oᵀ (column = query), so a row's rescale is
+    # carried out on its column by all four warps of the tile, for the
+    # 32-column chunk of the warp quarter that flagged it.  Here a marker
+    # feature makes the scores of a few chosen query rows jump at one later
+    # key block (rows 296-301: quarter 1 of the third query tile, and row
+    # 400: quarter 0 of the fourth), while every other row keeps its first
+    # block's reference: a rescale applied to the wrong chunk, or skipped,
+    # shows in those rows' outputs.  Feature 0 of every q head comes only
+    # from input column 0 (set on the marked query rows) and feature 0 of
+    # every kv head only from input column 1 (set on keys 200-205 and 390),
+    # so the marked rows' scores against the marked keys gain
+    # (2·10)² / √d (log2 units: 51, far above the threshold of 12) and no
+    # other score changes.  Gradients are held to the Frobenius bound (nearly one-hot
+    # rows, as for the growing scores).
+    b, s, h, nq, nkv, d, n = 1, 512, 512, 8, 2, 128, 2
+    cfg = I.workload("attn_gqa_bf16", b=b, s=s, h=h, n_q=nq, n_kv=nkv, n=n,
+                     causal=causal, w_std="fan_in")
+    x = I.attn_inputs(cfg, 7, "cpu")
+    X = x["X"].float()
+    Wq, Wk = x["Wq"].float(), x["Wk"].float()
+    marked_q = list(range(296, 302)) + [400]
+    marked_k = list(range(200, 206)) + [390]
+    X[:, 0] = 0.0
+    X[:, 1] = 0.0
+    X[marked_q, 0] = 10.0
+    X[marked_k, 1] = 10.0
+    Wq[:, :2] = 0.0
+    Wk[:, :2] = 0.0
+    Wq[torch.arange(nq) * d, :] = 0.0
+    Wk[torch.arange(nkv) * d, :] = 0.0
+    Wq[torch.arange(nq) * d, 0] = 2.0
+    Wk[torch.arange(nkv) * d, 1] = 2.0
+    x["X"], x["Wq"], x["Wk"] = (X.to(x["X"].dtype), Wq.to(x["Wq"].dtype),
+                                Wk.to(x["Wk"].dtype))
+    f = {k: I.to_f64(v) for k, v in x.items()}
+    ev = _rescale_events(f, cfg)
+    rows = {r for (_, r, _) in ev}
+    assert set(marked_q) <= rows                  # the marked rows rescale
+    assert len(rows - set(marked_q)) <= 8         # few others do
+    assert {(r // 128, (r % 128) // 32) for r in marked_q} == {(2, 1), (3, 0)}
+    dv = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    a = TPAttention(b, s, h, nq, nkv, d, n, causal=causal)
+    out = a.forward(dv["X"], dv["Wq"], dv["Wk"], dv["Wv"], dv["Wo"])
+    g = a.backward(dv["dOut"], dv["X"], dv["Wq"], dv["Wk"], dv["Wv"],
+                   dv["Wo"])
+    tp.device_status()
+    kw = dict(b=b, s=s, n_q=nq, n_kv=nkv, d=d, causal=causal)
+    fo = oracle.attention_forward(f["X"], f["Wq"], f["Wk"], f["Wv"], f["Wo"],
+                                  **kw)
+    go = oracle.attention_backward(f["dOut"], f["X"], f["Wq"], f["Wk"],
+                                   f["Wv"], f["Wo"], fo, **kw)
+    check(out, fo["Out"], "Out")
+    # the marked rows themselves, row by row, against the oracle
+    o = out.float().cpu().numpy()
+    ref = fo["Out"]
+    for r in marked_q:
+        err = np.abs(o[r] - ref[r]).max() / np.sqrt(np.mean(ref[r] ** 2))
+        assert err <= 3e-2, (r, err)
+    for k in ("dX", "dWq", "dWk", "dWv", "dWo"):
+        check_fro(g[k], go[k], k)
+
