@@ -347,3 +347,45 @@ def test_rescale_of_a_few_rows_of_one_tile(tp, causal):
     for k in ("dX", "dWq", "dWk", "dWv", "dWo"):
         check_fro(g[k], go[k], k)
 
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_growing_scores_odd_group(tp, causal):
+    # Three q heads per kv head: the forward pairs two consecutive query
+    # blocks of one head in a CTA, so under the causal mask the second tile
+    # goes on alone (one N=128 output product per block) after the first has
+    # ended, and s = 640 (five blocks) leaves the last CTA's second tile past
+    # the end.  Rows growing by 1 + t/256 make many rows take new reference
+    # maxima, some of them in the blocks where the second tile runs alone
+    # (CPU replay of the rule), with softmax rows less peaked than at
+    # 1 + t/128, whose nearly one-hot rows put dWq's rounding noise (D from
+    # the bf16 O) at the Frobenius bound.  Output to both bounds, gradients
+    # to the Frobenius bound.
+    b, s, h, nq, nkv, d, n = 1, 640, 1024, 12, 4, 128, 2
+    cfg = I.workload("attn_gqa_bf16", b=b, s=s, h=h, n_q=nq, n_kv=nkv, n=n,
+                     causal=causal, w_std="fan_in")
+    x = I.attn_inputs(cfg, 43, "cpu")
+    grow = 1.0 + np.arange(s) / 256.0
+    x["X"] = (x["X"].float() *
+              torch.from_numpy(np.tile(grow, b)).float()[:, None]).to(
+                  x["X"].dtype)
+    f = {k: I.to_f64(v) for k, v in x.items()}
+    ev = _rescale_events(f, cfg)
+    assert len({(j, r) for (j, r, _) in ev}) > s * nq // 4
+    if causal:
+        alone = [e for e in ev if (e[1] // 128) % 2 == 1 and e[2] == e[1] // 128]
+        assert len(alone) > 100
+    dv = {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+    a = TPAttention(b, s, h, nq, nkv, d, n, causal=causal)
+    out = a.forward(dv["X"], dv["Wq"], dv["Wk"], dv["Wv"], dv["Wo"])
+    g = a.backward(dv["dOut"], dv["X"], dv["Wq"], dv["Wk"], dv["Wv"],
+                   dv["Wo"])
+    tp.device_status()
+    kw = dict(b=b, s=s, n_q=nq, n_kv=nkv, d=d, causal=causal)
+    fo = oracle.attention_forward(f["X"], f["Wq"], f["Wk"], f["Wv"], f["Wo"],
+                                  **kw)
+    go = oracle.attention_backward(f["dOut"], f["X"], f["Wq"], f["Wk"],
+                                   f["Wv"], f["Wo"], fo, **kw)
+    check(out, fo["Out"], "Out")
+    for k in ("dX", "dWq", "dWk", "dWv", "dWo"):
+        check_fro(g[k], go[k], k)
+
