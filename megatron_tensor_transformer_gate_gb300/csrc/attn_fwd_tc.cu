@@ -203,7 +203,7 @@ __global__ void __maxnreg__(168)
   uint64_t* kv_empty = bar + 4;   // [NSLOT]
   uint64_t* s_full = bar + 7;     // [NT] S_t written
   uint64_t* s_free = bar + 9;     // [NT] S_t copied to registers
-  uint64_t* p_full = bar + 11;    // [NT] P_t written (and O_t rescaled)
+  uint64_t* p_full = bar + 11;    // [NT] P_t written (and Oᵀ rescaled)
   uint64_t* pv_done = bar + 13;   // [NT] Oᵀ += Vᵀ·P_tᵀ done (P_t free)
   uint64_t* drain = bar + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 16);
@@ -250,7 +250,7 @@ __global__ void __maxnreg__(168)
       // ------------------------------------------------------------- TMA --
       // The ring carries K_0, then K_{j+1} and V_j for each block j: a K
       // slot is released once both tiles' S MMAs have read it, a V slot once
-      // both O += P·V have.
+      // the output product has.
       tma_prefetch_desc(&a.mq);
       tma_prefetch_desc(&a.mk);
       tma_prefetch_desc(&a.mv);
