@@ -137,6 +137,18 @@ def test_group_size_extremes(tp, n_q, n_kv, n):
     run_case(tp, cfg, 0, 38)
 
 
+@pytest.mark.parametrize("n_q,n_kv", [(4, 2), (4, 4)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_sequences_shorter_than_a_block(tp, n_q, n_kv, causal):
+    # s = 77 < 128: one partial key block per sequence, three sequences; the
+    # forward's output rows past the end are clipped on store.  GQA group 2
+    # pairs two heads in a CTA; group 1 pairs query blocks, and the second
+    # one is past the end in every CTA
+    cfg = I.workload("attn_gqa_bf16", b=3, s=77, h=512, n_q=n_q, n_kv=n_kv,
+                     n=2, causal=causal, w_std="fan_in")
+    run_case(tp, cfg, 0, 44)
+
+
 @pytest.mark.parametrize("b,s", [(1, 384), (2, 500)])
 @pytest.mark.parametrize("causal", [True, False])
 def test_odd_group_size(tp, b, s, causal):
