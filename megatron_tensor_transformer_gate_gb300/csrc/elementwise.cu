@@ -619,6 +619,139 @@ __global__ void __launch_bounds__(512, 1)
                         dgacc + j * V);
 }
 
+// rmsnorm_bwd_kernel<T, NV, false> with the rows staged in shared memory:
+// one thread copies dy, x and dres (when given) of row r + 2 into one of two
+// stages by bulk copies while the block computes row r from the other, so
+// two rows of inputs are in flight per SM against one in the register form.
+// The arithmetic is the register form's, in the same order, so the results
+// are bit-identical to it.  Waits are bounded (site 34); the block agrees on
+// every outcome before it leaves the loop.
+template <typename T, int NV>
+__global__ void __launch_bounds__(512, 1)
+    rmsnorm_bwd_staged_kernel(const T* __restrict__ dy,
+                              const T* __restrict__ x,
+                              const T* __restrict__ gamma,
+                              const float* __restrict__ rstd,
+                              const T* __restrict__ dres, T* __restrict__ dx,
+                              float* __restrict__ dg_partial, int64_t rows,
+                              int64_t h, int64_t rpc, unsigned* status) {
+  constexpr int V = Vec<T>::N;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const int nin = dres != nullptr ? 3 : 2;   // rows a stage holds
+  T* const stage0 = reinterpret_cast<T*>(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(
+      smem_raw + (size_t)2 * nin * h * sizeof(T));   // [2]
+  __shared__ float red[2][16];
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int64_t col[NV];
+  bool on[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    col[j] = ((int64_t)threadIdx.x + 512 * j) * V;
+    on[j] = col[j] < h;
+  }
+  float dgacc[NV * V];
+#pragma unroll
+  for (int q = 0; q < NV * V; ++q) dgacc[q] = 0.0f;
+  const int64_t r_begin = (int64_t)blockIdx.x * rpc;
+  const int64_t r_end = min(rows, r_begin + rpc);
+  const uint32_t row_bytes = (uint32_t)(h * (int64_t)sizeof(T));
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // thread 0: dy, x (and dres) of row r into stage sg
+  auto issue = [&](int64_t r, int sg) {
+    T* st = stage0 + (int64_t)sg * nin * h;
+    mbar_arrive_expect_tx(&full[sg], (uint32_t)nin * row_bytes);
+    bulk_g2s(st, dy + r * h, row_bytes, &full[sg]);
+    bulk_g2s(st + h, x + r * h, row_bytes, &full[sg]);
+    if (nin == 3) bulk_g2s(st + 2 * h, dres + r * h, row_bytes, &full[sg]);
+  };
+  if (threadIdx.x == 0) {
+    if (r_begin < r_end) issue(r_begin, 0);
+    if (r_begin + 1 < r_end) issue(r_begin + 1, 1);
+  }
+  int64_t r = r_begin;
+  for (; r < r_end; ++r) {
+    const int64_t k = r - r_begin;
+    const int sg = (int)(k & 1);
+    const bool got =
+        mbar_wait(&full[sg], (uint32_t)((k >> 1) & 1),
+                  reinterpret_cast<volatile int*>(&abort_flag), status, 34);
+    if (!__syncthreads_and(got)) break;
+    const T* st = stage0 + (int64_t)sg * nin * h;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    float d[NV * V], xv[NV * V], g[NV * V];
+    uint4 cr[NV];   // this row's dres, raw 16-byte vectors
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const uint4 cd =
+          on[j] ? *reinterpret_cast<const uint4*>(st + col[j]) : zero;
+      const uint4 cx =
+          on[j] ? *reinterpret_cast<const uint4*>(st + h + col[j]) : zero;
+      cr[j] = (on[j] && nin == 3)
+                  ? *reinterpret_cast<const uint4*>(st + 2 * h + col[j])
+                  : zero;
+      Vec<T>::from_raw(cd, d + j * V);
+      Vec<T>::from_raw(cx, xv + j * V);
+    }
+    __syncthreads();   // stage sg consumed
+    if (threadIdx.x == 0 && r + 2 < r_end) issue(r + 2, sg);
+    const float rs = rstd[r];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      if (on[j]) {
+        Vec<T>::load(gamma + col[j], g + j * V);
+      } else {
+#pragma unroll
+        for (int q = 0; q < V; ++q) g[j * V + q] = 0.0f;
+      }
+    }
+    float dot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV * V; ++i) {
+      dot = fmaf(d[i] * g[i], xv[i], dot);
+      dgacc[i] = fmaf(d[i] * xv[i], rs, dgacc[i]);
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1)
+      dot += __shfl_xor_sync(0xffffffffu, dot, o2);
+    if (lane == 0) red[r & 1][w] = dot;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) tot += red[r & 1][i];
+    const float coef = rs * rs * rs * tot / (float)h;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      if (!on[j]) continue;
+      float o[V];
+      Vec<T>::from_raw(cr[j], o);
+#pragma unroll
+      for (int q = 0; q < V; ++q)
+        o[q] += rs * d[j * V + q] * g[j * V + q] - xv[j * V + q] * coef;
+      Vec<T>::store(dx + r * h + col[j], o);
+    }
+  }
+  if (r < r_end && threadIdx.x == 0) {
+    // gave up: let the copies of rows r and r + 1 land before the block exits
+    volatile int no_abort = 0;
+    for (int64_t k = r - r_begin; k < min(r_end - r_begin, r - r_begin + 2);
+         ++k)
+      mbar_wait(&full[k & 1], (uint32_t)((k >> 1) & 1), &no_abort, nullptr, 0);
+  }
+#pragma unroll
+  for (int j = 0; j < NV; ++j)
+    if (on[j])
+      Vec<T>::store_f32(dg_partial + (int64_t)blockIdx.x * h + col[j],
+                        dgacc + j * V);
+}
+
 // The g reduction with the next block's RMSNorm fused in (Megatron-SP
 // forward, [Troverld] §III.III: the reduce-scatter leaves each rank its rows
 // of the block output, the token-wise ops of the next block run on them, and
@@ -871,6 +1004,25 @@ int launch_rmsnorm_bwd_bulk(int chunks, size_t smem, cudaStream_t s,
   return cudaSuccess;
 }
 
+// The staged form of the plain backward: two stages of dy, x and dres rows
+// in shared memory, up to this many bytes.
+constexpr int64_t kStagedBytes = 200 * 1024;
+
+template <typename T, int NV>
+int launch_rmsnorm_bwd_staged(int chunks, size_t smem, cudaStream_t s,
+                              const T* dy, const T* x, const T* gamma,
+                              const float* rstd, const T* dres, T* dx,
+                              float* scratch, int64_t rows, int64_t h,
+                              int64_t rpc, unsigned* status) {
+  static cudaError_t attr = cudaFuncSetAttribute(
+      rmsnorm_bwd_staged_kernel<T, NV>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kStagedBytes + 64));
+  if (attr != cudaSuccess) return attr;
+  rmsnorm_bwd_staged_kernel<T, NV><<<chunks, 512, smem, s>>>(
+      dy, x, gamma, rstd, dres, dx, scratch, rows, h, rpc, status);
+  return cudaSuccess;
+}
+
 template <typename T>
 int rmsnorm_bwd_sum(const void* dy, int n, int64_t zstride, const void* x,
                     const void* gamma, const float* rstd, const void* dres,
@@ -898,7 +1050,24 @@ int rmsnorm_bwd_sum(const void* dy, int n, int64_t zstride, const void* x,
   rmsnorm_bwd_kernel<T, NVV, SUMV><<<chunks, 512, 0, s>>>(                    \
       dyp, n, zstride, xp, gp, rstd, rp, dxp, scratch, rows, h, rpc)
   const int64_t part_bytes = (int64_t)n * h * (int64_t)sizeof(T);
-  if (n > 1 && part_bytes <= kBulkRowBytes) {
+  const int64_t staged_bytes =
+      2 * (dres != nullptr ? 3 : 2) * h * (int64_t)sizeof(T) + 16;
+  if (n == 1 && staged_bytes <= kStagedBytes) {
+    int err;
+    if (sweeps <= 1)
+      err = launch_rmsnorm_bwd_staged<T, 1>(chunks, (size_t)staged_bytes, s,
+                                            dyp, xp, gp, rstd, rp, dxp,
+                                            scratch, rows, h, rpc, status);
+    else if (sweeps <= 2)
+      err = launch_rmsnorm_bwd_staged<T, 2>(chunks, (size_t)staged_bytes, s,
+                                            dyp, xp, gp, rstd, rp, dxp,
+                                            scratch, rows, h, rpc, status);
+    else
+      err = launch_rmsnorm_bwd_staged<T, 4>(chunks, (size_t)staged_bytes, s,
+                                            dyp, xp, gp, rstd, rp, dxp,
+                                            scratch, rows, h, rpc, status);
+    if (err) return err;
+  } else if (n > 1 && part_bytes <= kBulkRowBytes) {
     const size_t smem = (size_t)part_bytes + 16;
     int err;
     if (sweeps <= 1)
