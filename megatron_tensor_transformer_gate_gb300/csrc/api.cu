@@ -1416,14 +1416,10 @@ extern "C" tp_status tp_layer_fwd(const tp_layer_desc* d, const void* x,
       const int64_t qd = (int64_t)d->n_q * d->d, kd = (int64_t)d->n_kv * d->d;
       int err = rmsnorm_fwd<__nv_bfloat16>(x, g1, L.xn1, L.rstd1, T, h, d->eps,
                                            stream, L.xn1h, status);
-      char* wqkv = static_cast<char*>(L.wqkvh);
-      if (!err) err = convert_f16(Wq, wqkv, qd * h, status, stream);
-      if (!err)
-        err = convert_f16(Wk, wqkv + (size_t)qd * h * 2, kd * h, status,
-                          stream);
-      if (!err)
-        err = convert_f16(Wv, wqkv + (size_t)(qd + kd) * h * 2, kd * h,
-                          status, stream);
+      // [Wq; Wk; Wv] stacked in fp16, one launch
+      const void* wsrc[3] = {Wq, Wk, Wv};
+      const int64_t wn[3] = {qd * h, kd * h, kd * h};
+      if (!err) err = convert_f16(wsrc, wn, 3, L.wqkvh, status, stream);
       if (err) return cuda_status(err);
       QkvF16 f16in;
       f16in.x = L.xn1h;

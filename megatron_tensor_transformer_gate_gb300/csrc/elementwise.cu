@@ -305,18 +305,26 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------- bf16 → fp16 copy --
-// dst = fp16(src) over n elements (n a multiple of 8); a value beyond the
-// fp16 range records a range error.  bf16 values of magnitude below 2^-14
-// become fp16 subnormals (below 2^-24: zero).
+// dst = fp16(src_0 | src_1 | src_2): up to three bf16 arrays of n_i elements
+// (each a multiple of 8) converted into one contiguous fp16 array; a value
+// beyond the fp16 range records a range error.  bf16 values of magnitude
+// below 2^-14 become fp16 subnormals (below 2^-24: zero).
+struct F16Segments {
+  const __nv_bfloat16* src[3];
+  int64_t end[3];   // cumulative 8-element vectors after segment i
+};
+
 __global__ void __launch_bounds__(256)
-    convert_f16_kernel(const __nv_bfloat16* __restrict__ src,
-                       __half* __restrict__ dst, int64_t n, unsigned* status) {
+    convert_f16_kernel(const F16Segments sg, __half* __restrict__ dst,
+                       unsigned* status) {
   bool bad = false;
-  const int64_t nvec = n / 8;
+  const int64_t nvec = sg.end[2];
   for (int64_t iv = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; iv < nvec;
        iv += (int64_t)gridDim.x * blockDim.x) {
+    const int i = iv < sg.end[0] ? 0 : iv < sg.end[1] ? 1 : 2;
+    const int64_t base = i == 0 ? 0 : sg.end[i - 1];
     float v[8];
-    Vec<__nv_bfloat16>::load(src + iv * 8, v);
+    Vec<__nv_bfloat16>::load(sg.src[i] + (iv - base) * 8, v);
     uint32_t u[4];
 #pragma unroll
     for (int q = 0; q < 8; q += 2) {
@@ -962,14 +970,23 @@ int rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
   return cudaGetLastError();
 }
 
-int convert_f16(const void* src, void* dst, int64_t n, unsigned* status,
-                void* stream) {
-  if (n == 0) return cudaSuccess;
-  const int grid = grid_for(n / 8, 256);
-  ProfScope ps(stream, KF_ELEMENTWISE, 0.0, 4.0 * n);
+int convert_f16(const void* const* srcs, const int64_t* ns, int nseg,
+                void* dst, unsigned* status, void* stream) {
+  if (nseg < 1 || nseg > 3) return cudaErrorInvalidValue;
+  F16Segments sg;
+  int64_t tot = 0;
+  for (int i = 0; i < 3; ++i) {
+    const int64_t n = i < nseg ? ns[i] : 0;
+    if (n % 8) return cudaErrorInvalidValue;
+    sg.src[i] = i < nseg ? static_cast<const __nv_bfloat16*>(srcs[i]) : nullptr;
+    tot += n / 8;
+    sg.end[i] = tot;
+  }
+  if (tot == 0) return cudaSuccess;
+  const int grid = grid_for(tot, 256);
+  ProfScope ps(stream, KF_ELEMENTWISE, 0.0, 32.0 * tot);
   convert_f16_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(src), static_cast<__half*>(dst), n,
-      status);
+      sg, static_cast<__half*>(dst), status);
   count_launch();
   return cudaGetLastError();
 }

@@ -37,10 +37,11 @@ template <typename T>
 int rmsnorm_fwd(const void* x, const void* gamma, void* y, float* rstd,
                 int64_t rows, int64_t h, float eps, void* stream,
                 void* y16 = nullptr, unsigned* status = nullptr);
-// dst = fp16(src) for n bf16 values (n a multiple of 8, 16-byte aligned);
-// a value beyond the fp16 range records a range error in status.
-int convert_f16(const void* src, void* dst, int64_t n, unsigned* status,
-                void* stream);
+// dst = fp16 of nseg (1 to 3) bf16 arrays srcs[i] of ns[i] values (each a
+// multiple of 8, 16-byte aligned), one after another in one launch; a value
+// beyond the fp16 range records a range error in status.
+int convert_f16(const void* const* srcs, const int64_t* ns, int nseg,
+                void* dst, unsigned* status, void* stream);
 size_t rmsnorm_bwd_scratch(int64_t rows, int64_t h);
 template <typename T>
 int rmsnorm_bwd(const void* dy, const void* x, const void* gamma,
